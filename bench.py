@@ -1,0 +1,563 @@
+"""Benchmark of the paged-KV hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole path over one batch of synthetic input:
+copy_blocks (Copy-on-Write pairs, if any) -> reshape_and_cache (this step's
+new tokens) -> chunked prefill (if any) -> decode partial -> log-sum-exp merge,
+all on one stream with inputs resident in HBM.  The default workload is the
+Llama-8B-style GQA decode (batch 64, 32/8 heads, D=128, bs=16, contexts
+U{512..4096}); the others are selectable with --workload.
+
+Reported (one JSON line from rank 0):
+* value: algorithmic bytes of the step (KV + Q + O + block tables + lengths +
+  this step's cache writes) / step time, GB/s, summed over ranks (replicas);
+  decode_tokens_per_s alongside;
+* roofline: the dominant kernel (decode partial) timed with CUDA events on its
+  stream inside the timed region, against the measured HBM copy bandwidth;
+* cpu_baseline: the float64 CPU oracle on a bounded sample of the same
+  workload on this host (rank 0 only);
+* e2e: the same metric through the public API with host buffers: pinned host
+  -> device copies of the step's inputs and a device -> host read of its
+  outputs inside the timed region.
+``--impl reference`` times the CPU oracle itself as the reference arm.
+Multi-GPU: independent replicas (the path needs no collective); N>1 runs under
+torch.distributed.run with one rank per GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: achieved KV GB/s vs GB300 HBM peak; decode tokens/s"
+DEFAULT_WORKLOAD = "llama8b_gqa_decode"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic(profile_name: str, source_file: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(os.path.join(ROOT, source_file), "rb").read()).hexdigest()
+    if not cur.startswith(h.group(1)):
+        return None  # the kernel changed since the counters were taken
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload set-up
+class Step:
+    """Device buffers and host copies of one workload step; runs it through the C ABI."""
+
+    def __init__(self, wl: W.Workload, device: torch.device, value_seed: int):
+        from paged_kv_cache_76_gb300 import ops
+        from paged_kv_cache_76_gb300.allocator import BlockAllocator
+        self.ops = ops
+        self.wl = wl
+        self.dev = device
+        a = BlockAllocator(wl.num_blocks, wl.block_size, wl.free_order)
+        a.run(wl.setup_ops)
+        slots, pairs = a.run(wl.step_ops)
+        self.alloc = a
+        vals = W.make_values(wl, device=device, seed=value_seed)
+        self.vals = vals
+        self.k_cache, self.v_cache = vals["k_cache"], vals["v_cache"]
+        self.pre_k = None
+        self.h = {}   # pinned host copies of every per-step input
+        self.d = {}   # device copies
+        self.h["k_new"] = vals["k_new"].cpu().pin_memory()
+        self.h["v_new"] = vals["v_new"].cpu().pin_memory()
+        self.h["slots"] = torch.tensor(slots, dtype=torch.int32).pin_memory()
+        self.h["pairs"] = torch.tensor(pairs, dtype=torch.int32).reshape(-1, 2).pin_memory()
+        self.n_pairs = len(pairs)
+        self.dec = bool(wl.decode_seqs)
+        self.pre = bool(wl.prefill)
+        if self.dec:
+            maxblk = max(len(a.block_table(s)) for s in wl.decode_seqs)
+            t, l = a.build_tables(wl.decode_seqs, maxblk)
+            self.dec_lens = l.astype(np.int64)
+            self.dec_tables_np = t
+            self.h["dec_tables"] = torch.from_numpy(t).pin_memory()
+            self.h["dec_lens"] = torch.from_numpy(l).pin_memory()
+            self.h["q_decode"] = vals["q_decode"].cpu().pin_memory()
+            self.split = ops.decode_split_tokens(maxblk, wl.block_size, wl.split_tokens)
+            n = ops.decode_workspace_size(len(wl.decode_seqs), wl.q_heads, wl.head_dim, maxblk, wl.block_size,
+                                          self.split)
+            self.workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
+        if self.pre:
+            seqs = [s for s, _, _ in wl.prefill]
+            maxblk = max(len(a.block_table(s)) for s in seqs)
+            t, l = a.build_tables(seqs, maxblk)
+            self.pre_lens = l.astype(np.int64)
+            self.pre_tables_np = t
+            self.chunks = [c for _, c, _ in wl.prefill]
+            self.h["pre_tables"] = torch.from_numpy(t).pin_memory()
+            self.h["pre_lens"] = torch.from_numpy(l).pin_memory()
+            self.h["q_start"] = torch.tensor(np.concatenate([[0], np.cumsum(self.chunks)]),
+                                             dtype=torch.int32).pin_memory()
+            self.h["q_prefill"] = vals["q_prefill"].cpu().pin_memory()
+            self.max_q_len = max(self.chunks)
+        for k, v in self.h.items():
+            self.d[k] = v.to(device, non_blocking=False)
+        self.out_dec = torch.empty_like(self.d["q_decode"]) if self.dec else None
+        self.out_pre = torch.empty_like(self.d["q_prefill"]) if self.pre else None
+        self.h_out_dec = torch.empty(self.out_dec.shape, dtype=self.out_dec.dtype).pin_memory() if self.dec else None
+        self.h_out_pre = torch.empty(self.out_pre.shape, dtype=self.out_pre.dtype).pin_memory() if self.pre else None
+
+    # -- one step through the C ABI; ev = (start, end) events around the decode partial kernel
+    def run(self, stream, ev=None):
+        o, d, wl = self.ops, self.d, self.wl
+        if self.n_pairs:
+            o.copy_blocks(self.k_cache, self.v_cache, d["pairs"], stream=stream)
+        o.reshape_and_cache(d["k_new"], d["v_new"], d["slots"], self.k_cache, self.v_cache, stream=stream)
+        if self.pre:
+            o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
+                              d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=stream)
+        if self.dec:
+            if ev is not None:
+                ev[0].record(stream)
+            o.decode_partial(d["q_decode"], self.k_cache, self.v_cache, d["dec_tables"], d["dec_lens"], wl.scale,
+                             self.out_dec, split_tokens=self.split, workspace=self.workspace, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            o.lse_merge(self.workspace, d["dec_lens"], d["q_decode"], d["dec_tables"], wl.block_size, self.out_dec,
+                        split_tokens=self.split, stream=stream)
+
+    def run_e2e(self, stream):
+        """Host buffers in, host buffers out: copies inside the step."""
+        for k, v in self.h.items():
+            if v.numel():
+                self.d[k].copy_(v, non_blocking=True)
+        self.run(stream)
+        if self.dec:
+            self.h_out_dec.copy_(self.out_dec, non_blocking=True)
+        if self.pre:
+            self.h_out_pre.copy_(self.out_pre, non_blocking=True)
+
+    def e2e_bytes(self):
+        h2d = sum(v.numel() * v.element_size() for v in self.h.values())
+        d2h = 0
+        if self.dec:
+            d2h += self.h_out_dec.numel() * self.h_out_dec.element_size()
+        if self.pre:
+            d2h += self.h_out_pre.numel() * self.h_out_pre.element_size()
+        return h2d, d2h
+
+    # -- algorithmic bytes
+    def bytes_breakdown(self):
+        wl = self.wl
+        e = 2
+        tok = wl.kv_heads * wl.head_dim * e          # one token's K (or V), all KV heads
+        qrow = wl.q_heads * wl.head_dim * e
+        bs = wl.block_size
+        out = {}
+        if self.dec:
+            L = self.dec_lens
+            out["decode"] = int(np.sum(2 * L * tok + 2 * qrow + 4 * np.ceil(L / bs) + 4))
+            used = {}
+            for r, Lr in enumerate(L):
+                for j in range(int(math.ceil(Lr / bs))):
+                    b = int(self.dec_tables_np[r, j])
+                    used[b] = max(used.get(b, 0), min(bs, int(Lr) - j * bs))
+            out["decode_unique"] = int(sum(used.values()) * 2 * tok + np.sum(2 * qrow + 4 * np.ceil(L / bs) + 4))
+        T = int(self.h["slots"].numel())
+        out["reshape_and_cache"] = T * (4 * tok + 4)
+        out["copy_blocks"] = self.n_pairs * (4 * bs * tok + 8)
+        if self.pre:
+            L = self.pre_lens
+            ch = np.asarray(self.chunks)
+            out["prefill"] = int(np.sum(2 * L * tok + 2 * ch * qrow + 4 * np.ceil(L / bs) + 8))
+            vis = sum(sum(int(L[i]) - int(ch[i]) + q + 1 for q in range(int(ch[i]))) for i in range(len(ch)))
+            out["prefill_flops"] = 4 * vis * wl.q_heads * wl.head_dim
+        return out
+
+
+# ----------------------------------------------------------------------------- the CPU oracle on a sample
+def oracle_units(step: Step):
+    """(kind, request index, kv head) units of the step, in a fixed order."""
+    wl = step.wl
+    units = []
+    if step.dec:
+        units += [("decode", r, g) for r in range(len(wl.decode_seqs)) for g in range(wl.kv_heads)]
+    if step.pre:
+        units += [("prefill", r, g) for r in range(len(wl.prefill)) for g in range(wl.kv_heads)]
+    return units
+
+
+def _unit_inputs(step: Step, unit, token_index):
+    """Host float64 inputs of one unit: its request's blocks for one KV head (not timed)."""
+    kind, r, g = unit
+    wl = step.wl
+    bs, G = wl.block_size, wl.q_heads // wl.kv_heads
+    if kind == "decode":
+        table = step.dec_tables_np[r]
+        L = int(step.dec_lens[r])
+        q = step.h["q_decode"][r, g * G:(g + 1) * G][None]
+    else:
+        table = step.pre_tables_np[r]
+        L = int(step.pre_lens[r])
+        a, b = int(step.h["q_start"][r]), int(step.h["q_start"][r + 1])
+        q = step.h["q_prefill"][a:b, g * G:(g + 1) * G]
+    nblk = int(math.ceil(L / bs))
+    ids = torch.as_tensor(table[:nblk].astype(np.int64), device=step.dev)
+    kc = step.vals["k_cache"][ids][:, :, g:g + 1].float().cpu().double().numpy()
+    vc = step.vals["v_cache"][ids][:, :, g:g + 1].float().cpu().double().numpy()
+    # this step's new tokens that land in these blocks (remapped to the sub-pool)
+    slots = step.h["slots"].numpy()
+    pos = {int(b): i for i, b in enumerate(table[:nblk])}
+    sel, sub = [], []
+    for i, s in enumerate(slots):
+        if s >= 0 and int(s) // bs in pos:
+            sel.append(i)
+            sub.append(pos[int(s) // bs] * bs + int(s) % bs)
+    kn = step.h["k_new"][sel][:, g:g + 1].double().numpy() if sel else np.zeros((0, 1, wl.head_dim))
+    vn = step.h["v_new"][sel][:, g:g + 1].double().numpy() if sel else np.zeros((0, 1, wl.head_dim))
+    return dict(q=q.double().numpy(), kc=kc, vc=vc, kn=kn, vn=vn, slots=np.asarray(sub, np.int64),
+                table=np.arange(nblk)[None], L=L, chunk=(q.shape[0] if kind == "prefill" else 1))
+
+
+def _unit_bytes(step: Step, unit):
+    kind, r, g = unit
+    wl = step.wl
+    e, D, G, bs = 2, wl.head_dim, wl.q_heads // wl.kv_heads, wl.block_size
+    if kind == "decode":
+        L = int(step.dec_lens[r])
+        return 2 * L * D * e + 2 * G * D * e + (4 * math.ceil(L / bs) + 4) / wl.kv_heads
+    L = int(step.pre_lens[r])
+    c = step.chunks[r]
+    return 2 * L * D * e + 2 * c * G * D * e + (4 * math.ceil(L / bs) + 8) / wl.kv_heads
+
+
+def run_oracle_units(step: Step, units, budget_s: float):
+    """Time the oracle (as it stands) on units until the budget is spent."""
+    from oracle import paged_attention as opa
+    wl = step.wl
+    done_bytes, t_oracle, done = 0.0, 0.0, []
+    cpu0 = time.process_time()
+    for u in units:
+        x = _unit_inputs(step, u, 0)
+        t0 = time.perf_counter()
+        kc, vc = opa.reshape_and_cache(x["kn"], x["vn"], x["slots"], x["kc"], x["vc"])
+        if u[0] == "decode":
+            opa.decode(x["q"], kc, vc, x["table"], [x["L"]], wl.scale)
+        else:
+            opa.chunked_prefill(x["q"], [0, x["chunk"]], [x["L"]], kc, vc, x["table"], wl.scale)
+        t_oracle += time.perf_counter() - t0
+        done_bytes += _unit_bytes(step, u)
+        done.append(u)
+        if t_oracle >= budget_s:
+            break
+    cpu = time.process_time() - cpu0
+    return done_bytes, t_oracle, done, cpu
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+
+    if args.impl == "reference" and rank != 0:
+        torch.distributed.destroy_process_group()   # the reference arm runs on rank 0 alone
+        return
+    from paged_kv_cache_76_gb300 import _lib
+    _lib.lib()  # fails loudly if the CUDA library is missing
+
+    wl = W.WORKLOADS[args.workload]()
+    step = Step(wl, device, value_seed=1000 * rank)
+    peak, peak_kind = measured_peaks()
+
+    if args.impl == "reference":
+        return reference_arm(args, step, ws, rank, peak)
+
+    stream = torch.cuda.Stream(device)
+    nb = step.bytes_breakdown()
+    total_bytes = sum(v for k, v in nb.items() if k not in ("decode_unique", "prefill_flops"))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step.run(stream)
+    stream.synchronize()
+    from paged_kv_cache_76_gb300 import ops
+    if ops.get_device_error(stream) != 0:
+        raise RuntimeError("device error recorded during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if ws == 1 else local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = ops.launch_count()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            step.run(stream, evs[i] if step.dec else None)
+        t_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    launches = ops.launch_count() - launches0
+    clk = clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    ms = t_start.elapsed_time(t_end)
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs])) if step.dec else None
+    if ops.get_device_error(stream) != 0:
+        raise RuntimeError("device error recorded during the timed region")
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    ms_per_step = ms / args.steps
+
+    # e2e: host buffers through the public API
+    e2e_val = None
+    h2d, d2h = step.e2e_bytes()
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            step.run_e2e(stream)
+    stream.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.e2e_steps):
+            step.run_e2e(stream)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], dtype=torch.float64, device=device)
+    if ws > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_s = float(te.item())
+    e2e_val = ws * total_bytes * args.e2e_steps / e2e_s / 1e9
+
+    value = ws * total_bytes / (ms_per_step * 1e-3) / 1e9
+    n_dec = len(wl.decode_seqs)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded; N(0,1) or U[-1,1] per workload)",
+        "decode_tokens_per_s": round(ws * n_dec / (ms_per_step * 1e-3), 1) if n_dec else None,
+        "config": {
+            "workload": wl.name,
+            "batch": n_dec,
+            "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "head_dim": wl.head_dim,
+            "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+            "context_lens": [int(min(step.dec_lens)), int(max(step.dec_lens))] if n_dec else None,
+            "mean_context": float(np.mean(step.dec_lens)) if n_dec else None,
+            "split_tokens": step.split if n_dec else None,
+            "prefill_chunks": step.chunks if step.pre else None,
+            "copy_pairs": step.n_pairs,
+            "bytes_per_step": nb,
+            "l2": f"inputs larger than L2: {total_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2",
+            "parallelism": f"replicas x{ws}",
+        },
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if step.dec:
+        dec_bytes = nb["decode"]
+        achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+        traffic = kernel_traffic(f"decode_partial_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/decode.cu")
+        res["roofline"] = {
+            "kernel": "decode_partial_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": dec_bytes,
+            "avg_launch_ms": round(dec_ms, 5),
+        }
+        if "decode_unique" in nb and nb["decode_unique"] < dec_bytes:
+            res["roofline"]["unique_bytes_per_launch"] = nb["decode_unique"]
+            res["roofline"]["achieved_unique"] = round(nb["decode_unique"] / (dec_ms * 1e-3) / 1e9, 1)
+            res["roofline"]["frac_unique"] = round(nb["decode_unique"] / (dec_ms * 1e-3) / 1e9 / peak, 4)
+    res["e2e"] = {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                  "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+                  "ms_per_step": round(e2e_s / args.e2e_steps * 1e3, 4)}
+    if rank == 0 and not args.no_cpu_baseline:
+        units = oracle_units(step)
+        b, t_or, done, cpu = run_oracle_units(step, units, args.cpu_budget)
+        res["cpu_baseline"] = {
+            "value": round(b / t_or / 1e9, 6), "unit": "GB/s",
+            "cores": max(1, int(round(cpu / max(t_or, 1e-9)))),
+            "kind": "oracle",
+            "sample": f"{len(done)} of {len(units)} (request, kv-head) units of {wl.name}, "
+                      f"first {len(done)} in order; {t_or:.1f} s of float64 NumPy oracle",
+            "host_cores_available": len(os.sched_getaffinity(0)),
+        }
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+def reference_arm(args, step, ws, rank, peak):
+    """The reference arm: the float64 CPU oracle, a bounded sample per step."""
+    units = oracle_units(step)
+    per_step = max(1, len(units) // 64)
+    # steps = per_step units each, rotating through the workload
+    k = 0
+    for _ in range(args.warmup):
+        run_oracle_units(step, [units[(k + i) % len(units)] for i in range(per_step)], 1e9)
+        k += per_step
+    tot_b, tot_t, cpu_t, n_units = 0.0, 0.0, 0.0, 0
+    for _ in range(args.steps):
+        us = [units[(k + i) % len(units)] for i in range(per_step)]
+        b, t, done, cpu = run_oracle_units(step, us, 1e9)
+        tot_b += b
+        tot_t += t
+        cpu_t += cpu
+        n_units += len(done)
+        k += per_step
+        if tot_t > 150:
+            break
+    val = tot_b / tot_t / 1e9
+    res = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(val, 6),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(tot_t / max(1, n_units // per_step) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": step.wl.name, "units_per_step": per_step,
+                   "note": "each step is a bounded sample of the workload: per_step (request, kv-head) units"},
+        "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "kind": "oracle",
+                         "cores": max(1, int(round(cpu_t / max(tot_t, 1e-9)))),
+                         "sample": f"{n_units} (request, kv-head) units of {step.wl.name}"},
+        "e2e": {"value": round(val, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

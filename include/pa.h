@@ -1,0 +1,278 @@
+/*
+ * pa.h - C ABI of a paged-KV-cache attention library for NVIDIA GB300 (sm_103a).
+ *
+ * The KV cache is split into fixed-size physical blocks of `block_size` tokens;
+ * a request's logical blocks map to physical blocks through its Block Table,
+ * so its KV need not be contiguous ("2.1 PagedAttention", §2-§3).  Attention
+ * kernels translate each logical token t into (physical_block_number =
+ * table[t / block_size], physical_block_offset = t % block_size) (§5).
+ *
+ * Conventions for every call below
+ * --------------------------------
+ * - Cache layout: k_cache and v_cache are separate tensors, each
+ *   [num_blocks][block_size][kv_heads][head_dim], row-major, contiguous.
+ * - Block tables: int32 [num_seqs][max_blocks_per_seq], row-major; entries
+ *   past a request's last logical block are never read (any value).
+ * - Element types: PA_FP16 or PA_BF16 for q/k/v/out (inputs and outputs in the
+ *   same type); accumulation and softmax are fp32.
+ * - head_dim in {64, 128}; block_size in {4, 8, 16, 32};
+ *   q_heads % kv_heads == 0 and q_heads / kv_heads <= 16.  Query head h reads
+ *   KV head h / (q_heads / kv_heads) (contiguous GQA groups).
+ * - Device calls: every pointer is device memory owned by the caller; the
+ *   library allocates no device memory and keeps no pointer after returning.
+ *   Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream).  All device pointers must be 16-byte aligned.
+ * - Errors: every call returns a pa_status.  Argument errors are caught on the
+ *   host before anything is launched.  Data errors that only the device can
+ *   see (a block id outside [0, num_blocks), a slot past the pool, a context
+ *   length past the table, a wait that timed out) never fault or trap: the
+ *   kernel records the first such code in a per-device error word, skips the
+ *   offending access, and finishes; read it with pa_get_device_error().
+ *   Nothing aborts, nothing throws.
+ * - Thread safety: device calls may be made from any host thread.  A pa_alloc
+ *   handle is single-threaded.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = -1,        /* bad argument (shape, pointer, id, range)        */
+  PA_ERR_NO_FREE_BLOCKS = -2, /* pool exhausted; allocator state unchanged      */
+  PA_ERR_DTYPE = -3,          /* unsupported element type                       */
+  PA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed              */
+  PA_ERR_DEVICE_CHECK = -5,   /* pa_get_device_error found a recorded error     */
+  PA_ERR_SHARED_BLOCK = -6,   /* append into a shared partial block: cow first  */
+  PA_ERR_WORKSPACE = -7       /* workspace missing or smaller than required     */
+} pa_status;
+
+typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Device error codes recorded by kernels (first one wins). */
+enum {
+  PA_DEVERR_NONE = 0,
+  PA_DEVERR_BLOCK_ID = 1,     /* block-table entry or copy pair outside [0, num_blocks) */
+  PA_DEVERR_CONTEXT_LEN = 2,  /* context length < 0 or > max_blocks_per_seq*block_size */
+  PA_DEVERR_SLOT = 3,         /* slot_mapping entry >= num_blocks*block_size            */
+  PA_DEVERR_TIMEOUT = 4,      /* a bounded wait on a shared-memory barrier expired      */
+  PA_DEVERR_QUERY_RANGE = 5   /* bad q_start / chunk length in chunked prefill          */
+};
+
+typedef struct CUstream_st* pa_stream; /* identical to cudaStream_t */
+
+/* Human-readable name of a pa_status value (static string). */
+const char* pa_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pa_version(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pa_launch_count(void);
+
+/* ----------------------------------------------------------------------------
+ * pa_reshape_and_cache - scatter new tokens' K/V into their slots.
+ *
+ * "2.1 PagedAttention" §3: each new token fills the next free slot of its
+ * request's current block; the forward pass writes the KV into the blocks the
+ * allocator handed out ("Khám phá vLLM … phần 2", prefix caching).  For token
+ * i with slot s = slot_mapping[i] >= 0:
+ *     k_cache[s / block_size][s % block_size][:][:] = k[i][:][:]   (same for v)
+ * A negative slot marks a padding token and is skipped.  The copy is
+ * bit-exact.
+ *   k, v          [num_tokens][kv_heads][head_dim], contiguous
+ *   slot_mapping  int32 [num_tokens]; slots must be distinct
+ *   k_cache,v_cache  the pool (see conventions)
+ * num_tokens == 0 is a no-op.  A slot >= num_blocks*block_size records
+ * PA_DEVERR_SLOT and is skipped.
+ * ------------------------------------------------------------------------- */
+int pa_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mapping, int num_tokens,
+                         void* k_cache, void* v_cache, int num_blocks, int block_size, int kv_heads,
+                         int head_dim, pa_dtype dtype, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
+ * pa_copy_blocks - the device half of Copy-on-Write.
+ *
+ * "2.1 PagedAttention" §6: before a request writes a block other requests
+ * share, the block is copied to a private block and the request's table
+ * entry is repointed (the allocator's pa_alloc_cow does the bookkeeping).
+ * For each pair p: block pairs[2p+1] (dst) of k_cache and v_cache becomes a
+ * bit-exact copy of block pairs[2p] (src).
+ *   pairs  int32 [num_pairs][2] (src, dst), DEVICE memory.  A dst must not
+ *          repeat nor be the src of another pair (otherwise the result is
+ *          unspecified).  Ids outside [0, num_blocks) record
+ *          PA_DEVERR_BLOCK_ID and the pair is skipped.
+ * num_pairs == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
+                   int block_size, int kv_heads, int head_dim, pa_dtype dtype, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
+ * Paged decode attention (one query token per request).
+ *
+ * "2.1 PagedAttention" §3 and §5: the kernel reads the request's whole KV
+ * history from scattered physical blocks through its Block Table.  For
+ * request r and query head h (g = h / (q_heads / kv_heads)):
+ *     s_t = scale * <q[r][h], K_r[t][g]>           for t < context_lens[r]
+ *     out[r][h] = sum_t softmax(s)_t * V_r[t][g]
+ * context_lens[r] counts every token of the request, including the one this
+ * step wrote with pa_reshape_and_cache.  A zero context gives a zero row.
+ *
+ * The context is processed in partitions of `split_tokens` tokens (0 = the
+ * library's choice).  pa_decode_split_tokens returns the partition size a
+ * call with these arguments uses, or PA_ERR_INVALID if split_tokens is not
+ * allowed.  A request with one
+ * partition is written straight to `out`; a request with more keeps per
+ * partition the unnormalised output and its running max and sum, and
+ * pa_lse_merge combines them:  M = max_c m_c,  out = sum_c e^(m_c-M) o_c /
+ * sum_c e^(m_c-M) l_c.
+ *
+ *   q             [num_seqs][q_heads][head_dim]
+ *   out           [num_seqs][q_heads][head_dim]
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens  int32 [num_seqs], each in [0, max_blocks_per_seq*block_size]
+ *   split_tokens  0, or a multiple of max(16, block_size) no larger than
+ *                 256*block_size
+ *   workspace     device scratch of at least pa_decode_workspace_size(...)
+ *                 bytes (may be NULL when that size is 0).  Owned by the
+ *                 caller; its contents need no initialisation.
+ * pa_decode = pa_decode_partial followed by pa_lse_merge on the same stream.
+ * ------------------------------------------------------------------------- */
+int pa_decode_split_tokens(int max_blocks_per_seq, int block_size, int split_tokens);
+
+size_t pa_decode_workspace_size(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq,
+                                int block_size, int split_tokens);
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_heads,
+              int kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+              int split_tokens, void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype,
+              pa_stream stream);
+
+/* First half of pa_decode: per-partition partials (or the final row for
+ * requests with a single partition). Same arguments as pa_decode. */
+int pa_decode_partial(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads,
+                      int head_dim, int block_size, int num_blocks, float scale, int split_tokens,
+                      void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype,
+                      pa_stream stream);
+
+/* Second half of pa_decode: log-sum-exp merge of the partials of every request
+ * with more than one partition.  Arguments must match the pa_decode_partial
+ * call whose workspace it reads. */
+int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* context_lens,
+                 int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq, int block_size,
+                 int split_tokens, void* out, pa_dtype dtype, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
+ * pa_chunked_prefill - a chunk of prompt tokens per request attends its paged
+ * history plus itself, causally.
+ *
+ * "Khám phá vLLM … phần 2", chunked prefill: a long prompt is prefilled a
+ * bounded number of tokens per engine step; the chunk's K/V are written to the
+ * cache first (pa_reshape_and_cache) and its queries attend everything before
+ * them.  Request r's queries are rows q_start[r] .. q_start[r+1]-1 of q;
+ * context_lens[r] includes the chunk, so the chunk starts at absolute
+ * position p0 = context_lens[r] - chunk and query i sees keys 0 .. p0 + i.
+ *   q, out        [total_q][q_heads][head_dim]
+ *   q_start       int32 [num_reqs + 1], non-decreasing, q_start[num_reqs] <= total_q
+ *   max_q_len     host-side upper bound of any chunk length (sizes the grid)
+ * A chunk longer than max_q_len or a context shorter than its chunk records
+ * PA_DEVERR_QUERY_RANGE and that request is skipped.
+ * ------------------------------------------------------------------------- */
+int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* context_lens,
+                       const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                       int max_blocks_per_seq, int num_reqs, int total_q, int max_q_len,
+                       int q_heads, int kv_heads, int head_dim, int block_size, int num_blocks,
+                       float scale, void* out, pa_dtype dtype, pa_stream stream);
+
+/* Read and clear the calling device's error word.  Synchronises `stream`.
+ * *host_code receives the PA_DEVERR_* code (0 = none).  Returns
+ * PA_ERR_DEVICE_CHECK if a code was recorded, PA_OK otherwise. */
+int pa_get_device_error(int32_t* host_code, pa_stream stream);
+
+/* ============================================================================
+ * Host block allocator ("2.1 PagedAttention" §9.1-§9.3, §3, §6).
+ *
+ * A pool of num_blocks physical blocks with a reference count each and a free
+ * queue kept as a doubly linked list (O(1) pop from the head, O(1) removal
+ * from the middle).  Sequences own Block Tables that grow a block at a time,
+ * only when the last block is full.  Tables may share blocks (refcount =
+ * number of tables holding the block); a sequence about to write a shared
+ * block copies it first (pa_alloc_cow).  Freeing a sequence releases its
+ * blocks in reverse order; blocks whose count reaches zero go to the HEAD of
+ * the free queue in that order, so a request's last block is reused first.
+ * Freed blocks keep their contents (no clearing).
+ *
+ * Every call is all-or-nothing: on error the state is unchanged.  Handles are
+ * single-threaded.  Sequence ids are any non-negative int.
+ * ========================================================================== */
+typedef struct pa_alloc pa_alloc;
+
+typedef struct {
+  int64_t num_blocks;
+  int64_t num_free;
+  int64_t num_used;        /* blocks with refcount > 0                        */
+  int64_t num_shared;      /* blocks with refcount > 1                        */
+  int64_t num_seqs;
+  int64_t cow_copies;      /* pa_alloc_cow calls that produced a copy          */
+  int64_t alloc_failures;  /* calls that returned PA_ERR_NO_FREE_BLOCKS        */
+  int64_t waste_slots;     /* sum over sequences of unused slots in the last block */
+} pa_alloc_stats;
+
+/* initial_free_order: NULL for ascending ids, else a permutation of
+ * 0..num_blocks-1 giving the initial free-queue order (head first). */
+int pa_alloc_create(int num_blocks, int block_size, const int32_t* initial_free_order, pa_alloc** out);
+void pa_alloc_destroy(pa_alloc* a);
+
+int pa_alloc_add_seq(pa_alloc* a, int seq_id);
+
+/* Give the next n_tokens tokens of seq_id their slots (slots_out[i] =
+ * block*block_size + offset), taking new blocks from the head of the free
+ * queue only as the last block fills.  PA_ERR_NO_FREE_BLOCKS if the pool
+ * cannot cover them; PA_ERR_SHARED_BLOCK if the partially filled last block is
+ * shared (call pa_alloc_cow first).  slots_out may be NULL. */
+int pa_alloc_append_slots(pa_alloc* a, int seq_id, int n_tokens, int32_t* slots_out);
+
+/* dst_seq (empty) starts with the first n_tokens tokens of src_seq: its table
+ * points at src's first ceil(n_tokens/block_size) blocks, each refcount +1. */
+int pa_alloc_share(pa_alloc* a, int dst_seq, int src_seq, int n_tokens);
+
+/* Make seq_id's logical block private.  If its refcount is 1, src_dst_out =
+ * {b, b} and nothing changes.  Otherwise a fresh block n is taken from the
+ * free queue, the table entry becomes n, b's refcount drops by one, and
+ * src_dst_out = {b, n}: the caller must then run pa_copy_blocks on (b, n). */
+int pa_alloc_cow(pa_alloc* a, int seq_id, int logical_block, int32_t* src_dst_out);
+
+int pa_alloc_free_seq(pa_alloc* a, int seq_id);
+
+/* Copy seq_id's Block Table into out[0..cap); *n_out = its length.
+ * PA_ERR_INVALID if cap is too small (nothing written). */
+int pa_alloc_block_table(const pa_alloc* a, int seq_id, int32_t* out, int cap, int* n_out);
+
+/* Fill a padded batch table: out is [n][max_blocks_per_seq], row i = table of
+ * seq_ids[i] padded with -1; lens_out[i] = its token count (may be NULL). */
+int pa_alloc_build_tables(const pa_alloc* a, const int* seq_ids, int n, int32_t* out,
+                          int max_blocks_per_seq, int32_t* lens_out);
+
+int pa_alloc_seq_len(const pa_alloc* a, int seq_id, int64_t* n_tokens_out);
+int pa_alloc_num_free(const pa_alloc* a);
+/* Refcount of block_id, or PA_ERR_INVALID if it is out of range. */
+int pa_alloc_ref(const pa_alloc* a, int block_id);
+/* Free-queue snapshot head to tail into out[0..cap); returns the number
+ * written, or PA_ERR_INVALID if cap < the queue length. */
+int pa_alloc_free_list(const pa_alloc* a, int32_t* out, int cap);
+int pa_alloc_get_stats(const pa_alloc* a, pa_alloc_stats* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -206,7 +206,7 @@ def decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, split_t
     return out
 
 
-def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, scale):
+def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, scale, rows=None):
     """Attention of a chunk of queries per request over its paged history.
 
     "Khám phá vLLM … phần 2", chunked prefill: a long prompt is processed a
@@ -215,6 +215,8 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
     ``q_start[r] .. q_start[r+1]-1`` of ``q`` ([T, q_heads, D]);
     ``context_lens[r]`` includes the chunk, so the chunk starts at
     p0 = context_lens[r] - chunk and query i sees keys 0 .. p0 + i.
+    ``rows`` optionally restricts the work to those rows of ``q`` (the others
+    stay zero), for sampled checks of large inputs.
     """
     q = np.asarray(q, dtype=np.float64)
     T, Hq, D = q.shape
@@ -223,6 +225,7 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
     group = Hq // Hkv
     out = np.zeros((T, Hq, D))
     R = len(q_start) - 1
+    wanted = None if rows is None else set(int(x) for x in rows)
     for r in range(R):
         a, b = int(q_start[r]), int(q_start[r + 1])
         chunk = b - a
@@ -233,6 +236,8 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
         K = gather_context(k_cache, block_tables[r], L, bs)
         V = gather_context(v_cache, block_tables[r], L, bs)
         for i in range(chunk):
+            if wanted is not None and a + i not in wanted:
+                continue
             visible = p0 + i + 1
             for h in range(Hq):
                 g = h // group

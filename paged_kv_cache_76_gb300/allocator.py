@@ -1,0 +1,134 @@
+"""Python handle over the C++ block allocator (``pa_alloc_*`` in include/pa.h)."""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from . import _lib
+from ._lib import PA_ERR_NO_FREE_BLOCKS, PAError, check
+
+__all__ = ["BlockAllocator", "NoFreeBlocks"]
+
+
+class NoFreeBlocks(PAError):
+    """The pool cannot cover the request; the allocator state is unchanged."""
+
+
+def _chk(st, what):
+    if st == PA_ERR_NO_FREE_BLOCKS:
+        raise NoFreeBlocks(st, what)
+    return check(st, what)
+
+
+def _i32p(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+class BlockAllocator:
+    """Free queue + refcounts + per-sequence Block Tables, in C++."""
+
+    def __init__(self, num_blocks: int, block_size: int, initial_free_order=None):
+        self._L = _lib.lib()
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        h = C.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+            if order.shape != (self.num_blocks,):
+                raise ValueError("initial_free_order must list every block once")
+        _chk(self._L.pa_alloc_create(self.num_blocks, self.block_size,
+                                     _i32p(order) if order is not None else None, C.byref(h)),
+             "pa_alloc_create")
+        self._h = h
+        self._order_keepalive = order
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._L.pa_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, seq: int):
+        _chk(self._L.pa_alloc_add_seq(self._h, int(seq)), "pa_alloc_add_seq")
+
+    def append_slots(self, seq: int, n: int) -> np.ndarray:
+        out = np.empty(int(n), dtype=np.int32)
+        _chk(self._L.pa_alloc_append_slots(self._h, int(seq), int(n), _i32p(out)), "pa_alloc_append_slots")
+        return out
+
+    def share(self, dst: int, src: int, n_tokens: int):
+        _chk(self._L.pa_alloc_share(self._h, int(dst), int(src), int(n_tokens)), "pa_alloc_share")
+
+    def cow(self, seq: int, logical_block: int):
+        out = np.empty(2, dtype=np.int32)
+        _chk(self._L.pa_alloc_cow(self._h, int(seq), int(logical_block), _i32p(out)), "pa_alloc_cow")
+        return int(out[0]), int(out[1])
+
+    def free_seq(self, seq: int):
+        _chk(self._L.pa_alloc_free_seq(self._h, int(seq)), "pa_alloc_free_seq")
+
+    def block_table(self, seq: int) -> list:
+        n = C.c_int(0)
+        self._L.pa_alloc_block_table(self._h, int(seq), None, 0, C.byref(n))
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _chk(self._L.pa_alloc_block_table(self._h, int(seq), _i32p(out), out.shape[0], C.byref(n)),
+             "pa_alloc_block_table")
+        return out[:n.value].tolist()
+
+    def build_tables(self, seqs, max_blocks_per_seq: int):
+        ids = np.ascontiguousarray(seqs, dtype=np.int32).astype(np.intc)
+        n = ids.shape[0]
+        tables = np.empty((n, int(max_blocks_per_seq)), dtype=np.int32)
+        lens = np.empty(n, dtype=np.int32)
+        _chk(self._L.pa_alloc_build_tables(self._h, ids.ctypes.data_as(C.POINTER(C.c_int)), n, _i32p(tables),
+                                           int(max_blocks_per_seq), _i32p(lens)), "pa_alloc_build_tables")
+        return tables, lens
+
+    def seq_len(self, seq: int) -> int:
+        v = C.c_int64(0)
+        _chk(self._L.pa_alloc_seq_len(self._h, int(seq), C.byref(v)), "pa_alloc_seq_len")
+        return int(v.value)
+
+    def num_free(self) -> int:
+        return _chk(self._L.pa_alloc_num_free(self._h), "pa_alloc_num_free")
+
+    def ref(self, block: int) -> int:
+        return _chk(self._L.pa_alloc_ref(self._h, int(block)), "pa_alloc_ref")
+
+    def free_list(self) -> list:
+        out = np.empty(self.num_blocks, dtype=np.int32)
+        n = _chk(self._L.pa_alloc_free_list(self._h, _i32p(out), self.num_blocks), "pa_alloc_free_list")
+        return out[:n].tolist()
+
+    def stats(self) -> dict:
+        s = _lib.AllocStats()
+        _chk(self._L.pa_alloc_get_stats(self._h, C.byref(s)), "pa_alloc_get_stats")
+        return {name: int(getattr(s, name)) for name, _ in s._fields_}
+
+    def run(self, ops):
+        """Replay an allocator script (see ``workloads``); returns (slots, cow pairs)."""
+        slots, pairs = [], []
+        for op in ops:
+            kind = op[0]
+            if kind == "add":
+                self.add_seq(op[1])
+            elif kind == "append":
+                slots.extend(self.append_slots(op[1], op[2]).tolist())
+            elif kind == "share":
+                self.share(op[1], op[2], op[3])
+            elif kind == "cow":
+                s, d = self.cow(op[1], op[2])
+                if s != d:
+                    pairs.append((s, d))
+            elif kind == "free":
+                self.free_seq(op[1])
+            else:
+                raise ValueError(f"unknown op {kind}")
+        return slots, pairs

@@ -1,0 +1,272 @@
+// Host block allocator of the paged KV cache (C ABI: pa_alloc_* in pa.h).
+//
+// Design ("2.1 PagedAttention" §9.1-§9.3, §3, §6):
+//  * a global pool of physical blocks, each with a reference count (number of
+//    Block Tables holding it);
+//  * a free queue kept as an intrusive doubly linked list over block ids
+//    (prev/next int32 arrays): pop from the head and removal from the middle
+//    are O(1), as the free queue in §9.2 requires;
+//  * per-sequence Block Tables that grow one block at a time, only when the
+//    last block is full (§3: nothing is reserved ahead);
+//  * sharing (many tables point at one block) and Copy-on-Write (§6);
+//  * release in reverse order; zero-count blocks go to the head of the queue
+//    in that order (the free_blocks rule of §9.3 for blocks without a prefix
+//    hash), so the tail block of a finished request is reused first.
+// Every entry point validates first and mutates only once success is certain.
+#include <algorithm>
+#include <cstdint>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "pa.h"
+
+namespace {
+
+struct Seq {
+  std::vector<int32_t> blocks;
+  int64_t num_tokens = 0;
+};
+
+}  // namespace
+
+struct pa_alloc {
+  int32_t num_blocks = 0;
+  int32_t block_size = 0;
+  std::vector<int32_t> ref;
+  std::vector<int32_t> prev, next;  // free-queue links, -1 = none
+  std::vector<uint8_t> in_free;
+  int32_t head = -1, tail = -1, num_free = 0;
+  std::unordered_map<int, Seq> seqs;
+  int64_t cow_copies = 0;
+  int64_t alloc_failures = 0;
+
+  void push_back(int32_t b) {
+    prev[b] = tail;
+    next[b] = -1;
+    if (tail < 0) head = b; else next[tail] = b;
+    tail = b;
+    in_free[b] = 1;
+    ++num_free;
+  }
+  void push_front(int32_t b) {
+    next[b] = head;
+    prev[b] = -1;
+    if (head < 0) tail = b; else prev[head] = b;
+    head = b;
+    in_free[b] = 1;
+    ++num_free;
+  }
+  void unlink(int32_t b) {
+    int32_t p = prev[b], n = next[b];
+    if (p < 0) head = n; else next[p] = n;
+    if (n < 0) tail = p; else prev[n] = p;
+    prev[b] = next[b] = -1;
+    in_free[b] = 0;
+    --num_free;
+  }
+  // popleft: caller has checked num_free > 0
+  int32_t pop_front() {
+    int32_t b = head;
+    unlink(b);
+    return b;
+  }
+  Seq* find(int id) {
+    auto it = seqs.find(id);
+    return it == seqs.end() ? nullptr : &it->second;
+  }
+  const Seq* find(int id) const {
+    auto it = seqs.find(id);
+    return it == seqs.end() ? nullptr : &it->second;
+  }
+};
+
+static inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+extern "C" {
+
+int pa_alloc_create(int num_blocks, int block_size, const int32_t* initial_free_order, pa_alloc** out) {
+  if (!out || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID;
+  *out = nullptr;
+  if (initial_free_order) {
+    std::vector<uint8_t> seen(num_blocks, 0);
+    for (int i = 0; i < num_blocks; ++i) {
+      int32_t b = initial_free_order[i];
+      if (b < 0 || b >= num_blocks || seen[b]) return PA_ERR_INVALID;
+      seen[b] = 1;
+    }
+  }
+  pa_alloc* a = new (std::nothrow) pa_alloc();
+  if (!a) return PA_ERR_INVALID;
+  a->num_blocks = num_blocks;
+  a->block_size = block_size;
+  a->ref.assign(num_blocks, 0);
+  a->prev.assign(num_blocks, -1);
+  a->next.assign(num_blocks, -1);
+  a->in_free.assign(num_blocks, 0);
+  for (int i = 0; i < num_blocks; ++i) a->push_back(initial_free_order ? initial_free_order[i] : i);
+  *out = a;
+  return PA_OK;
+}
+
+void pa_alloc_destroy(pa_alloc* a) { delete a; }
+
+int pa_alloc_add_seq(pa_alloc* a, int seq_id) {
+  if (!a || seq_id < 0 || a->find(seq_id)) return PA_ERR_INVALID;
+  a->seqs.emplace(seq_id, Seq());
+  return PA_OK;
+}
+
+int pa_alloc_append_slots(pa_alloc* a, int seq_id, int n_tokens, int32_t* slots_out) {
+  if (!a || n_tokens < 0) return PA_ERR_INVALID;
+  Seq* s = a->find(seq_id);
+  if (!s) return PA_ERR_INVALID;
+  const int64_t bs = a->block_size;
+  const int64_t cur = s->num_tokens;
+  if (n_tokens > 0 && cur % bs != 0 && a->ref[s->blocks.back()] > 1) return PA_ERR_SHARED_BLOCK;
+  const int64_t need = cdiv64(cur + n_tokens, bs) - (int64_t)s->blocks.size();
+  if (need > a->num_free) {
+    ++a->alloc_failures;
+    return PA_ERR_NO_FREE_BLOCKS;
+  }
+  if ((cur + n_tokens) * 1 > (int64_t)INT32_MAX) return PA_ERR_INVALID;
+  for (int64_t i = 0; i < need; ++i) {
+    int32_t b = a->pop_front();
+    a->ref[b] += 1;  // was 0: every queued block is unreferenced
+    s->blocks.push_back(b);
+  }
+  if (slots_out) {
+    for (int64_t t = cur; t < cur + n_tokens; ++t)
+      slots_out[t - cur] = (int32_t)((int64_t)s->blocks[t / bs] * bs + t % bs);
+  }
+  s->num_tokens = cur + n_tokens;
+  return PA_OK;
+}
+
+int pa_alloc_share(pa_alloc* a, int dst_seq, int src_seq, int n_tokens) {
+  if (!a || dst_seq == src_seq) return PA_ERR_INVALID;
+  Seq* d = a->find(dst_seq);
+  Seq* s = a->find(src_seq);
+  if (!d || !s || !d->blocks.empty() || d->num_tokens != 0) return PA_ERR_INVALID;
+  if (n_tokens < 0 || n_tokens > s->num_tokens) return PA_ERR_INVALID;
+  const int64_t nblk = cdiv64(n_tokens, a->block_size);
+  d->blocks.assign(s->blocks.begin(), s->blocks.begin() + nblk);
+  for (int32_t b : d->blocks) {
+    if (a->ref[b] == 0 && a->in_free[b]) a->unlink(b);  // touch: revive a free block
+    a->ref[b] += 1;
+  }
+  d->num_tokens = n_tokens;
+  return PA_OK;
+}
+
+int pa_alloc_cow(pa_alloc* a, int seq_id, int logical_block, int32_t* src_dst_out) {
+  if (!a || !src_dst_out) return PA_ERR_INVALID;
+  Seq* s = a->find(seq_id);
+  if (!s || logical_block < 0 || logical_block >= (int)s->blocks.size()) return PA_ERR_INVALID;
+  const int32_t b = s->blocks[logical_block];
+  if (a->ref[b] == 1) {
+    src_dst_out[0] = src_dst_out[1] = b;
+    return PA_OK;
+  }
+  if (a->num_free < 1) {
+    ++a->alloc_failures;
+    return PA_ERR_NO_FREE_BLOCKS;
+  }
+  const int32_t n = a->pop_front();
+  a->ref[n] = 1;
+  a->ref[b] -= 1;
+  s->blocks[logical_block] = n;
+  ++a->cow_copies;
+  src_dst_out[0] = b;
+  src_dst_out[1] = n;
+  return PA_OK;
+}
+
+int pa_alloc_free_seq(pa_alloc* a, int seq_id) {
+  if (!a) return PA_ERR_INVALID;
+  auto it = a->seqs.find(seq_id);
+  if (it == a->seqs.end()) return PA_ERR_INVALID;
+  const std::vector<int32_t>& blocks = it->second.blocks;
+  // reverse order: tail block first; zero-count blocks are prepended keeping
+  // that order, i.e. pushed to the front from the last of them to the first
+  std::vector<int32_t> to_free;
+  to_free.reserve(blocks.size());
+  for (auto rit = blocks.rbegin(); rit != blocks.rend(); ++rit) {
+    a->ref[*rit] -= 1;
+    if (a->ref[*rit] == 0) to_free.push_back(*rit);
+  }
+  for (auto rit = to_free.rbegin(); rit != to_free.rend(); ++rit) a->push_front(*rit);
+  a->seqs.erase(it);
+  return PA_OK;
+}
+
+int pa_alloc_block_table(const pa_alloc* a, int seq_id, int32_t* out, int cap, int* n_out) {
+  if (!a) return PA_ERR_INVALID;
+  const Seq* s = a->find(seq_id);
+  if (!s) return PA_ERR_INVALID;
+  const int n = (int)s->blocks.size();
+  if (n_out) *n_out = n;
+  if (n > cap || (n > 0 && !out)) return PA_ERR_INVALID;
+  std::copy(s->blocks.begin(), s->blocks.end(), out);
+  return PA_OK;
+}
+
+int pa_alloc_build_tables(const pa_alloc* a, const int* seq_ids, int n, int32_t* out,
+                          int max_blocks_per_seq, int32_t* lens_out) {
+  if (!a || n < 0 || max_blocks_per_seq < 0 || (n > 0 && (!seq_ids || !out))) return PA_ERR_INVALID;
+  for (int i = 0; i < n; ++i) {
+    const Seq* s = a->find(seq_ids[i]);
+    if (!s || (int64_t)s->blocks.size() > max_blocks_per_seq || s->num_tokens > INT32_MAX)
+      return PA_ERR_INVALID;
+  }
+  for (int i = 0; i < n; ++i) {
+    const Seq* s = a->find(seq_ids[i]);
+    int32_t* row = out + (int64_t)i * max_blocks_per_seq;
+    std::copy(s->blocks.begin(), s->blocks.end(), row);
+    std::fill(row + s->blocks.size(), row + max_blocks_per_seq, -1);
+    if (lens_out) lens_out[i] = (int32_t)s->num_tokens;
+  }
+  return PA_OK;
+}
+
+int pa_alloc_seq_len(const pa_alloc* a, int seq_id, int64_t* n_tokens_out) {
+  if (!a || !n_tokens_out) return PA_ERR_INVALID;
+  const Seq* s = a->find(seq_id);
+  if (!s) return PA_ERR_INVALID;
+  *n_tokens_out = s->num_tokens;
+  return PA_OK;
+}
+
+int pa_alloc_num_free(const pa_alloc* a) { return a ? a->num_free : PA_ERR_INVALID; }
+
+int pa_alloc_ref(const pa_alloc* a, int block_id) {
+  if (!a || block_id < 0 || block_id >= a->num_blocks) return PA_ERR_INVALID;
+  return a->ref[block_id];
+}
+
+int pa_alloc_free_list(const pa_alloc* a, int32_t* out, int cap) {
+  if (!a || cap < a->num_free || (a->num_free > 0 && !out)) return PA_ERR_INVALID;
+  int i = 0;
+  for (int32_t b = a->head; b >= 0; b = a->next[b]) out[i++] = b;
+  return i;
+}
+
+int pa_alloc_get_stats(const pa_alloc* a, pa_alloc_stats* out) {
+  if (!a || !out) return PA_ERR_INVALID;
+  pa_alloc_stats st{};
+  st.num_blocks = a->num_blocks;
+  st.num_free = a->num_free;
+  for (int32_t r : a->ref) {
+    if (r > 0) ++st.num_used;
+    if (r > 1) ++st.num_shared;
+  }
+  st.num_seqs = (int64_t)a->seqs.size();
+  st.cow_copies = a->cow_copies;
+  st.alloc_failures = a->alloc_failures;
+  for (const auto& kv : a->seqs)
+    st.waste_slots += (int64_t)kv.second.blocks.size() * a->block_size - kv.second.num_tokens;
+  *out = st;
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// KV-cache writes for sm_103a: reshape_and_cache (scatter new tokens into
+// their slots) and copy_blocks (the device half of Copy-on-Write).
+//
+// Both are pure data movement bound by HBM bandwidth.  With the cache layout
+// [num_blocks][block_size][kv_heads][head_dim], one token's K for all KV heads
+// is one contiguous row of kv_heads*head_dim elements in the source and in its
+// slot, so reshape_and_cache is a row gather/scatter of 16-byte vectors, and a
+// whole physical block is one contiguous span that copy_blocks moves with
+// 16-byte vectors.  Both copy bits, never values, so they are bit-exact.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Grid-stride over (token, 16-byte vector of the token's row).
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                             const int32_t* __restrict__ slots, uint4* __restrict__ k_cache,
+                             uint4* __restrict__ v_cache, int num_tokens, int row_vecs, int64_t num_slots,
+                             int* err) {
+  const int64_t total = (int64_t)num_tokens * row_vecs;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tok = i / row_vecs;
+    const int64_t j = i - tok * row_vecs;
+    const int32_t s = __ldg(slots + tok);
+    if (s < 0) continue;  // padding token
+    if (s >= num_slots) {
+      if (j == 0) record_error(err, PA_DEVERR_SLOT);
+      continue;
+    }
+    const uint4 kv = ld_stream(k + i);
+    const uint4 vv = ld_stream(v + i);
+    k_cache[(int64_t)s * row_vecs + j] = kv;
+    v_cache[(int64_t)s * row_vecs + j] = vv;
+  }
+}
+
+// blockIdx.y strides over pairs; x threads over the block's 16-byte vectors.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ pairs,
+                       int num_pairs, int64_t block_vecs, int num_blocks, int* err) {
+  for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
+    const int src = __ldg(pairs + 2 * pi), dst = __ldg(pairs + 2 * pi + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+      continue;
+    }
+    const uint4* ks = k_cache + (int64_t)src * block_vecs;
+    const uint4* vs = v_cache + (int64_t)src * block_vecs;
+    uint4* kd = k_cache + (int64_t)dst * block_vecs;
+    uint4* vd = v_cache + (int64_t)dst * block_vecs;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < block_vecs;
+         i += (int64_t)gridDim.x * blockDim.x) {
+      const uint4 a = ks[i];
+      const uint4 b = vs[i];
+      kd[i] = a;
+      vd[i] = b;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
+                                     void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,
+                                     cudaStream_t stream) {
+  const int row_vecs = row_bytes / 16;
+  const int64_t total = (int64_t)num_tokens * row_vecs;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), num_tokens, row_vecs, num_slots, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
+                               int64_t block_bytes, int* err, cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int64_t block_vecs = block_bytes / 16;
+  int64_t bx = (block_vecs + 255) / 256;
+  if (bx > 8) bx = 8;
+  const int by = num_pairs < 65535 ? num_pairs : 65535;
+  copy_blocks_kernel<<<dim3((unsigned)bx, by), 256, 0, stream>>>(static_cast<uint4*>(k_cache),
+                                                                  static_cast<uint4*>(v_cache), pairs, num_pairs,
+                                                                  block_vecs, num_blocks, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,449 @@
+// Paged decode attention for sm_103a: context-split partial kernel and the
+// log-sum-exp merge.
+//
+// Work decomposition.  One warp owns one (request r, KV head h, partition c)
+// unit and walks the partition's tokens in tiles of 16 (one bs=16 block, or
+// 16/bs blocks for smaller blocks), in logical order.  A CTA holds WARPS
+// consecutive units of one request (for 8 KV heads and 4 warps: four heads of
+// one partition), so neighbouring heads of the same physical block are read
+// by the same CTA at about the same time.  Each warp has its own ring of
+// STAGES shared-memory stages fed by TMA (cp.async.bulk.tensor) behind a
+// per-warp copy of the partition's Block Table slice: the warp issues the
+// loads of tile j+STAGES as soon as it has consumed tile j, so up to STAGES
+// tiles per warp are in flight while it computes.
+//
+// Math per tile (GQA: the whole query-head group shares every K/V tile):
+//   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]       mma.m16n8k16, D/16 k-steps
+//   online softmax per head column (running max in log2 units, running sum)
+//   P^T -> bf16/fp16, transposed in registers with movmatrix into the B
+//   fragment of   O^T[D x 8] += V^T[D x 16 tok] . P^T[16 x 8]   (D/16 m-tiles)
+// Tokens past the context are masked to -inf in S and their V rows are zeroed
+// in shared memory, so stale data in a partially filled block (NaN included)
+// never reaches the output.  All reduction orders depend only on logical
+// positions, so relabelling physical blocks gives bitwise-identical results.
+#include <cuda_pipeline.h>
+#include <float.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 3;
+constexpr int kMaxTableEntries = 256;  // per warp: split_tokens / block_size <= 256
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES>
+struct DecodeSmem {
+  using Tile = KvTile<D, BSUB, 16>;
+  static constexpr int STAGE_BYTES = 2 * Tile::BYTES;  // K tile then V tile
+  static constexpr int WARP_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = WARPS * WARP_BYTES;
+  static constexpr int TAB_OFF = BAR_OFF + WARPS * STAGES * 8;
+  static constexpr int BYTES = TAB_OFF + WARPS * kMaxTableEntries * 4 + 1024;  // + alignment slack
+};
+
+template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+    decode_partial_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          const DecodeParams p) {
+  using L = DecodeSmem<D, BSUB, NT, T, WARPS, STAGES>;
+  using Tile = typename L::Tile;
+  constexpr int KSTEPS = D / 16;
+  constexpr int LOADS = Tile::NH * 2;  // TMA boxes per sub-block: halves x {K, V}
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint8_t* wbase = smem + warp * L::WARP_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * STAGES;
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF) + warp * kMaxTableEntries;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  __syncthreads();  // the only CTA-wide barrier; warps are independent below
+
+  const int r = blockIdx.y;
+  const int u = blockIdx.x * WARPS + warp;
+  const int h = u % p.kv_heads;
+  const int c = u / p.kv_heads;
+  const int cap = p.maxblk * p.block_size;
+  int ctx = __ldg(p.lens + r);
+  if (ctx < 0 || ctx > cap) {
+    if (lane == 0) record_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    ctx = ctx < 0 ? 0 : cap;
+  }
+  const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
+  if (c >= (nsplit > 0 ? nsplit : 1)) return;
+
+  const int G = p.group;
+  const int qh0 = h * G;
+  T* out = reinterpret_cast<T*>(p.out);
+  if (ctx == 0) {
+    T* o = out + ((size_t)r * p.q_heads + qh0) * D;
+    for (int i = lane; i < G * D; i += 32) o[i] = Elem<T>::from(0.f);
+    return;
+  }
+
+  const int tok0 = c * p.split_tokens;
+  const int tok1 = min(tok0 + p.split_tokens, ctx);
+  const int ntiles = (tok1 - tok0 + 15) >> 4;
+  const int blk0 = tok0 / p.block_size;
+  const int nblk = (tok1 - 1) / p.block_size - blk0 + 1;
+
+  // Block Table slice of this partition; an out-of-range id is recorded and
+  // replaced by num_blocks, whose rows lie past the tensor map: TMA then
+  // zero-fills instead of reading anything.
+  const int32_t* trow = p.tables + (size_t)r * p.maxblk + blk0;
+  for (int i = lane; i < nblk; i += 32) {
+    int b = __ldg(trow + i);
+    if (b < 0 || b >= p.num_blocks) {
+      record_error(p.err, PA_DEVERR_BLOCK_ID);
+      b = p.num_blocks;
+    }
+    tab[i] = b;
+  }
+
+  // Q^T as the B operand of S^T = K Q^T: lane holds head (lane/4) of each
+  // 8-head n-tile, elements d = 16ks + 2(lane%4) + {0,1} and +8.
+  uint32_t qf[NT][KSTEPS][2];
+  {
+    const T* qb = reinterpret_cast<const T*>(p.q) + ((size_t)r * p.q_heads + qh0) * D;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int hd = nt * 8 + (lane >> 2);
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int d = ks * 16 + 2 * (lane & 3);
+        if (hd < G) {
+          qf[nt][ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + hd * D + d));
+          qf[nt][ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + hd * D + d + 8));
+        } else {
+          qf[nt][ks][0] = 0u;
+          qf[nt][ks][1] = 0u;
+        }
+      }
+    }
+  }
+  __syncwarp();
+
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int j) {
+    const int s = j % STAGES;
+    const int ts = tok0 + 16 * j;
+    const int nvalid = min(16, tok1 - ts);
+    const int nsub = (nvalid + BSUB - 1) / BSUB;
+    const uint32_t bar = smem_u32(&bars[s]);
+    const uint32_t kdst = smem_u32(wbase + s * L::STAGE_BYTES);
+    fence_proxy_async_smem();  // earlier generic reads/writes of this stage before the async writes
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(bar, nsub * LOADS * Tile::BOX_BYTES);
+    __syncwarp();
+    if (lane < nsub * LOADS) {
+      const int sub = lane / LOADS;
+      const int rem = lane % LOADS;
+      const int isv = rem / Tile::NH;
+      const int hf = rem % Tile::NH;
+      const int tok = ts + sub * BSUB;
+      const int b = tab[tok / p.block_size - blk0];
+      const int row = b * p.block_size + tok % p.block_size;
+      tma_load_4d_hint(kdst + isv * Tile::BYTES + Tile::box(hf, sub), isv ? &vmap : &kmap, bar, 0, hf, h, row,
+                       pol);
+    }
+  };
+
+  float m[NT][2], lp[NT][2];
+  float acc[NT][KSTEPS][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m[nt][0] = m[nt][1] = -INFINITY;
+    lp[nt][0] = lp[nt][1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
+  }
+
+  const int npro = ntiles < STAGES ? ntiles : STAGES;
+  for (int j = 0; j < npro; ++j) issue(j);
+
+  const float sl2 = p.scale_log2;
+  const int mi = lane >> 3, rr = lane & 7;
+  const int r0 = lane >> 2;
+  bool failed = false;
+  int j = 0;
+  for (; j < ntiles; ++j) {
+    const int s = j % STAGES;
+    if (!mbar_wait(smem_u32(&bars[s]), (j / STAGES) & 1)) {
+      failed = true;
+      break;
+    }
+    const int ts = tok0 + 16 * j;
+    const int nvalid = min(16, tok1 - ts);
+    uint8_t* kt = wbase + s * L::STAGE_BYTES;
+    uint8_t* vt = kt + Tile::BYTES;
+    if (nvalid < 16) {
+      // rows past the context: zero V so that p = 0 never meets stale NaN/Inf
+      const int nz = (16 - nvalid) * Tile::NH * 8;
+      for (int i = lane; i < nz; i += 32) {
+        const int row = nvalid + i / (Tile::NH * 8);
+        const int rem = i % (Tile::NH * 8);
+        *reinterpret_cast<uint4*>(vt + Tile::line(rem >> 3, row) + ((rem & 7) << 4)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    const uint32_t kts = smem_u32(kt), vts = smem_u32(vt);
+
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      uint32_t a[4];
+      ldmatrix_x4(a, kts + Tile::offset(rr + 8 * (mi & 1), 2 * ks + (mi >> 1)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816<T>(sacc[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+    }
+
+    uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float s0 = r0 < nvalid ? sacc[nt][0] * sl2 : -INFINITY;
+      const float s1 = r0 < nvalid ? sacc[nt][1] * sl2 : -INFINITY;
+      const float s2 = r0 + 8 < nvalid ? sacc[nt][2] * sl2 : -INFINITY;
+      const float s3 = r0 + 8 < nvalid ? sacc[nt][3] * sl2 : -INFINITY;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+      const float al0 = exp2f(m[nt][0] - mn0), al1 = exp2f(m[nt][1] - mn1);
+      m[nt][0] = mn0;
+      m[nt][1] = mn1;
+      const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+      const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+      lp[nt][0] = lp[nt][0] * al0 + (p0 + p2);
+      lp[nt][1] = lp[nt][1] * al1 + (p1 + p3);
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        acc[nt][mt][0] *= al0;
+        acc[nt][mt][1] *= al1;
+        acc[nt][mt][2] *= al0;
+        acc[nt][mt][3] *= al1;
+      }
+      pb0[nt] = movmatrix_trans(Elem<T>::pack(p0, p1));
+      pb1[nt] = movmatrix_trans(Elem<T>::pack(p2, p3));
+    }
+
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vts + Tile::offset(rr + 8 * (mi >> 1), 2 * mt + (mi & 1)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816<T>(acc[nt][mt], a, pb0[nt], pb1[nt]);
+    }
+    __syncwarp();
+    if (j + STAGES < ntiles) issue(j + STAGES);
+  }
+
+  if (failed) {
+    if (lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
+    // drain this warp's loads still in flight (bounded) before leaving
+    for (int k = j + 1; k < ntiles && k < j + STAGES; ++k) mbar_wait(smem_u32(&bars[k % STAGES]), (k / STAGES) & 1);
+    return;
+  }
+
+  // finish the per-head sums across the 8 lanes holding each column
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l = lp[nt][e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      lp[nt][e] = l;
+    }
+
+  if (nsplit == 1) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int hd = nt * 8 + 2 * (lane & 3) + e;
+        if (hd < G) {
+          const float inv = lp[nt][e] > 0.f ? 1.f / lp[nt][e] : 0.f;
+          T* o = out + ((size_t)r * p.q_heads + qh0 + hd) * D;
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            o[mt * 16 + r0] = Elem<T>::from(acc[nt][mt][e] * inv);
+            o[mt * 16 + r0 + 8] = Elem<T>::from(acc[nt][mt][2 + e] * inv);
+          }
+        }
+      }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int hd = nt * 8 + 2 * (lane & 3) + e;
+        if (hd < G) {
+          const size_t row = (size_t)r * p.q_heads + qh0 + hd;
+          float* po = p.part_o + (row * p.max_splits + c) * D;
+#pragma unroll
+          for (int mt = 0; mt < KSTEPS; ++mt) {
+            po[mt * 16 + r0] = acc[nt][mt][e];
+            po[mt * 16 + r0 + 8] = acc[nt][mt][2 + e];
+          }
+          if (r0 == 0) {
+            p.part_m[row * p.max_splits + c] = m[nt][e];
+            p.part_l[row * p.max_splits + c] = lp[nt][e];
+          }
+        }
+      }
+  }
+}
+
+// One warp per (request, query head): combine the partitions of requests that
+// have more than one.  M = max_c m_c; w_c = 2^(m_c - M);
+// out = sum_c w_c o_c / sum_c w_c l_c, partitions in logical order.
+template <int D, typename T>
+__global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
+  constexpr int V = D / 32;
+  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.num_seqs * p.q_heads) return;
+  const int r = wid / p.q_heads;
+  int ctx = __ldg(p.lens + r);
+  ctx = ctx < 0 ? 0 : (ctx > p.cap ? p.cap : ctx);
+  const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
+  if (nsplit <= 1) return;
+  const float* pm = p.part_m + (size_t)wid * p.max_splits;
+  const float* pl = p.part_l + (size_t)wid * p.max_splits;
+  const float* po = p.part_o + (size_t)wid * p.max_splits * D + lane * V;
+  float M = -INFINITY;
+  for (int c = lane; c < nsplit; c += 32) M = fmaxf(M, pm[c]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float a[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) a[i] = 0.f;
+  float den = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < nsplit; ++c) {
+    const float w = exp2f(pm[c] - M);
+    den += w * pl[c];
+    if constexpr (V == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(po + (size_t)c * D);
+      a[0] += w * x.x;
+      a[1] += w * x.y;
+      a[2] += w * x.z;
+      a[3] += w * x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(po + (size_t)c * D);
+      a[0] += w * x.x;
+      a[1] += w * x.y;
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  T* o = reinterpret_cast<T*>(p.out) + (size_t)wid * D + lane * V;
+#pragma unroll
+  for (int i = 0; i < V; i += 2) *reinterpret_cast<uint32_t*>(o + i) = Elem<T>::pack(a[i] * inv, a[i + 1] * inv);
+}
+
+template <int D, int BSUB, int NT, typename T>
+cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                            cudaStream_t stream) {
+  constexpr int W = kDecodeWarps, S = kDecodeStages;
+  using L = DecodeSmem<D, BSUB, NT, T, W, S>;
+  auto kern = decode_partial_kernel<D, BSUB, NT, T, W, S>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int units = p.max_splits * p.kv_heads;
+  dim3 grid((units + W - 1) / W, p.num_seqs);
+  kern<<<grid, W * 32, L::BYTES, stream>>>(kmap, vmap, p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <int D, int BSUB, typename T>
+cudaError_t launch_decode_nt(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                             cudaStream_t stream) {
+  if (p.group <= 8) return launch_decode_t<D, BSUB, 1, T>(kmap, vmap, p, stream);
+  return launch_decode_t<D, BSUB, 2, T>(kmap, vmap, p, stream);
+}
+
+template <int D, typename T>
+cudaError_t launch_decode_bs(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p, int bsub,
+                             cudaStream_t stream) {
+  switch (bsub) {
+    case 4: return launch_decode_nt<D, 4, T>(kmap, vmap, p, stream);
+    case 8: return launch_decode_nt<D, 8, T>(kmap, vmap, p, stream);
+    case 16: return launch_decode_nt<D, 16, T>(kmap, vmap, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                                  int head_dim, int bsub, pa_dtype dt, cudaStream_t stream) {
+  if (head_dim == 128) {
+    return dt == PA_BF16 ? launch_decode_bs<128, __nv_bfloat16>(kmap, vmap, p, bsub, stream)
+                         : launch_decode_bs<128, __half>(kmap, vmap, p, bsub, stream);
+  }
+  if (head_dim == 64) {
+    return dt == PA_BF16 ? launch_decode_bs<64, __nv_bfloat16>(kmap, vmap, p, bsub, stream)
+                         : launch_decode_bs<64, __half>(kmap, vmap, p, bsub, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream) {
+  const int rows = p.num_seqs * p.q_heads;
+  dim3 grid((rows + 3) / 4);
+  if (head_dim == 128) {
+    if (dt == PA_BF16) lse_merge_kernel<128, __nv_bfloat16><<<grid, 128, 0, stream>>>(p);
+    else lse_merge_kernel<128, __half><<<grid, 128, 0, stream>>>(p);
+  } else if (head_dim == 64) {
+    if (dt == PA_BF16) lse_merge_kernel<64, __nv_bfloat16><<<grid, 128, 0, stream>>>(p);
+    else lse_merge_kernel<64, __half><<<grid, 128, 0, stream>>>(p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+DecodeWorkspace decode_workspace_layout(int num_seqs, int q_heads, int head_dim, int max_splits) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  DecodeWorkspace w{};
+  const size_t rows = (size_t)num_seqs * q_heads * max_splits;
+  w.o_off = 0;
+  w.m_off = al(rows * head_dim * sizeof(float));
+  w.l_off = w.m_off + al(rows * sizeof(float));
+  w.bytes = w.l_off + al(rows * sizeof(float));
+  return w;
+}
+
+}  // namespace pa

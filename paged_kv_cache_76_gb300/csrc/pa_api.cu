@@ -1,0 +1,376 @@
+// C ABI of the paged-KV library: argument checks, TMA descriptor cache,
+// per-device error word, and the launches (see include/pa.h for the contract).
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// Per-device error word: kernels record the first data error here.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+constexpr int kAutoSplitTokens = 512;
+
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+// Device address of the error word on the current device (set up once).
+int* device_error_ptr() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<int*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// Small cache of KV tensor maps keyed by (pointer, shape, dtype, device).
+struct MapKey {
+  const void* ptr;
+  int64_t rows;
+  int kv_heads, head_dim, bsub, dtype, dev;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && kv_heads == o.kv_heads && head_dim == o.head_dim &&
+           bsub == o.bsub && dtype == o.dtype && dev == o.dev;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  uint64_t stamp;
+  bool used;
+};
+constexpr int kMapCache = 32;
+MapEntry g_maps[kMapCache];
+uint64_t g_stamp = 0;
+
+// 4-D view of a cache tensor: {64, head_dim/64, kv_heads, num_blocks*block_size}
+// elements, boxes {64, 1, 1, bsub}, 128-byte swizzle.
+bool kv_map(const void* base, int num_blocks, int block_size, int kv_heads, int head_dim, pa_dtype dt,
+            CUtensorMap* out) {
+  const int bsub = block_size < 16 ? block_size : 16;
+  const int64_t rows = (int64_t)num_blocks * block_size;
+  MapKey key{base, rows, kv_heads, head_dim, bsub, (int)dt, current_device()};
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto& e : g_maps)
+      if (e.used && e.key == key) {
+        e.stamp = ++g_stamp;
+        *out = e.map;
+        return true;
+      }
+  }
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)kv_heads, (cuuint64_t)rows};
+  cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * 2, (cuuint64_t)kv_heads * head_dim * 2};
+  cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)bsub};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMap m;
+  CUresult rc = enc(&m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (rc != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  MapEntry* victim = &g_maps[0];
+  for (auto& e : g_maps) {
+    if (!e.used) {
+      victim = &e;
+      break;
+    }
+    if (e.stamp < victim->stamp) victim = &e;
+  }
+  victim->key = key;
+  victim->map = m;
+  victim->stamp = ++g_stamp;
+  victim->used = true;
+  *out = m;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_kv_shape(int num_blocks, int block_size, int kv_heads, int head_dim, pa_dtype dt) {
+  if (dt != PA_FP16 && dt != PA_BF16) return PA_ERR_DTYPE;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_INVALID;
+  if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_INVALID;
+  if (kv_heads <= 0 || kv_heads > 1024 || num_blocks <= 0) return PA_ERR_INVALID;
+  // row coordinates (one past the pool included) must fit the TMA's int32
+  if ((int64_t)(num_blocks + 1) * block_size > INT32_MAX) return PA_ERR_INVALID;
+  return PA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+struct DecodeSetup {
+  int split, max_splits;
+  DecodeWorkspace ws;
+};
+
+int decode_setup(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq, int block_size, int split_tokens,
+                 DecodeSetup* s) {
+  const int split = pa_decode_split_tokens(max_blocks_per_seq, block_size, split_tokens);
+  if (split <= 0) return PA_ERR_INVALID;
+  const int64_t cap = (int64_t)max_blocks_per_seq * block_size;
+  if (cap > INT32_MAX) return PA_ERR_INVALID;
+  s->split = split;
+  s->max_splits = (int)((cap + split - 1) / split);
+  if (s->max_splits < 1) s->max_splits = 1;
+  s->ws = s->max_splits > 1 ? decode_workspace_layout(num_seqs, q_heads, head_dim, s->max_splits)
+                            : DecodeWorkspace{0, 0, 0, 0};
+  return PA_OK;
+}
+
+}  // namespace
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID";
+    case PA_ERR_NO_FREE_BLOCKS: return "PA_ERR_NO_FREE_BLOCKS";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
+    case PA_ERR_SHARED_BLOCK: return "PA_ERR_SHARED_BLOCK";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    default: return "PA_UNKNOWN_STATUS";
+  }
+}
+
+int pa_version(void) { return 100; }
+
+uint64_t pa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pa_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mapping, int num_tokens, void* k_cache,
+                         void* v_cache, int num_blocks, int block_size, int kv_heads, int head_dim, pa_dtype dtype,
+                         pa_stream stream) {
+  int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  return cuda_status(launch_reshape_and_cache(k, v, slot_mapping, num_tokens, k_cache, v_cache,
+                                              (int64_t)num_blocks * block_size, kv_heads * head_dim * 2, err,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks, int block_size,
+                   int kv_heads, int head_dim, pa_dtype dtype, pa_stream stream) {
+  int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return PA_ERR_INVALID;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !pairs || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  return cuda_status(launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks,
+                                        (int64_t)block_size * kv_heads * head_dim * 2, err,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_decode_split_tokens(int max_blocks_per_seq, int block_size, int split_tokens) {
+  if (max_blocks_per_seq <= 0 || block_size <= 0) return PA_ERR_INVALID;
+  const int unit = block_size > 16 ? block_size : 16;
+  int s = split_tokens == 0 ? kAutoSplitTokens : split_tokens;
+  if (s <= 0 || s % unit != 0 || s > 256 * block_size) return PA_ERR_INVALID;
+  return s;
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq, int block_size,
+                                int split_tokens) {
+  if (num_seqs < 0 || q_heads <= 0 || head_dim <= 0) return 0;
+  DecodeSetup s;
+  if (decode_setup(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s) != PA_OK) return 0;
+  return s.ws.bytes;
+}
+
+int pa_decode_partial(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads,
+                      int head_dim, int block_size, int num_blocks, float scale, int split_tokens, void* workspace,
+                      size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
+  int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || q_heads <= 0 || q_heads % kv_heads != 0 || q_heads / kv_heads > 16)
+    return PA_ERR_INVALID;
+  if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID;
+  DecodeSetup s;
+  st = decode_setup(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s);
+  if (st != PA_OK) return st;
+  if (s.ws.bytes > 0 && (!workspace || workspace_bytes < s.ws.bytes || !aligned16(workspace)))
+    return PA_ERR_WORKSPACE;
+  if ((int64_t)s.max_splits * kv_heads > (int64_t)INT32_MAX) return PA_ERR_INVALID;
+  CUtensorMap km, vm;
+  if (!kv_map(k_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &km) ||
+      !kv_map(v_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &vm))
+    return PA_ERR_CUDA;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  DecodeParams p{};
+  p.q = q;
+  p.tables = block_tables;
+  p.lens = context_lens;
+  p.out = out;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.part_o = s.ws.bytes ? reinterpret_cast<float*>(ws + s.ws.o_off) : nullptr;
+  p.part_m = s.ws.bytes ? reinterpret_cast<float*>(ws + s.ws.m_off) : nullptr;
+  p.part_l = s.ws.bytes ? reinterpret_cast<float*>(ws + s.ws.l_off) : nullptr;
+  p.err = err;
+  p.maxblk = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.q_heads = q_heads;
+  p.kv_heads = kv_heads;
+  p.group = q_heads / kv_heads;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.split_tokens = s.split;
+  p.max_splits = s.max_splits;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int bsub = block_size < 16 ? block_size : 16;
+  return cuda_status(
+      launch_decode_partial(km, vm, p, head_dim, bsub, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* context_lens, int num_seqs,
+                 int q_heads, int head_dim, int max_blocks_per_seq, int block_size, int split_tokens, void* out,
+                 pa_dtype dtype, pa_stream stream) {
+  if (dtype != PA_FP16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_INVALID;
+  if (num_seqs < 0 || q_heads <= 0) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  DecodeSetup s;
+  int st = decode_setup(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s);
+  if (st != PA_OK) return st;
+  if (s.ws.bytes == 0) return PA_OK;  // a single partition: pa_decode_partial wrote `out`
+  if (!workspace || workspace_bytes < s.ws.bytes || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  if (!context_lens || !out || !aligned16(out)) return PA_ERR_INVALID;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  MergeParams p{};
+  p.part_o = reinterpret_cast<const float*>(ws + s.ws.o_off);
+  p.part_m = reinterpret_cast<const float*>(ws + s.ws.m_off);
+  p.part_l = reinterpret_cast<const float*>(ws + s.ws.l_off);
+  p.lens = context_lens;
+  p.out = out;
+  p.num_seqs = num_seqs;
+  p.q_heads = q_heads;
+  p.max_splits = s.max_splits;
+  p.split_tokens = s.split;
+  p.cap = max_blocks_per_seq * block_size;
+  return cuda_status(launch_lse_merge(p, head_dim, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads,
+              int head_dim, int block_size, int num_blocks, float scale, int split_tokens, void* workspace,
+              size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
+  int st = pa_decode_partial(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, q_heads,
+                             kv_heads, head_dim, block_size, num_blocks, scale, split_tokens, workspace,
+                             workspace_bytes, out, dtype, stream);
+  if (st != PA_OK) return st;
+  return pa_lse_merge(workspace, workspace_bytes, context_lens, num_seqs, q_heads, head_dim, max_blocks_per_seq,
+                      block_size, split_tokens, out, dtype, stream);
+}
+
+int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* context_lens, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq, int num_reqs,
+                       int total_q, int max_q_len, int q_heads, int kv_heads, int head_dim, int block_size,
+                       int num_blocks, float scale, void* out, pa_dtype dtype, pa_stream stream) {
+  int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_reqs < 0 || num_reqs > 65535 || total_q < 0 || max_q_len < 0 || q_heads <= 0 ||
+      q_heads % kv_heads != 0 || kv_heads > 65535 || max_blocks_per_seq <= 0 || !std::isfinite(scale))
+    return PA_ERR_INVALID;
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_INVALID;
+  if (num_reqs == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
+  if ((int64_t)max_q_len * (q_heads / kv_heads) > (int64_t)INT32_MAX / 2) return PA_ERR_INVALID;
+  if (!q || !q_start || !context_lens || !k_cache || !v_cache || !block_tables || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID;
+  CUtensorMap km, vm;
+  if (!kv_map(k_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &km) ||
+      !kv_map(v_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &vm))
+    return PA_ERR_CUDA;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  PrefillParams p{};
+  p.q = q;
+  p.q_start = q_start;
+  p.lens = context_lens;
+  p.tables = block_tables;
+  p.out = out;
+  p.err = err;
+  p.maxblk = max_blocks_per_seq;
+  p.num_reqs = num_reqs;
+  p.total_q = total_q;
+  p.max_q_len = max_q_len;
+  p.q_heads = q_heads;
+  p.kv_heads = kv_heads;
+  p.group = q_heads / kv_heads;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int bsub = block_size < 16 ? block_size : 16;
+  return cuda_status(
+      launch_chunked_prefill(km, vm, p, head_dim, bsub, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_get_device_error(int32_t* host_code, pa_stream stream) {
+  if (!host_code) return PA_ERR_INVALID;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  *host_code = v;
+  return v ? PA_ERR_DEVICE_CHECK : PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// Internal interfaces between the library's translation units (not exported).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Counts kernel launches (pa_launch_count).
+void note_launch(int n = 1);
+
+struct DecodeParams {
+  const void* q;
+  const int32_t* tables;
+  const int32_t* lens;
+  void* out;
+  float* part_o;   // [num_seqs][q_heads][max_splits][head_dim]
+  float* part_m;   // [num_seqs][q_heads][max_splits], log2 units
+  float* part_l;   // [num_seqs][q_heads][max_splits]
+  int* err;
+  int maxblk, num_seqs, q_heads, kv_heads, group, num_blocks, block_size, split_tokens, max_splits;
+  float scale_log2;
+};
+
+struct MergeParams {
+  const float* part_o;
+  const float* part_m;
+  const float* part_l;
+  const int32_t* lens;
+  void* out;
+  int num_seqs, q_heads, max_splits, split_tokens, cap;
+};
+
+struct PrefillParams {
+  const void* q;
+  const int32_t* q_start;
+  const int32_t* lens;
+  const int32_t* tables;
+  void* out;
+  int* err;
+  int maxblk, num_reqs, total_q, max_q_len, q_heads, kv_heads, group, num_blocks, block_size;
+  float scale_log2;
+};
+
+// Workspace carve-up for decode partials.
+struct DecodeWorkspace {
+  size_t o_off, m_off, l_off, bytes;
+};
+DecodeWorkspace decode_workspace_layout(int num_seqs, int q_heads, int head_dim, int max_splits);
+
+// Launchers (return cudaSuccess or the launch error).  `bsub` is the TMA box
+// height min(block_size, 16); the tensor maps describe k_cache / v_cache as
+// 4-D {64, head_dim/64, kv_heads, num_blocks*block_size} with boxes
+// {64, 1, 1, bsub} and the 128-byte swizzle.
+cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                                  int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
+cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream);
+cudaError_t launch_chunked_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
+                                   int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
+                                     void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,
+                                     cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                               int num_blocks, int64_t block_bytes, int* err, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,174 @@
+"""Torch-tensor binding of the paged-KV C ABI (argument marshalling only).
+
+Every function passes ``data_ptr()`` values, sizes and the current CUDA
+stream to the function of the same name in ``include/pa.h``; all work runs in
+the library's kernels.  Tensors must be contiguous CUDA tensors of the
+documented shapes; int32 index tensors live on the same device.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+from ._lib import PA_BF16, PA_FP16, check
+
+__all__ = [
+    "reshape_and_cache",
+    "copy_blocks",
+    "decode",
+    "decode_partial",
+    "lse_merge",
+    "decode_split_tokens",
+    "decode_workspace_size",
+    "chunked_prefill",
+    "get_device_error",
+    "launch_count",
+    "dtype_code",
+]
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return PA_BF16
+    if dt == torch.float16:
+        return PA_FP16
+    raise TypeError(f"unsupported dtype {dt}: use torch.bfloat16 or torch.float16")
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _i32(t: torch.Tensor, name: str):
+    if t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    return _dev(t, name)
+
+
+def _cache_dims(k_cache: torch.Tensor):
+    if k_cache.dim() != 4:
+        raise ValueError("caches are [num_blocks, block_size, kv_heads, head_dim]")
+    return k_cache.shape
+
+
+def launch_count() -> int:
+    return int(_lib.lib().pa_launch_count())
+
+
+def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    if v_cache.shape != k_cache.shape or k.shape != v.shape or k.shape[1:] != (hkv, d):
+        raise ValueError("shape mismatch")
+    check(_lib.lib().pa_reshape_and_cache(
+        _dev(k, "k"), _dev(v, "v"), _i32(slot_mapping, "slot_mapping"), int(k.shape[0]),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), nb, bs, hkv, d, dtype_code(k_cache.dtype),
+        _stream(stream)), "pa_reshape_and_cache")
+
+
+def copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """``pairs``: int32 [n, 2] (src, dst) on the cache's device."""
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    check(_lib.lib().pa_copy_blocks(
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(pairs, "pairs"), int(pairs.shape[0]),
+        nb, bs, hkv, d, dtype_code(k_cache.dtype), _stream(stream)), "pa_copy_blocks")
+
+
+def decode_split_tokens(max_blocks_per_seq: int, block_size: int, split_tokens: int = 0) -> int:
+    return check(_lib.lib().pa_decode_split_tokens(max_blocks_per_seq, block_size, split_tokens),
+                 "pa_decode_split_tokens")
+
+
+def decode_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens=0) -> int:
+    return int(_lib.lib().pa_decode_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq,
+                                                   block_size, split_tokens))
+
+
+def _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, workspace):
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    B, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    maxblk = int(block_tables.shape[1])
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (None, 0)
+    return (_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(block_tables, "block_tables"),
+            maxblk, _i32(context_lens, "context_lens"), B, hq, hkv, d, bs, nb, float(scale), int(split_tokens),
+            ws_ptr, ws_bytes, _dev(out, "out"), dtype_code(q.dtype))
+
+
+def make_workspace(q, block_tables, block_size, split_tokens=0):
+    """Allocate (with torch) the scratch that :func:`decode` needs, or None."""
+    B, hq, d = q.shape
+    n = decode_workspace_size(B, hq, d, int(block_tables.shape[1]), block_size, split_tokens)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, split_tokens=0, workspace=None,
+           stream=None):
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = make_workspace(q, block_tables, k_cache.shape[1], split_tokens)
+    args = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, workspace)
+    check(_lib.lib().pa_decode(*args, _stream(stream)), "pa_decode")
+    return out
+
+
+def decode_partial(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens=0, workspace=None,
+                   stream=None):
+    args = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, workspace)
+    check(_lib.lib().pa_decode_partial(*args, _stream(stream)), "pa_decode_partial")
+
+
+def lse_merge(workspace, context_lens, q, block_tables, block_size, out, split_tokens=0, stream=None):
+    B, hq, d = q.shape
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    check(_lib.lib().pa_lse_merge(ws_ptr, ws_bytes, _i32(context_lens, "context_lens"), B, hq, d,
+                                  int(block_tables.shape[1]), block_size, int(split_tokens), _dev(out, "out"),
+                                  dtype_code(out.dtype), _stream(stream)), "pa_lse_merge")
+
+
+def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, scale, max_q_len, out=None,
+                    stream=None):
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    T, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("head_dim mismatch")
+    R = int(context_lens.shape[0])
+    if q_start.shape[0] != R + 1 or block_tables.shape[0] != R:
+        raise ValueError("q_start must have num_reqs+1 entries")
+    if out is None:
+        out = torch.empty_like(q)
+    check(_lib.lib().pa_chunked_prefill(
+        _dev(q, "q"), _i32(q_start, "q_start"), _i32(context_lens, "context_lens"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _i32(block_tables, "block_tables"), int(block_tables.shape[1]), R, T,
+        int(max_q_len), hq, hkv, d, bs, nb, float(scale), _dev(out, "out"), dtype_code(q.dtype),
+        _stream(stream)), "pa_chunked_prefill")
+    return out
+
+
+def get_device_error(stream=None) -> int:
+    """Read and clear the device error word (synchronises the stream)."""
+    import ctypes as C
+    code = C.c_int32(0)
+    st = _lib.lib().pa_get_device_error(C.byref(code), _stream(stream))
+    if st not in (_lib.PA_OK, _lib.PA_ERR_DEVICE_CHECK):
+        check(st, "pa_get_device_error")
+    return int(code.value)
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,117 @@
+// Host fuzz driver for the block allocator, built with ASan/UBSan by
+// tests/test_allocator_cpp.py.  Runs a seeded random script through the C ABI
+// and checks structural invariants after every call:
+//   * refcount of every block == number of tables holding it;
+//   * the free queue holds exactly the blocks with refcount 0, once each;
+//   * each table has ceil(len / block_size) entries;
+//   * a failed call changes nothing (checked via a snapshot).
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <random>
+#include <vector>
+
+#include "pa.h"
+
+struct Snapshot {
+  std::vector<int32_t> free_list, refs;
+  std::map<int, std::vector<int32_t>> tables;
+  std::map<int, int64_t> lens;
+  bool operator==(const Snapshot& o) const {
+    return free_list == o.free_list && refs == o.refs && tables == o.tables && lens == o.lens;
+  }
+};
+
+static int g_nb, g_bs;
+
+static Snapshot snap(pa_alloc* a, const std::vector<int>& live) {
+  Snapshot s;
+  s.free_list.resize(g_nb);
+  int n = pa_alloc_free_list(a, s.free_list.data(), g_nb);
+  if (n < 0) { std::printf("free_list failed\n"); std::exit(2); }
+  s.free_list.resize(n);
+  for (int b = 0; b < g_nb; ++b) s.refs.push_back(pa_alloc_ref(a, b));
+  for (int id : live) {
+    std::vector<int32_t> t(4096);
+    int m = 0;
+    if (pa_alloc_block_table(a, id, t.data(), (int)t.size(), &m) != PA_OK) { std::printf("table\n"); std::exit(2); }
+    t.resize(m);
+    s.tables[id] = t;
+    int64_t len = 0;
+    pa_alloc_seq_len(a, id, &len);
+    s.lens[id] = len;
+  }
+  return s;
+}
+
+static void check_invariants(const Snapshot& s) {
+  std::vector<int> count(g_nb, 0), in_free(g_nb, 0);
+  for (auto& kv : s.tables) {
+    if ((int64_t)kv.second.size() != (s.lens.at(kv.first) + g_bs - 1) / g_bs) { std::printf("table size\n"); std::exit(3); }
+    for (int32_t b : kv.second) count[b]++;
+  }
+  for (int32_t b : s.free_list) {
+    if (in_free[b]++) { std::printf("duplicate in free list\n"); std::exit(3); }
+  }
+  for (int b = 0; b < g_nb; ++b) {
+    if (s.refs[b] != count[b]) { std::printf("refcount mismatch at %d\n", b); std::exit(3); }
+    if ((s.refs[b] == 0) != (in_free[b] == 1)) { std::printf("free set mismatch at %d\n", b); std::exit(3); }
+  }
+}
+
+int main(int argc, char** argv) {
+  const int steps = argc > 1 ? std::atoi(argv[1]) : 10000;
+  std::mt19937 rng(1234);
+  for (int round = 0; round < 8; ++round) {
+    g_nb = 4 + (int)(rng() % 60);
+    const int bss[] = {1, 2, 4, 16};
+    g_bs = bss[rng() % 4];
+    std::vector<int32_t> order(g_nb);
+    for (int i = 0; i < g_nb; ++i) order[i] = i;
+    std::shuffle(order.begin(), order.end(), rng);
+    pa_alloc* a = nullptr;
+    if (pa_alloc_create(g_nb, g_bs, order.data(), &a) != PA_OK) return 1;
+    std::vector<int> live;
+    int next = 0;
+    std::vector<int32_t> slots(4096);
+    for (int i = 0; i < steps / 8; ++i) {
+      Snapshot before = snap(a, live);
+      int op = rng() % 7, rc = PA_OK;
+      int id = live.empty() ? -1 : live[rng() % live.size()];
+      if (op == 0 || live.empty()) {
+        rc = pa_alloc_add_seq(a, next);
+        if (rc == PA_OK) live.push_back(next++);
+      } else if (op <= 2) {
+        rc = pa_alloc_append_slots(a, id, (int)(rng() % (3 * g_bs + 2)), slots.data());
+      } else if (op == 3) {
+        int64_t len = 0;
+        pa_alloc_seq_len(a, id, &len);
+        pa_alloc_add_seq(a, next);
+        live.push_back(next);
+        before = snap(a, live);
+        rc = pa_alloc_share(a, next++, id, (int)(len ? rng() % (len + 1) : 0));
+      } else if (op == 4) {
+        int32_t pair[2];
+        std::vector<int32_t> t(4096);
+        int m = 0;
+        pa_alloc_block_table(a, id, t.data(), 4096, &m);
+        rc = pa_alloc_cow(a, id, (int)(rng() % (m + 2)) - 1, pair);
+      } else if (op == 5) {
+        rc = pa_alloc_free_seq(a, id);
+        if (rc == PA_OK) live.erase(std::find(live.begin(), live.end(), id));
+      } else {
+        rc = pa_alloc_free_seq(a, 1 << 20);  // unknown: must fail without effect
+        if (rc == PA_OK) return 4;
+        if (pa_alloc_ref(a, g_nb) != PA_ERR_INVALID || pa_alloc_ref(a, -1) != PA_ERR_INVALID) return 4;
+      }
+      Snapshot after = snap(a, live);
+      if (rc != PA_OK && !(after == before)) { std::printf("failed call changed state (op %d rc %d)\n", op, rc); return 5; }
+      check_invariants(after);
+    }
+    pa_alloc_destroy(a);
+  }
+  std::printf("ok\n");
+  return 0;
+}

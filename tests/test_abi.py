@@ -1,0 +1,71 @@
+"""The C-ABI library loads here (no GPU needed) and exports every declared call."""
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_76_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        return _lib.lib()
+    except _lib.LibraryMissing:
+        from paged_kv_cache_76_gb300 import build
+        build.build()
+        return _lib.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 25
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_binding_prototypes_cover_the_header():
+    assert set(_lib.PROTOTYPES) == set(declared_functions())
+
+
+def test_host_only_calls(lib):
+    assert lib.pa_version() >= 100
+    assert lib.pa_status_string(-2) == b"PA_ERR_NO_FREE_BLOCKS"
+    assert lib.pa_decode_split_tokens(256, 16, 0) == 512
+    assert lib.pa_decode_split_tokens(256, 16, 24) == _lib.PA_ERR_INVALID      # not a multiple of 16
+    assert lib.pa_decode_split_tokens(256, 32, 48) == _lib.PA_ERR_INVALID      # not a multiple of bs=32
+    assert lib.pa_decode_split_tokens(256, 4, 2048) == _lib.PA_ERR_INVALID     # > 256 * bs
+    # one partition needs no scratch; several need o + m + l per (seq, head, partition)
+    assert lib.pa_decode_workspace_size(64, 32, 128, 32, 16, 512) == 0
+    ws = lib.pa_decode_workspace_size(8, 64, 128, 8192, 16, 512)
+    rows = 8 * 64 * 256
+    assert ws >= rows * (128 + 2) * 4 and ws < rows * (128 + 2) * 4 + 1024
+
+
+def test_device_calls_reject_bad_arguments_before_launching(lib):
+    # invalid shapes are caught on the host (no GPU touched): bad head_dim, bad block size, bad dtype
+    assert lib.pa_reshape_and_cache(None, None, None, 1, None, None, 4, 16, 1, 96, 1, None) == _lib.PA_ERR_INVALID
+    assert lib.pa_copy_blocks(None, None, None, 1, 4, 12, 1, 64, 1, None) == _lib.PA_ERR_INVALID
+    assert lib.pa_copy_blocks(None, None, None, 1, 4, 16, 1, 64, 7, None) == _lib.PA_ERR_DTYPE
+    # zero-size work is a no-op that needs no pointers
+    assert lib.pa_reshape_and_cache(None, None, None, 0, None, None, 4, 16, 1, 64, 1, None) == _lib.PA_OK
+    assert lib.pa_decode(None, None, None, None, 4, None, 0, 8, 2, 128, 16, 4, 0.1, 0, None, 0, None, 1,
+                         None) == _lib.PA_OK
+    # q_heads not a multiple of kv_heads, or group > 16
+    assert lib.pa_decode(1, 1, 1, 1, 4, 1, 1, 6, 4, 128, 16, 4, 0.1, 0, None, 0, 1, 1, None) == _lib.PA_ERR_INVALID
+    assert lib.pa_decode(1, 1, 1, 1, 4, 1, 1, 34, 2, 128, 16, 4, 0.1, 0, None, 0, 1, 1, None) == _lib.PA_ERR_INVALID
+    # a split context without a workspace
+    assert lib.pa_decode(16, 16, 16, 16, 64, 16, 1, 8, 2, 128, 16, 4, 0.1, 512, None, 0, 16, 1,
+                         None) == _lib.PA_ERR_WORKSPACE
+    # misaligned device pointer
+    assert lib.pa_decode(17, 16, 16, 16, 4, 16, 1, 8, 2, 128, 16, 4, 0.1, 0, None, 0, 16, 1,
+                         None) == _lib.PA_ERR_INVALID
