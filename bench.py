@@ -350,6 +350,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--split", type=int, default=None, help="decode partition size (default: the workload's)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -372,6 +373,8 @@ def main():
     _lib.lib()  # fails loudly if the CUDA library is missing
 
     wl = W.WORKLOADS[args.workload]()
+    if args.split is not None:
+        wl.split_tokens = args.split
     step = Step(wl, device, value_seed=1000 * rank)
     peak, peak_kind = measured_peaks()
 
