@@ -193,6 +193,40 @@ int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* con
                        int q_heads, int kv_heads, int head_dim, int block_size, int num_blocks,
                        float scale, void* out, pa_dtype dtype, pa_stream stream);
 
+/* ----------------------------------------------------------------------------
+ * pa_decode_noalloc - pa_decode without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this call: it only repackages pa_decode
+ * for callers that cannot allocate device memory for the decode scratch - a
+ * plugin inside a host framework that has already reserved the GPU's memory
+ * for its own pool and offers the plugin no allocator, or a latency-critical
+ * loop where cudaMalloc/cudaFree (which can synchronise the device) are not
+ * acceptable.  The caller still passes all inputs and outputs (same meaning
+ * as pa_decode); the split-K partials go to a scratch array held by the
+ * library: a file-scope device array of PA_DECODE_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) that every GPU loading the library keeps until the process exits.
+ * The call allocates nothing.
+ *
+ * - Size limit: if the scratch this call needs (pa_decode_workspace_size with
+ *   the same arguments) exceeds PA_DECODE_NOALLOC_SCRATCH_BYTES it returns
+ *   PA_ERR_WORKSPACE and launches nothing; use pa_decode with your own
+ *   workspace then.  Requests that fit one partition need no scratch.
+ * - Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Sharing: all calls share the one array, which keeps the last call's
+ *   contents.  Nothing in it has to start at zero (every partial the merge
+ *   reads is written earlier in the same call).  Calls that overlap on the
+ *   GPU (two streams, or two host threads launching at once) race on the
+ *   array and corrupt each other's results: serialise them.
+ * ------------------------------------------------------------------------- */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_heads,
+                      int kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                      int split_tokens, void* out, pa_dtype dtype, pa_stream stream);
+
 /* Read and clear the calling device's error word.  Synchronises `stream`.
  * *host_code receives the PA_DEVERR_* code (0 = none).  Returns
  * PA_ERR_DEVICE_CHECK if a code was recorded, PA_OK otherwise. */

@@ -66,6 +66,7 @@ PROTOTYPES = {
     "pa_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I, _P]),
     "pa_decode_partial": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I, _P]),
     "pa_lse_merge": (_I, [_P, _SZ, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P]),
+    "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
     "pa_chunked_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
     "pa_get_device_error": (_I, [_I32P, _P]),
     "pa_alloc_create": (_I, [_I, _I, _I32P, C.POINTER(_P)]),
