@@ -392,7 +392,6 @@ def main():
     if ops.get_device_error(stream) != 0:
         raise RuntimeError("device error recorded during warm-up")
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device() if ws == 1 else local)
     if ws > 1:
@@ -403,7 +402,7 @@ def main():
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for i in range(args.steps):
-            step.run(stream, evs[i] if step.dec else None)
+            step.run(stream)
         t_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -412,7 +411,6 @@ def main():
     if ws > 1:
         torch.distributed.barrier()
     ms = t_start.elapsed_time(t_end)
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs])) if step.dec else None
     if ops.get_device_error(stream) != 0:
         raise RuntimeError("device error recorded during the timed region")
     t = torch.tensor([ms], dtype=torch.float64, device=device)
@@ -420,6 +418,19 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     ms = float(t.item())
     ms_per_step = ms / args.steps
+
+    # Dominant kernel: the same K steps again, each decode-partial launch
+    # bracketed by CUDA events on its stream.  (Kept out of the region above:
+    # an event between two kernels ends their programmatic-launch overlap.)
+    dec_ms = None
+    if step.dec:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step.run(stream, evs[i])
+        stream.synchronize()
+        dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
 
     # e2e: host buffers through the public API
     e2e_val = None
@@ -490,6 +501,8 @@ def main():
             "traffic": traffic,
             "algorithmic_bytes_per_launch": dec_bytes,
             "avg_launch_ms": round(dec_ms, 5),
+            "timing": "CUDA events around each of K decode_partial launches on the bench stream, "
+                      "in a second pass of the same K steps",
         }
         if "decode_unique" in nb and nb["decode_unique"] < dec_bytes:
             res["roofline"]["unique_bytes_per_launch"] = nb["decode_unique"]

@@ -22,6 +22,14 @@
  *   library allocates no device memory and keeps no pointer after returning.
  *   Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *   legacy default stream).  All device pointers must be 16-byte aligned.
+ * - Ordering: kernels are launched with programmatic dependent launch.  A
+ *   kernel of this library may start its set-up while the kernel before it on
+ *   the same stream is finishing, and reads only q, block tables, q_start and
+ *   context lengths during that set-up; caches, scratch and outputs are read
+ *   or written only once the previous kernel has completed.  So those four
+ *   inputs must be ready when the call is enqueued (they are if whatever writes
+ *   them was enqueued earlier on the stream without allowing early launch of
+ *   its successor, as plain kernels and copies do).
  * - Errors: every call returns a pa_status.  Argument errors are caught on the
  *   host before anything is launched.  Data errors that only the device can
  *   see (a block id outside [0, num_blocks), a slot past the pool, a context

@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(256)
                              const int32_t* __restrict__ slots, uint4* __restrict__ k_cache,
                              uint4* __restrict__ v_cache, int num_tokens, int row_vecs, int64_t num_slots,
                              int* err) {
+  griddep_wait();  // k/v/slots and the cache may come from the kernel before this one
+  griddep_launch_dependents();
   const int64_t total = (int64_t)num_tokens * row_vecs;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t tok = i / row_vecs;
@@ -49,6 +51,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ pairs,
                        int num_pairs, int64_t block_vecs, int num_blocks, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
     const int src = __ldg(pairs + 2 * pi), dst = __ldg(pairs + 2 * pi + 1);
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -79,11 +83,9 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), num_tokens, row_vecs, num_slots, err);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                    static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, static_cast<uint4*>(k_cache),
+                    static_cast<uint4*>(v_cache), num_tokens, row_vecs, num_slots, err);
 }
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
@@ -93,11 +95,8 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
   int64_t bx = (block_vecs + 255) / 256;
   if (bx > 8) bx = 8;
   const int by = num_pairs < 65535 ? num_pairs : 65535;
-  copy_blocks_kernel<<<dim3((unsigned)bx, by), 256, 0, stream>>>(static_cast<uint4*>(k_cache),
-                                                                  static_cast<uint4*>(v_cache), pairs, num_pairs,
-                                                                  block_vecs, num_blocks, err);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(copy_blocks_kernel, dim3((unsigned)bx, by), dim3(256), 0, stream, static_cast<uint4*>(k_cache),
+                    static_cast<uint4*>(v_cache), pairs, num_pairs, block_vecs, num_blocks, err);
 }
 
 }  // namespace pa

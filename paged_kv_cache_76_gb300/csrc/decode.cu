@@ -10,7 +10,10 @@
 // STAGES shared-memory stages fed by TMA (cp.async.bulk.tensor) behind a
 // per-warp copy of the partition's Block Table slice: the warp issues the
 // loads of tile j+STAGES as soon as it has consumed tile j, so up to STAGES
-// tiles per warp are in flight while it computes.
+// tiles per warp are in flight while it computes.  Measured on GB300: 4 warps
+// x 2 stages (~65 KB of shared memory, 3 CTAs and 12 streaming warps per SM)
+// beats deeper rings with fewer resident CTAs - shorter CTA lifetimes leave a
+// smaller tail when the grid drains.
 //
 // Math per tile (GQA: the whole query-head group shares every K/V tile):
 //   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]       mma.m16n8k16, D/16 k-steps
@@ -32,7 +35,7 @@ namespace pa {
 namespace {
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeStages = 3;
+constexpr int kDecodeStages = 2;
 constexpr int kMaxTableEntries = 256;  // per warp: split_tokens / block_size <= 256
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -46,7 +49,9 @@ struct DecodeSmem {
   static constexpr int WARP_BYTES = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = WARPS * WARP_BYTES;
   static constexpr int TAB_OFF = BAR_OFF + WARPS * STAGES * 8;
-  static constexpr int BYTES = TAB_OFF + WARPS * kMaxTableEntries * 4 + 1024;  // + alignment slack
+  // dynamic bytes for `entries` table entries per warp, + alignment slack
+  static constexpr int bytes(int entries) { return TAB_OFF + WARPS * entries * 4 + 1024; }
+  static constexpr int MAX_BYTES = TAB_OFF + WARPS * kMaxTableEntries * 4 + 1024;
 };
 
 template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES>
@@ -64,7 +69,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int lane = threadIdx.x & 31;
   uint8_t* wbase = smem + warp * L::WARP_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * STAGES;
-  int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF) + warp * kMaxTableEntries;
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF) + warp * p.tab_entries;
 
   if (lane == 0) {
 #pragma unroll
@@ -76,6 +81,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     prefetch_tensormap(&vmap);
   }
   __syncthreads();  // the only CTA-wide barrier; warps are independent below
+  griddep_launch_dependents();
 
   const int r = blockIdx.y;
   const int u = blockIdx.x * WARPS + warp;
@@ -83,45 +89,37 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int c = u / p.kv_heads;
   const int cap = p.maxblk * p.block_size;
   int ctx = __ldg(p.lens + r);
-  if (ctx < 0 || ctx > cap) {
-    if (lane == 0) record_error(p.err, PA_DEVERR_CONTEXT_LEN);
-    ctx = ctx < 0 ? 0 : cap;
-  }
+  const bool bad_len = ctx < 0 || ctx > cap;
+  ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
   const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
-  if (c >= (nsplit > 0 ? nsplit : 1)) return;
-
+  const bool active = c < (nsplit > 0 ? nsplit : 1);
   const int G = p.group;
   const int qh0 = h * G;
-  T* out = reinterpret_cast<T*>(p.out);
-  if (ctx == 0) {
-    T* o = out + ((size_t)r * p.q_heads + qh0) * D;
-    for (int i = lane; i < G * D; i += 32) o[i] = Elem<T>::from(0.f);
-    return;
-  }
-
   const int tok0 = c * p.split_tokens;
   const int tok1 = min(tok0 + p.split_tokens, ctx);
-  const int ntiles = (tok1 - tok0 + 15) >> 4;
+  const int ntiles = active && ctx > 0 ? (tok1 - tok0 + 15) >> 4 : 0;
   const int blk0 = tok0 / p.block_size;
-  const int nblk = (tok1 - 1) / p.block_size - blk0 + 1;
 
-  // Block Table slice of this partition; an out-of-range id is recorded and
-  // replaced by num_blocks, whose rows lie past the tensor map: TMA then
-  // zero-fills instead of reading anything.
-  const int32_t* trow = p.tables + (size_t)r * p.maxblk + blk0;
-  for (int i = lane; i < nblk; i += 32) {
-    int b = __ldg(trow + i);
-    if (b < 0 || b >= p.num_blocks) {
-      record_error(p.err, PA_DEVERR_BLOCK_ID);
-      b = p.num_blocks;
-    }
-    tab[i] = b;
-  }
-
-  // Q^T as the B operand of S^T = K Q^T: lane holds head (lane/4) of each
-  // 8-head n-tile, elements d = 16ks + 2(lane%4) + {0,1} and +8.
+  // Set-up that reads only this call's immutable inputs (block table slice,
+  // q) overlaps the previous kernel's tail; the cache is read after
+  // griddep_wait().
+  bool bad_id = false;
   uint32_t qf[NT][KSTEPS][2];
-  {
+  if (ntiles > 0) {
+    // Block Table slice of this partition; an out-of-range id is replaced by
+    // num_blocks, whose rows lie past the tensor map: TMA then zero-fills.
+    const int nblk = (tok1 - 1) / p.block_size - blk0 + 1;
+    const int32_t* trow = p.tables + (size_t)r * p.maxblk + blk0;
+    for (int i = lane; i < nblk; i += 32) {
+      int b = __ldg(trow + i);
+      if (b < 0 || b >= p.num_blocks) {
+        bad_id = true;
+        b = p.num_blocks;
+      }
+      tab[i] = b;
+    }
+    // Q^T as the B operand of S^T = K Q^T: lane holds head (lane/4) of each
+    // 8-head n-tile, elements d = 16ks + 2(lane%4) + {0,1} and +8.
     const T* qb = reinterpret_cast<const T*>(p.q) + ((size_t)r * p.q_heads + qh0) * D;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -138,6 +136,17 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
       }
     }
+  }
+  griddep_wait();
+  if (bad_len && lane == 0) record_error(p.err, PA_DEVERR_CONTEXT_LEN);
+  if (bad_id) record_error(p.err, PA_DEVERR_BLOCK_ID);
+  if (!active) return;
+
+  T* out = reinterpret_cast<T*>(p.out);
+  if (ctx == 0) {
+    T* o = out + ((size_t)r * p.q_heads + qh0) * D;
+    for (int i = lane; i < G * D; i += 32) o[i] = Elem<T>::from(0.f);
+    return;
   }
   __syncwarp();
 
@@ -318,33 +327,46 @@ __global__ void __launch_bounds__(WARPS * 32)
   }
 }
 
-// One warp per (request, query head): combine the partitions of requests that
-// have more than one.  M = max_c m_c; w_c = 2^(m_c - M);
-// out = sum_c w_c o_c / sum_c w_c l_c, partitions in logical order.
+// One CTA of 4 warps per (request, query head): combine the partitions of
+// requests that have more than one.  M = max_c m_c; w_c = 2^(m_c - M);
+// out = sum_c w_c o_c / sum_c w_c l_c.  Warp w takes partitions w, w+4, ...;
+// the four partial sums are added in warp order, so the result depends only on
+// logical positions.
 template <int D, typename T>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
   constexpr int V = D / 32;
-  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (wid >= p.num_seqs * p.q_heads) return;
-  const int r = wid / p.q_heads;
+  constexpr int NW = 4;
+  __shared__ float s_max[NW];
+  __shared__ float s_den[NW];
+  __shared__ __align__(16) float s_acc[NW][D];
+  griddep_wait();  // the partials come from the kernel before this one
+  griddep_launch_dependents();
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (row >= p.num_seqs * p.q_heads) return;
+  const int r = row / p.q_heads;
   int ctx = __ldg(p.lens + r);
   ctx = ctx < 0 ? 0 : (ctx > p.cap ? p.cap : ctx);
   const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit <= 1) return;
-  const float* pm = p.part_m + (size_t)wid * p.max_splits;
-  const float* pl = p.part_l + (size_t)wid * p.max_splits;
-  const float* po = p.part_o + (size_t)wid * p.max_splits * D + lane * V;
+  if (nsplit <= 1) return;  // pa_decode_partial wrote this row directly
+  const float* pm = p.part_m + (size_t)row * p.max_splits;
+  const float* pl = p.part_l + (size_t)row * p.max_splits;
+  const float* po = p.part_o + (size_t)row * p.max_splits * D + lane * V;
+
   float M = -INFINITY;
-  for (int c = lane; c < nsplit; c += 32) M = fmaxf(M, pm[c]);
+  for (int c = threadIdx.x; c < nsplit; c += NW * 32) M = fmaxf(M, pm[c]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_max[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+
   float a[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) a[i] = 0.f;
   float den = 0.f;
 #pragma unroll 4
-  for (int c = 0; c < nsplit; ++c) {
+  for (int c = warp; c < nsplit; c += NW) {
     const float w = exp2f(pm[c] - M);
     den += w * pl[c];
     if constexpr (V == 4) {
@@ -359,10 +381,15 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
       a[1] += w * x.y;
     }
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  T* o = reinterpret_cast<T*>(p.out) + (size_t)wid * D + lane * V;
 #pragma unroll
-  for (int i = 0; i < V; i += 2) *reinterpret_cast<uint32_t*>(o + i) = Elem<T>::pack(a[i] * inv, a[i + 1] * inv);
+  for (int i = 0; i < V; ++i) s_acc[warp][lane * V + i] = a[i];
+  if (lane == 0) s_den[warp] = den;
+  __syncthreads();
+  const float dsum = ((s_den[0] + s_den[1]) + s_den[2]) + s_den[3];
+  const float inv = dsum > 0.f ? 1.f / dsum : 0.f;
+  T* o = reinterpret_cast<T*>(p.out) + (size_t)row * D;
+  for (int d = threadIdx.x; d < D; d += NW * 32)
+    o[d] = Elem<T>::from((((s_acc[0][d] + s_acc[1][d]) + s_acc[2][d]) + s_acc[3][d]) * inv);
 }
 
 template <int D, int BSUB, int NT, typename T>
@@ -375,15 +402,13 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::MAX_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int units = p.max_splits * p.kv_heads;
   dim3 grid((units + W - 1) / W, p.num_seqs);
-  kern<<<grid, W * 32, L::BYTES, stream>>>(kmap, vmap, p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(W * 32), L::bytes(p.tab_entries), stream, kmap, vmap, p);
 }
 
 template <int D, int BSUB, typename T>
@@ -420,19 +445,14 @@ cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vm
 }
 
 cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream) {
-  const int rows = p.num_seqs * p.q_heads;
-  dim3 grid((rows + 3) / 4);
-  if (head_dim == 128) {
-    if (dt == PA_BF16) lse_merge_kernel<128, __nv_bfloat16><<<grid, 128, 0, stream>>>(p);
-    else lse_merge_kernel<128, __half><<<grid, 128, 0, stream>>>(p);
-  } else if (head_dim == 64) {
-    if (dt == PA_BF16) lse_merge_kernel<64, __nv_bfloat16><<<grid, 128, 0, stream>>>(p);
-    else lse_merge_kernel<64, __half><<<grid, 128, 0, stream>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  note_launch();
-  return cudaGetLastError();
+  const dim3 grid(p.num_seqs * p.q_heads), block(128);
+  if (head_dim == 128)
+    return dt == PA_BF16 ? launch_pdl(lse_merge_kernel<128, __nv_bfloat16>, grid, block, 0, stream, p)
+                         : launch_pdl(lse_merge_kernel<128, __half>, grid, block, 0, stream, p);
+  if (head_dim == 64)
+    return dt == PA_BF16 ? launch_pdl(lse_merge_kernel<64, __nv_bfloat16>, grid, block, 0, stream, p)
+                         : launch_pdl(lse_merge_kernel<64, __half>, grid, block, 0, stream, p);
+  return cudaErrorInvalidValue;
 }
 
 DecodeWorkspace decode_workspace_layout(int num_seqs, int q_heads, int head_dim, int max_splits) {

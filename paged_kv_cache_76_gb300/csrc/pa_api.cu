@@ -19,7 +19,13 @@ std::atomic<uint64_t> g_launches{0};
 __device__ int g_device_error;
 
 constexpr int kMaxDevices = 64;
-constexpr int kAutoSplitTokens = 512;
+// Automatic partition size: shorter partitions balance the grid better,
+// longer ones write fewer partials for the merge.  Measured on GB300: 384 tokens
+// is best for contexts up to 8K (batch-64 Llama-8B-style decode), 512 beyond
+// (128K-token contexts, where 256 doubles the merge traffic).
+constexpr int kAutoSplitShort = 384;
+constexpr int kAutoSplitLong = 512;
+constexpr int64_t kShortContext = 8192;
 
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
@@ -216,7 +222,8 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
 int pa_decode_split_tokens(int max_blocks_per_seq, int block_size, int split_tokens) {
   if (max_blocks_per_seq <= 0 || block_size <= 0) return PA_ERR_INVALID;
   const int unit = block_size > 16 ? block_size : 16;
-  int s = split_tokens == 0 ? kAutoSplitTokens : split_tokens;
+  const int64_t cap = (int64_t)max_blocks_per_seq * block_size;
+  int s = split_tokens != 0 ? split_tokens : (cap <= kShortContext ? kAutoSplitShort : kAutoSplitLong);
   if (s <= 0 || s % unit != 0 || s > 256 * block_size) return PA_ERR_INVALID;
   return s;
 }
@@ -272,6 +279,7 @@ int pa_decode_partial(const void* q, const void* k_cache, const void* v_cache, c
   p.block_size = block_size;
   p.split_tokens = s.split;
   p.max_splits = s.max_splits;
+  p.tab_entries = s.split / block_size;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int bsub = block_size < 16 ? block_size : 16;
   return cuda_status(

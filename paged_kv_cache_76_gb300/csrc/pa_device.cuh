@@ -169,6 +169,21 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch
+// ----------------------------------------------------------------------------
+// Every kernel of this library is launched with programmatic stream
+// serialisation.  griddep_wait() blocks until the kernel before it on the
+// stream has completed and its memory is visible (a no-op when launched
+// without the attribute); a kernel reads only its own immutable inputs (q,
+// block tables, context lengths) before it, and touches caches, scratch and
+// outputs only after it.  griddep_launch_dependents() lets the next kernel on
+// the stream start its own set-up early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // error word
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void record_error(int* err, int code) {

@@ -6,12 +6,36 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pa.h"
 
 namespace pa {
 
 // Counts kernel launches (pa_launch_count).
 void note_launch(int n = 1);
+
+// Launch with programmatic stream serialisation (programmatic dependent
+// launch): the kernel may start while the previous kernel on the stream is
+// finishing; it synchronises with griddepcontrol.wait before touching memory
+// that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
 
 struct DecodeParams {
   const void* q;
@@ -23,6 +47,7 @@ struct DecodeParams {
   float* part_l;   // [num_seqs][q_heads][max_splits]
   int* err;
   int maxblk, num_seqs, q_heads, kv_heads, group, num_blocks, block_size, split_tokens, max_splits;
+  int tab_entries;  // block-table entries per partition: split_tokens / block_size
   float scale_log2;
 };
 

@@ -70,11 +70,15 @@ __global__ void __launch_bounds__((CW + 1) * 32)
   const int ctx = __ldg(p.lens + r);
   const int p0 = ctx - chunk;
   if (qs < 0 || qe < qs || qe > p.total_q || chunk > p.max_q_len || p0 < 0 || ctx > p.maxblk * p.block_size) {
+    griddep_wait();
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
     return;
   }
   const int rows = chunk * G;
-  if (row0 >= rows) return;
+  if (row0 >= rows) {
+    griddep_wait();
+    return;
+  }
   const int last_row = min(row0 + ROWS, rows) - 1;
   const int kmax = p0 + last_row / G + 1;  // keys [0, kmax) are visible to some row
   const int ntiles = (kmax + kKeyTile - 1) / kKeyTile;
@@ -90,6 +94,7 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     prefetch_tensormap(&vmap);
   }
   __syncthreads();
+  griddep_launch_dependents();
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
@@ -97,6 +102,7 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     const int need_blocks = (kmax + p.block_size - 1) / p.block_size;
     int chunk_base = -kTableChunk;
     const uint64_t pol = policy_evict_last();  // K/V tiles are re-read by the other row tiles
+    griddep_wait();  // the cache (this step's reshape_and_cache) comes from the kernel before
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % STAGES;
       if (j >= STAGES && !mbar_wait(smem_u32(&empty[s]), ((j / STAGES) - 1) & 1)) {
@@ -161,6 +167,7 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     }
   }
 
+  griddep_wait();  // before writing `out` (and reading tiles of this step's cache)
   float acc[DT8][4];
 #pragma unroll
   for (int i = 0; i < DT8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -311,9 +318,7 @@ cudaError_t launch_prefill_t(const CUtensorMap& kmap, const CUtensorMap& vmap, c
   }
   const int row_tiles = (p.max_q_len * p.group + CW * 16 - 1) / (CW * 16);
   dim3 grid(row_tiles, p.kv_heads, p.num_reqs);
-  kern<<<grid, (CW + 1) * 32, L::BYTES, stream>>>(kmap, vmap, p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3((CW + 1) * 32), L::BYTES, stream, kmap, vmap, p);
 }
 
 template <int D, typename T>

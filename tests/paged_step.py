@@ -105,8 +105,9 @@ class DeviceStep:
         self.pairs_host = np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
         self.split_tokens = wl.split_tokens if split_tokens is None else split_tokens
         d = self.dev
-        self.k_cache = vals["k_cache"].to(d).contiguous()
-        self.v_cache = vals["v_cache"].to(d).contiguous()
+        # private copies: the step writes the pool, the caller's tensors stay the pre-step input
+        self.k_cache = vals["k_cache"].to(d, copy=True).contiguous()
+        self.v_cache = vals["v_cache"].to(d, copy=True).contiguous()
         self.k_new = vals["k_new"].to(d).contiguous()
         self.v_new = vals["v_new"].to(d).contiguous()
         self.slots = torch.from_numpy(self.slots_host).to(d)

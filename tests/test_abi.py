@@ -40,12 +40,13 @@ def test_binding_prototypes_cover_the_header():
 def test_host_only_calls(lib):
     assert lib.pa_version() >= 100
     assert lib.pa_status_string(-2) == b"PA_ERR_NO_FREE_BLOCKS"
-    assert lib.pa_decode_split_tokens(256, 16, 0) == 512
+    assert lib.pa_decode_split_tokens(256, 16, 0) == 384          # auto, contexts up to 8K
+    assert lib.pa_decode_split_tokens(1024, 16, 0) == 512         # auto, longer contexts
     assert lib.pa_decode_split_tokens(256, 16, 24) == _lib.PA_ERR_INVALID      # not a multiple of 16
     assert lib.pa_decode_split_tokens(256, 32, 48) == _lib.PA_ERR_INVALID      # not a multiple of bs=32
     assert lib.pa_decode_split_tokens(256, 4, 2048) == _lib.PA_ERR_INVALID     # > 256 * bs
     # one partition needs no scratch; several need o + m + l per (seq, head, partition)
-    assert lib.pa_decode_workspace_size(64, 32, 128, 32, 16, 512) == 0
+    assert lib.pa_decode_workspace_size(64, 32, 128, 24, 16, 0) == 0
     ws = lib.pa_decode_workspace_size(8, 64, 128, 8192, 16, 512)
     rows = 8 * 64 * 256
     assert ws >= rows * (128 + 2) * 4 and ws < rows * (128 + 2) * 4 + 1024

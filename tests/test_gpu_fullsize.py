@@ -1,0 +1,96 @@
+"""Parity at the full sizes of the five measured workloads (GPU).
+
+The device runs the whole step exactly as bench.py times it (same kernels,
+partitions and launch configuration: copy_blocks -> reshape_and_cache ->
+chunked prefill -> decode partial -> merge); pools are generated on the GPU.
+The float64 oracle checks sampled outputs on a compacted copy of the blocks
+they read; bitwise properties (physical relabelling, copy-on-write vs shared)
+are checked on every output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.paged_step import DeviceStep, assert_close, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_76_gb300 import _lib
+    try:
+        _lib.lib()
+    except _lib.LibraryMissing:
+        from paged_kv_cache_76_gb300 import build
+        build.build()
+
+
+def _no_err():
+    from paged_kv_cache_76_gb300 import ops
+    assert ops.get_device_error() == 0
+
+
+def test_llama8b_gqa_decode_full_size():
+    wl = W.llama8b_gqa_decode()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    dev.run()
+    rows = list(range(0, 64, 4))
+    ref = oracle_step(wl, vals, decode_rows=rows, compact=True)
+    assert_close(dev.out_decode[rows], ref["decode"], "llama8b sampled")
+    _no_err()
+
+
+def test_long_context_splitk_decode_full_size():
+    wl = W.long_context_splitk_decode()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    dev.run()
+    row = int(np.argmin(wl.decode_lens))
+    ref = oracle_step(wl, vals, decode_rows=[row], compact=True)
+    assert_close(dev.out_decode[[row]], ref["decode"], "long context sampled")
+    # every output: a random relabelling of all physical blocks gives the same bits
+    out = dev.out_decode.clone()
+    pi = torch.randperm(wl.num_blocks, generator=torch.Generator().manual_seed(1)).cuda()
+    k2, v2 = torch.empty_like(dev.k_cache), torch.empty_like(dev.v_cache)
+    k2[pi] = dev.k_cache
+    v2[pi] = dev.v_cache
+    t2 = torch.where(dev.dec_tables >= 0, pi[dev.dec_tables.clamp(min=0).long()].int(), dev.dec_tables)
+    from paged_kv_cache_76_gb300 import ops
+    out2 = ops.decode(dev.q_decode, k2, v2, t2, dev.dec_lens, wl.scale, split_tokens=wl.split_tokens)
+    assert torch.equal(out, out2)
+    _no_err()
+
+
+def test_prefix_shared_cow_decode_full_size():
+    wl = W.prefix_shared_cow_decode()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    assert len(dev.pairs_host) == 26
+    dev.run()
+    cow_rows = sorted({int(op[1]) for op in wl.step_ops if op[0] == "cow"})[:8]
+    rows = sorted(set(cow_rows + list(range(0, 256, 16))))
+    ref = oracle_step(wl, vals, decode_rows=rows, compact=True)
+    assert_close(dev.out_decode[rows], ref["decode"], "prefix sampled")
+    # every output: the same step without the copies reads the shared block instead
+    wl2 = W.Workload(**{**wl.__dict__, "step_ops": [op for op in wl.step_ops if op[0] != "cow"]})
+    dev2 = DeviceStep(wl2, vals)
+    dev2.run()
+    assert torch.equal(dev.out_decode, dev2.out_decode)
+    _no_err()
+
+
+def test_mixed_prefill_decode_full_size():
+    wl = W.mixed_prefill_decode()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    dev.run()
+    dec_rows = list(range(0, 192, 24))
+    # prefill rows: first, last and a spread inside each 512-query chunk
+    pre_rows = sorted({512 * r + i for r in range(4) for i in (0, 1, 63, 64, 255, 256, 510, 511)})
+    ref = oracle_step(wl, vals, decode_rows=dec_rows, prefill_rows=pre_rows, compact=True)
+    assert_close(dev.out_decode[dec_rows], ref["decode"], "mixed decode sampled")
+    assert_close(dev.out_prefill[pre_rows], ref["prefill"][pre_rows], "mixed prefill sampled")
+    _no_err()
