@@ -140,7 +140,7 @@ class ClockSampler:
 class Step:
     """Device buffers and host copies of one workload step; runs it through the C ABI."""
 
-    def __init__(self, wl: W.Workload, device: torch.device, value_seed: int):
+    def __init__(self, wl: W.Workload, device: torch.device, value_seed: int, overlap_streams: bool = True):
         from paged_kv_cache_76_gb300 import ops
         from paged_kv_cache_76_gb300.allocator import BlockAllocator
         self.ops = ops
@@ -190,6 +190,10 @@ class Step:
             self.max_q_len = max(self.chunks)
         for k, v in self.h.items():
             self.d[k] = v.to(device, non_blocking=False)
+        self.side = None
+        if self.pre and self.dec and overlap_streams:
+            self.side = torch.cuda.Stream(device)
+            self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
         self.out_dec = torch.empty_like(self.d["q_decode"]) if self.dec else None
         self.out_pre = torch.empty_like(self.d["q_prefill"]) if self.pre else None
         self.h_out_dec = torch.empty(self.out_dec.shape, dtype=self.out_dec.dtype).pin_memory() if self.dec else None
@@ -201,7 +205,16 @@ class Step:
         if self.n_pairs:
             o.copy_blocks(self.k_cache, self.v_cache, d["pairs"], stream=stream)
         o.reshape_and_cache(d["k_new"], d["v_new"], d["slots"], self.k_cache, self.v_cache, stream=stream)
-        if self.pre:
+        overlap = self.pre and self.dec and self.side is not None
+        if overlap:
+            # prefill (tensor-bound) on a second stream, concurrent with decode (HBM-bound);
+            # both only read the cache this step's reshape_and_cache wrote
+            self.ev_fork.record(stream)
+            self.side.wait_event(self.ev_fork)
+            o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
+                              d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=self.side)
+            self.ev_join.record(self.side)
+        elif self.pre:
             o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
                               d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=stream)
         if self.dec:
@@ -213,6 +226,8 @@ class Step:
                 ev[1].record(stream)
             o.lse_merge(self.workspace, d["dec_lens"], d["q_decode"], d["dec_tables"], wl.block_size, self.out_dec,
                         split_tokens=self.split, stream=stream)
+        if overlap:
+            stream.wait_event(self.ev_join)
 
     def run_e2e(self, stream):
         """Host buffers in, host buffers out: copies inside the step."""
@@ -354,6 +369,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial", action="store_true", help="run prefill and decode on one stream, one after the other")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -375,7 +391,7 @@ def main():
     wl = W.WORKLOADS[args.workload]()
     if args.split is not None:
         wl.split_tokens = args.split
-    step = Step(wl, device, value_seed=1000 * rank)
+    step = Step(wl, device, value_seed=1000 * rank, overlap_streams=not args.serial)
     peak, peak_kind = measured_peaks()
 
     if args.impl == "reference":
@@ -482,6 +498,7 @@ def main():
             "bytes_per_step": nb,
             "l2": f"inputs larger than L2: {total_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2",
             "parallelism": f"replicas x{ws}",
+            "streams": "prefill on a second stream concurrent with decode" if step.side is not None else "one",
         },
         "gpu_launches": int(launches),
         "clocks": clk,

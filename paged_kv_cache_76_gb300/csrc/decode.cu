@@ -245,8 +245,11 @@ __global__ void __launch_bounds__(WARPS * 32)
       m[nt][1] = mn1;
       const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
       const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
-      lp[nt][0] = lp[nt][0] * al0 + (p0 + p2);
-      lp[nt][1] = lp[nt][1] * al1 + (p1 + p3);
+      // P is rounded to the input type for the P.V MMA; the denominator sums
+      // the same rounded values, so the output is an exact convex combination
+      const uint32_t pk01 = Elem<T>::pack(p0, p1), pk23 = Elem<T>::pack(p2, p3);
+      lp[nt][0] = lp[nt][0] * al0 + (Elem<T>::lo(pk01) + Elem<T>::lo(pk23));
+      lp[nt][1] = lp[nt][1] * al1 + (Elem<T>::hi(pk01) + Elem<T>::hi(pk23));
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
         acc[nt][mt][0] *= al0;
@@ -254,8 +257,8 @@ __global__ void __launch_bounds__(WARPS * 32)
         acc[nt][mt][2] *= al0;
         acc[nt][mt][3] *= al1;
       }
-      pb0[nt] = movmatrix_trans(Elem<T>::pack(p0, p1));
-      pb1[nt] = movmatrix_trans(Elem<T>::pack(p2, p3));
+      pb0[nt] = movmatrix_trans(pk01);
+      pb1[nt] = movmatrix_trans(pk23);
     }
 
 #pragma unroll

@@ -364,8 +364,11 @@ int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* con
   p.block_size = block_size;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int bsub = block_size < 16 ? block_size : 16;
-  return cuda_status(
-      launch_chunked_prefill(km, vm, p, head_dim, bsub, dtype, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  // blocks of >= 8 tokens: 5th-generation tensor cores (tcgen05 + TMEM);
+  // 4-token blocks: warp-level MMA kernel
+  if (bsub >= 8) return cuda_status(launch_chunked_prefill_tc(km, vm, p, head_dim, bsub, dtype, st_));
+  return cuda_status(launch_chunked_prefill(km, vm, p, head_dim, bsub, dtype, st_));
 }
 
 int pa_get_device_error(int32_t* host_code, pa_stream stream) {

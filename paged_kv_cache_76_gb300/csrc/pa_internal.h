@@ -86,6 +86,9 @@ cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vm
 cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_chunked_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
                                    int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
+// tcgen05/TMEM variant; needs bsub >= 8 (one 8-row swizzle atom per box)
+cudaError_t launch_chunked_prefill_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
+                                      int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
                                      void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,
                                      cudaStream_t stream);

@@ -241,15 +241,16 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     const float ala = exp2f(ma - ua), alb = exp2f(mb - ub);
     ma = mna;
     mb = mnb;
+    // P rounded to the input type for the P.V MMA; the denominators sum the
+    // same rounded values, so each output row is an exact convex combination
     float suma = 0.f, sumb = 0.f;
+    uint32_t pka[8], pkb[8];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      sc[nt][0] = exp2f(sc[nt][0] - ua);
-      sc[nt][1] = exp2f(sc[nt][1] - ua);
-      sc[nt][2] = exp2f(sc[nt][2] - ub);
-      sc[nt][3] = exp2f(sc[nt][3] - ub);
-      suma += sc[nt][0] + sc[nt][1];
-      sumb += sc[nt][2] + sc[nt][3];
+      pka[nt] = Elem<T>::pack(exp2f(sc[nt][0] - ua), exp2f(sc[nt][1] - ua));
+      pkb[nt] = Elem<T>::pack(exp2f(sc[nt][2] - ub), exp2f(sc[nt][3] - ub));
+      suma += Elem<T>::sum2(pka[nt]);
+      sumb += Elem<T>::sum2(pkb[nt]);
     }
     la = la * ala + suma;
     lb = lb * alb + sumb;
@@ -264,11 +265,7 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     // O += P V: 4 k-steps of 16 keys; P from the S accumulators in registers
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      uint32_t pa[4];
-      pa[0] = Elem<T>::pack(sc[2 * kk][0], sc[2 * kk][1]);
-      pa[1] = Elem<T>::pack(sc[2 * kk][2], sc[2 * kk][3]);
-      pa[2] = Elem<T>::pack(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-      pa[3] = Elem<T>::pack(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+      const uint32_t pa[4] = {pka[2 * kk], pkb[2 * kk], pka[2 * kk + 1], pkb[2 * kk + 1]};
 #pragma unroll
       for (int nd = 0; nd < DT8; nd += 2) {
         uint32_t b[4];
