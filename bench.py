@@ -188,16 +188,48 @@ class Step:
                                              dtype=torch.int32).pin_memory()
             self.h["q_prefill"] = vals["q_prefill"].cpu().pin_memory()
             self.max_q_len = max(self.chunks)
+        # One pinned staging buffer for every per-step input and one for the
+        # outputs, so an end-to-end step is a single host->device copy, the
+        # kernels, and a single device->host copy.
+        def layout(tensors):
+            offs, off = {}, 0
+            for k, v in tensors.items():
+                offs[k] = off
+                off += (v.numel() * v.element_size() + 255) // 256 * 256
+            return offs, max(off, 256)
+
+        def views(buf, offs, like):
+            return {k: buf[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+                    for k, v in like.items()}
+
+        offs, nbytes = layout(self.h)
+        self.h_stage = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        self.d_stage = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        hv = views(self.h_stage, offs, self.h)
         for k, v in self.h.items():
-            self.d[k] = v.to(device, non_blocking=False)
+            hv[k].copy_(v)
+        self.h = hv
+        self.d = views(self.d_stage, offs, self.h)
+        self.d_stage.copy_(self.h_stage)
+        outs = {}
+        if self.dec:
+            outs["dec"] = self.h["q_decode"]
+        if self.pre:
+            outs["pre"] = self.h["q_prefill"]
+        ooffs, obytes = layout(outs)
+        self.d_out = torch.empty(obytes, dtype=torch.uint8, device=device)
+        self.h_outbuf = torch.empty(obytes, dtype=torch.uint8).pin_memory()
+        self.out_used = sum(v.numel() * v.element_size() for v in outs.values())
+        dv = views(self.d_out, ooffs, outs)
+        hv = views(self.h_outbuf, ooffs, outs)
         self.side = None
         if self.pre and self.dec and overlap_streams:
             self.side = torch.cuda.Stream(device)
             self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
-        self.out_dec = torch.empty_like(self.d["q_decode"]) if self.dec else None
-        self.out_pre = torch.empty_like(self.d["q_prefill"]) if self.pre else None
-        self.h_out_dec = torch.empty(self.out_dec.shape, dtype=self.out_dec.dtype).pin_memory() if self.dec else None
-        self.h_out_pre = torch.empty(self.out_pre.shape, dtype=self.out_pre.dtype).pin_memory() if self.pre else None
+        self.out_dec = dv.get("dec")
+        self.out_pre = dv.get("pre")
+        self.h_out_dec = hv.get("dec")
+        self.h_out_pre = hv.get("pre")
 
     # -- one step through the C ABI; ev = (start, end) events around the decode partial kernel
     def run(self, stream, ev=None):
@@ -230,24 +262,13 @@ class Step:
             stream.wait_event(self.ev_join)
 
     def run_e2e(self, stream):
-        """Host buffers in, host buffers out: copies inside the step."""
-        for k, v in self.h.items():
-            if v.numel():
-                self.d[k].copy_(v, non_blocking=True)
+        """Host buffers in, host buffers out: one copy each way inside the step."""
+        self.d_stage.copy_(self.h_stage, non_blocking=True)
         self.run(stream)
-        if self.dec:
-            self.h_out_dec.copy_(self.out_dec, non_blocking=True)
-        if self.pre:
-            self.h_out_pre.copy_(self.out_pre, non_blocking=True)
+        self.h_outbuf.copy_(self.d_out, non_blocking=True)
 
     def e2e_bytes(self):
-        h2d = sum(v.numel() * v.element_size() for v in self.h.values())
-        d2h = 0
-        if self.dec:
-            d2h += self.h_out_dec.numel() * self.h_out_dec.element_size()
-        if self.pre:
-            d2h += self.h_out_pre.numel() * self.h_out_pre.element_size()
-        return h2d, d2h
+        return int(self.h_stage.numel()), int(self.h_outbuf.numel())
 
     # -- algorithmic bytes
     def bytes_breakdown(self):
@@ -448,19 +469,42 @@ def main():
         stream.synchronize()
         dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
 
-    # e2e: host buffers through the public API
+    # e2e: host buffers through the public API.  One step = H2D copy of the
+    # step's inputs (one pinned buffer) -> kernels -> D2H copy of its outputs,
+    # captured once as a CUDA graph and replayed with a host sync per step.
     e2e_val = None
     h2d, d2h = step.e2e_bytes()
+    e2e_mode = "cuda graph (H2D + step + D2H), host sync per step"
+    graph = None
     with torch.cuda.stream(stream):
-        for _ in range(5):
+        for _ in range(3):
             step.run_e2e(stream)
     stream.synchronize()
+    eager_out = step.h_outbuf.clone()  # the eager step's outputs, for checking a replay
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step.run_e2e(stream)
+        step.h_outbuf.zero_()
+        with torch.cuda.stream(stream):
+            graph.replay()  # replays on the current stream
+        stream.synchronize()
+        if ops.get_device_error(stream) != 0:
+            raise RuntimeError("device error in graph replay")
+        if not torch.equal(step.h_outbuf[:step.out_used], eager_out[:step.out_used]):
+            raise RuntimeError("graph replay output differs from the eager step")
+    except Exception as exc:  # capture not possible here: eager launches instead
+        graph = None
+        e2e_mode = f"eager launches, host sync per step (graph capture not used: {exc})"
     if ws > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(args.e2e_steps):
-            step.run_e2e(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                step.run_e2e(stream)
             stream.synchronize()
     e2e_s = time.perf_counter() - t0
     te = torch.tensor([e2e_s], dtype=torch.float64, device=device)
@@ -526,7 +570,7 @@ def main():
             res["roofline"]["achieved_unique"] = round(nb["decode_unique"] / (dec_ms * 1e-3) / 1e9, 1)
             res["roofline"]["frac_unique"] = round(nb["decode_unique"] / (dec_ms * 1e-3) / 1e9 / peak, 4)
     res["e2e"] = {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-                  "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+                  "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps, "mode": e2e_mode,
                   "ms_per_step": round(e2e_s / args.e2e_steps * 1e3, 4)}
     if rank == 0 and not args.no_cpu_baseline:
         units = oracle_units(step)
