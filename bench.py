@@ -140,7 +140,8 @@ class ClockSampler:
 class Step:
     """Device buffers and host copies of one workload step; runs it through the C ABI."""
 
-    def __init__(self, wl: W.Workload, device: torch.device, value_seed: int, overlap_streams: bool = True):
+    def __init__(self, wl: W.Workload, device: torch.device, value_seed: int, overlap_streams: bool = True,
+                 shared_prefix: bool = True):
         from paged_kv_cache_76_gb300 import ops
         from paged_kv_cache_76_gb300.allocator import BlockAllocator
         self.ops = ops
@@ -174,6 +175,16 @@ class Step:
             self.split = ops.decode_split_tokens(maxblk, wl.block_size, wl.split_tokens)
             n = ops.decode_workspace_size(len(wl.decode_seqs), wl.q_heads, wl.head_dim, maxblk, wl.block_size,
                                           self.split)
+            # a prefix every decode request shares (e.g. a common system prompt)
+            # goes through pa_decode_shared_prefix: read once for all queries
+            self.prefix_len = 0
+            if shared_prefix and wl.block_size >= 8 and len(wl.decode_seqs) >= 8:
+                nshared = a.common_prefix(wl.decode_seqs)
+                if nshared >= 8:
+                    self.prefix_len = nshared * wl.block_size
+                    self.h["prefix_blocks"] = torch.tensor(t[0, :nshared], dtype=torch.int32).pin_memory()
+                    n = ops.decode_shared_prefix_workspace_size(len(wl.decode_seqs), wl.q_heads, wl.head_dim, maxblk,
+                                                                wl.block_size, self.prefix_len, self.split)
             self.workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
         if self.pre:
             seqs = [s for s, _, _ in wl.prefill]
@@ -249,7 +260,15 @@ class Step:
         elif self.pre:
             o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
                               d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=stream)
-        if self.dec:
+        if self.dec and self.prefix_len:
+            if ev is not None:
+                ev[0].record(stream)
+            o.decode_shared_prefix(d["q_decode"], self.k_cache, self.v_cache, d["prefix_blocks"], self.prefix_len,
+                                   d["dec_tables"], d["dec_lens"], wl.scale, out=self.out_dec, split_tokens=self.split,
+                                   workspace=self.workspace, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+        elif self.dec:
             if ev is not None:
                 ev[0].record(stream)
             o.decode_partial(d["q_decode"], self.k_cache, self.v_cache, d["dec_tables"], d["dec_lens"], wl.scale,
@@ -391,6 +410,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--serial", action="store_true", help="run prefill and decode on one stream, one after the other")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="decode a shared prefix per request instead of once for the batch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -412,7 +433,8 @@ def main():
     wl = W.WORKLOADS[args.workload]()
     if args.split is not None:
         wl.split_tokens = args.split
-    step = Step(wl, device, value_seed=1000 * rank, overlap_streams=not args.serial)
+    step = Step(wl, device, value_seed=1000 * rank, overlap_streams=not args.serial,
+                shared_prefix=not args.no_shared_prefix)
     peak, peak_kind = measured_peaks()
 
     if args.impl == "reference":
@@ -547,7 +569,28 @@ def main():
         "gpu_launches": int(launches),
         "clocks": clk,
     }
-    if step.dec:
+    if step.dec and step.prefix_len:
+        ub = nb["decode_unique"]
+        flops = 4 * len(wl.decode_seqs) * wl.q_heads * wl.head_dim * step.prefix_len
+        res["roofline"] = {
+            "kernel": "pa_decode_shared_prefix (tcgen05 prefix pass + suffix decode + merge)",
+            "bound": "hbm",
+            "achieved": round(ub / (dec_ms * 1e-3) / 1e9, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(ub / (dec_ms * 1e-3) / 1e9 / peak, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": ub,
+            "logical_bytes_per_launch": nb["decode"],
+            "achieved_logical": round(nb["decode"] / (dec_ms * 1e-3) / 1e9, 1),
+            "prefix_tokens": step.prefix_len,
+            "prefix_tflops": round(flops / (dec_ms * 1e-3) / 1e12, 1),
+            "avg_launch_ms": round(dec_ms, 5),
+            "timing": "CUDA events around each of K pa_decode_shared_prefix calls (3 kernels) on the bench "
+                      "stream, in a second pass of the same K steps",
+        }
+    elif step.dec:
         dec_bytes = nb["decode"]
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
         traffic = kernel_traffic(f"decode_partial_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/decode.cu")

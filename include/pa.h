@@ -180,6 +180,39 @@ int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* c
                  int split_tokens, void* out, pa_dtype dtype, pa_stream stream);
 
 /* ----------------------------------------------------------------------------
+ * pa_decode_shared_prefix - decode for a batch whose requests all start with
+ * the same physical blocks (a shared prompt prefix).
+ *
+ * "2.1 PagedAttention" §6: with paging, many Block Tables point at the same
+ * physical blocks of a common prefix.  Instead of reading those blocks once per
+ * request, this call attends the prefix once for every request's queries:
+ * rows (request, query head of the group) x prefix keys are dense tiles for the
+ * 5th-generation tensor cores, split into key ranges of 512 tokens, each
+ * producing a log-sum-exp partial; each request's own suffix (tokens
+ * prefix_len .. context_lens[r]-1) runs through the paged decode kernel into
+ * further partials; the merge combines them.  The result equals pa_decode
+ * with the full tables, up to floating-point rounding.
+ *   prefix_blocks  int32 [prefix_len / block_size], DEVICE memory: the shared
+ *                  physical blocks in logical order.  Every row of
+ *                  block_tables must begin with them (checked on the device:
+ *                  a mismatch records PA_DEVERR_BLOCK_ID).
+ *   prefix_len     host int, > 0, a multiple of block_size, <= every
+ *                  context_lens[r] (a shorter context records
+ *                  PA_DEVERR_CONTEXT_LEN).  pa_alloc_common_prefix gives the
+ *                  number of shared full blocks of a set of sequences.
+ *   workspace      at least pa_decode_shared_prefix_workspace_size(...) bytes.
+ * Other arguments as pa_decode.  With 4-token blocks this is pa_decode.
+ * ------------------------------------------------------------------------- */
+size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq,
+                                              int block_size, int prefix_len, int split_tokens);
+
+int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* prefix_blocks,
+                            int prefix_len, const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads, int head_dim,
+                            int block_size, int num_blocks, float scale, int split_tokens, void* workspace,
+                            size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
  * pa_chunked_prefill - a chunk of prompt tokens per request attends its paged
  * history plus itself, causally.
  *
@@ -304,6 +337,9 @@ int pa_alloc_block_table(const pa_alloc* a, int seq_id, int32_t* out, int cap, i
 int pa_alloc_build_tables(const pa_alloc* a, const int* seq_ids, int n, int32_t* out,
                           int max_blocks_per_seq, int32_t* lens_out);
 
+/* Number of leading FULL blocks that all of seq_ids[0..n) hold in common (same
+ * physical ids, in order): the shared prefix pa_decode_shared_prefix can use. */
+int pa_alloc_common_prefix(const pa_alloc* a, const int* seq_ids, int n, int* n_blocks_out);
 int pa_alloc_seq_len(const pa_alloc* a, int seq_id, int64_t* n_tokens_out);
 int pa_alloc_num_free(const pa_alloc* a);
 /* Refcount of block_id, or PA_ERR_INVALID if it is out of range. */

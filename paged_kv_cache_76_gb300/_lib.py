@@ -68,6 +68,9 @@ PROTOTYPES = {
     "pa_lse_merge": (_I, [_P, _SZ, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P]),
     "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
     "pa_chunked_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "pa_decode_shared_prefix_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "pa_decode_shared_prefix": (_I, [_P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I,
+                                     _P]),
     "pa_get_device_error": (_I, [_I32P, _P]),
     "pa_alloc_create": (_I, [_I, _I, _I32P, C.POINTER(_P)]),
     "pa_alloc_destroy": (None, [_P]),
@@ -78,6 +81,7 @@ PROTOTYPES = {
     "pa_alloc_free_seq": (_I, [_P, _I]),
     "pa_alloc_block_table": (_I, [_P, _I, _I32P, _I, C.POINTER(_I)]),
     "pa_alloc_build_tables": (_I, [_P, C.POINTER(_I), _I, _I32P, _I, _I32P]),
+    "pa_alloc_common_prefix": (_I, [_P, C.POINTER(_I), _I, C.POINTER(_I)]),
     "pa_alloc_seq_len": (_I, [_P, _I, C.POINTER(C.c_int64)]),
     "pa_alloc_num_free": (_I, [_P]),
     "pa_alloc_ref": (_I, [_P, _I]),

@@ -91,6 +91,14 @@ class BlockAllocator:
                                            int(max_blocks_per_seq), _i32p(lens)), "pa_alloc_build_tables")
         return tables, lens
 
+    def common_prefix(self, seqs) -> int:
+        """Leading full blocks all of ``seqs`` share (same physical ids)."""
+        ids = np.ascontiguousarray(seqs, dtype=np.intc)
+        n = C.c_int(0)
+        _chk(self._L.pa_alloc_common_prefix(self._h, ids.ctypes.data_as(C.POINTER(C.c_int)), ids.shape[0],
+                                            C.byref(n)), "pa_alloc_common_prefix")
+        return int(n.value)
+
     def seq_len(self, seq: int) -> int:
         v = C.c_int64(0)
         _chk(self._L.pa_alloc_seq_len(self._h, int(seq), C.byref(v)), "pa_alloc_seq_len")

@@ -229,6 +229,23 @@ int pa_alloc_build_tables(const pa_alloc* a, const int* seq_ids, int n, int32_t*
   return PA_OK;
 }
 
+int pa_alloc_common_prefix(const pa_alloc* a, const int* seq_ids, int n, int* n_blocks_out) {
+  if (!a || n <= 0 || !seq_ids || !n_blocks_out) return PA_ERR_INVALID;
+  const Seq* first = a->find(seq_ids[0]);
+  if (!first) return PA_ERR_INVALID;
+  int64_t common = first->num_tokens / a->block_size;  // full blocks only
+  for (int i = 1; i < n; ++i) {
+    const Seq* s = a->find(seq_ids[i]);
+    if (!s) return PA_ERR_INVALID;
+    common = std::min<int64_t>(common, s->num_tokens / a->block_size);
+    int64_t k = 0;
+    while (k < common && s->blocks[k] == first->blocks[k]) ++k;
+    common = k;
+  }
+  *n_blocks_out = (int)common;
+  return PA_OK;
+}
+
 int pa_alloc_seq_len(const pa_alloc* a, int seq_id, int64_t* n_tokens_out) {
   if (!a || !n_tokens_out) return PA_ERR_INVALID;
   const Seq* s = a->find(seq_id);

@@ -89,15 +89,17 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int c = u / p.kv_heads;
   const int cap = p.maxblk * p.block_size;
   int ctx = __ldg(p.lens + r);
-  const bool bad_len = ctx < 0 || ctx > cap;
-  ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-  const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
-  const bool active = c < (nsplit > 0 ? nsplit : 1);
+  // tokens [tok_begin, ctx) are this kernel's (tok_begin > 0: the suffix
+  // after a shared prefix attended elsewhere)
+  const bool bad_len = ctx < p.tok_begin || ctx > cap;
+  ctx = ctx < p.tok_begin ? p.tok_begin : (ctx > cap ? cap : ctx);
+  const int nsplit = (ctx - p.tok_begin + p.split_tokens - 1) / p.split_tokens;
+  const bool active = c < (nsplit > 0 ? nsplit : (p.always_partial ? 0 : 1));
   const int G = p.group;
   const int qh0 = h * G;
-  const int tok0 = c * p.split_tokens;
+  const int tok0 = p.tok_begin + c * p.split_tokens;
   const int tok1 = min(tok0 + p.split_tokens, ctx);
-  const int ntiles = active && ctx > 0 ? (tok1 - tok0 + 15) >> 4 : 0;
+  const int ntiles = active && ctx > tok0 ? (tok1 - tok0 + 15) >> 4 : 0;
   const int blk0 = tok0 / p.block_size;
 
   // Set-up that reads only this call's immutable inputs (block table slice,
@@ -136,6 +138,12 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
       }
     }
+  }
+  // shared-prefix mode: each table must start with the prefix blocks
+  if (p.prefix_blocks && c == 0 && h == 0) {
+    const int32_t* trow0 = p.tables + (size_t)r * p.maxblk;
+    for (int i = lane; i < p.prefix_nblk; i += 32)
+      if (__ldg(trow0 + i) != __ldg(p.prefix_blocks + i)) bad_id = true;
   }
   griddep_wait();
   if (bad_len && lane == 0) record_error(p.err, PA_DEVERR_CONTEXT_LEN);
@@ -291,7 +299,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       lp[nt][e] = l;
     }
 
-  if (nsplit == 1) {
+  if (nsplit == 1 && !p.always_partial) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -315,15 +323,16 @@ __global__ void __launch_bounds__(WARPS * 32)
         const int hd = nt * 8 + 2 * (lane & 3) + e;
         if (hd < G) {
           const size_t row = (size_t)r * p.q_heads + qh0 + hd;
-          float* po = p.part_o + (row * p.max_splits + c) * D;
+          const int slot = p.slot_base + c;
+          float* po = p.part_o + (row * p.max_splits + slot) * D;
 #pragma unroll
           for (int mt = 0; mt < KSTEPS; ++mt) {
             po[mt * 16 + r0] = acc[nt][mt][e];
             po[mt * 16 + r0 + 8] = acc[nt][mt][2 + e];
           }
           if (r0 == 0) {
-            p.part_m[row * p.max_splits + c] = m[nt][e];
-            p.part_l[row * p.max_splits + c] = lp[nt][e];
+            p.part_m[row * p.max_splits + slot] = m[nt][e];
+            p.part_l[row * p.max_splits + slot] = lp[nt][e];
           }
         }
       }
@@ -349,9 +358,9 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
   if (row >= p.num_seqs * p.q_heads) return;
   const int r = row / p.q_heads;
   int ctx = __ldg(p.lens + r);
-  ctx = ctx < 0 ? 0 : (ctx > p.cap ? p.cap : ctx);
-  const int nsplit = (ctx + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit <= 1) return;  // pa_decode_partial wrote this row directly
+  ctx = ctx < p.tok_begin ? p.tok_begin : (ctx > p.cap ? p.cap : ctx);
+  const int nsplit = p.extra_slots + (ctx - p.tok_begin + p.split_tokens - 1) / p.split_tokens;
+  if (nsplit <= 1 && !p.always) return;  // pa_decode_partial wrote this row directly
   const float* pm = p.part_m + (size_t)row * p.max_splits;
   const float* pl = p.part_l + (size_t)row * p.max_splits;
   const float* po = p.part_o + (size_t)row * p.max_splits * D + lane * V;
@@ -409,7 +418,7 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int units = p.max_splits * p.kv_heads;
+  const int units = p.grid_splits * p.kv_heads;
   dim3 grid((units + W - 1) / W, p.num_seqs);
   return launch_pdl(kern, grid, dim3(W * 32), L::bytes(p.tab_entries), stream, kmap, vmap, p);
 }

@@ -161,6 +161,32 @@ int decode_setup(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq
   return PA_OK;
 }
 
+// Shared-prefix decode: the prefix is cut into key ranges of kPrefixKeySplit
+// (one partial slot each), the suffix into decode partitions after them.
+constexpr int kPrefixKeySplit = 512;
+
+struct SharedPrefixSetup {
+  int split, prefix_splits, suffix_splits, max_splits;
+  DecodeWorkspace ws;
+};
+
+int shared_prefix_setup(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq, int block_size,
+                        int prefix_len, int split_tokens, SharedPrefixSetup* s) {
+  if (num_seqs < 0 || q_heads <= 0 || head_dim <= 0) return PA_ERR_INVALID;
+  const int split = pa_decode_split_tokens(max_blocks_per_seq, block_size, split_tokens);
+  if (split <= 0) return PA_ERR_INVALID;
+  const int64_t cap = (int64_t)max_blocks_per_seq * block_size;
+  if (cap > INT32_MAX || prefix_len <= 0 || prefix_len > cap || prefix_len % block_size != 0) return PA_ERR_INVALID;
+  s->split = split;
+  s->prefix_splits = (prefix_len + kPrefixKeySplit - 1) / kPrefixKeySplit;
+  const int64_t suffix = cap - prefix_len;
+  s->suffix_splits = (int)((suffix + split - 1) / split);
+  if (s->suffix_splits < 1) s->suffix_splits = 1;
+  s->max_splits = s->prefix_splits + s->suffix_splits;
+  s->ws = decode_workspace_layout(num_seqs, q_heads, head_dim, s->max_splits);
+  return PA_OK;
+}
+
 }  // namespace
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
@@ -279,6 +305,7 @@ int pa_decode_partial(const void* q, const void* k_cache, const void* v_cache, c
   p.block_size = block_size;
   p.split_tokens = s.split;
   p.max_splits = s.max_splits;
+  p.grid_splits = s.max_splits;
   p.tab_entries = s.split / block_size;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int bsub = block_size < 16 ? block_size : 16;
@@ -363,12 +390,135 @@ int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* con
   p.num_blocks = num_blocks;
   p.block_size = block_size;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = 1;
   const int bsub = block_size < 16 ? block_size : 16;
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   // blocks of >= 8 tokens: 5th-generation tensor cores (tcgen05 + TMEM);
   // 4-token blocks: warp-level MMA kernel
   if (bsub >= 8) return cuda_status(launch_chunked_prefill_tc(km, vm, p, head_dim, bsub, dtype, st_));
   return cuda_status(launch_chunked_prefill(km, vm, p, head_dim, bsub, dtype, st_));
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq,
+                                              int block_size, int prefix_len, int split_tokens) {
+  if (block_size < 8)  // 4-token blocks: plain pa_decode is used
+    return pa_decode_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens);
+  SharedPrefixSetup s;
+  if (shared_prefix_setup(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, prefix_len, split_tokens,
+                          &s) != PA_OK)
+    return 0;
+  return s.ws.bytes;
+}
+
+int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* prefix_blocks,
+                            int prefix_len, const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads, int head_dim,
+                            int block_size, int num_blocks, float scale, int split_tokens, void* workspace,
+                            size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
+  int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || q_heads <= 0 || q_heads % kv_heads != 0 || q_heads / kv_heads > 16)
+    return PA_ERR_INVALID;
+  if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PA_ERR_INVALID;
+  if (prefix_len <= 0 || prefix_len % block_size != 0 || prefix_len > max_blocks_per_seq * block_size)
+    return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (block_size < 8)  // no tensor-core prefix pass for 4-token blocks: same result through pa_decode
+    return pa_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, q_heads, kv_heads,
+                     head_dim, block_size, num_blocks, scale, split_tokens, workspace, workspace_bytes, out, dtype,
+                     stream);
+  if (!q || !k_cache || !v_cache || !prefix_blocks || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID;
+  SharedPrefixSetup s;
+  st = shared_prefix_setup(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, prefix_len, split_tokens, &s);
+  if (st != PA_OK) return st;
+  if (!workspace || workspace_bytes < s.ws.bytes || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  CUtensorMap km, vm;
+  if (!kv_map(k_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &km) ||
+      !kv_map(v_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &vm))
+    return PA_ERR_CUDA;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* po = reinterpret_cast<float*>(ws + s.ws.o_off);
+  float* pm = reinterpret_cast<float*>(ws + s.ws.m_off);
+  float* pl = reinterpret_cast<float*>(ws + s.ws.l_off);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int bsub = block_size < 16 ? block_size : 16;
+  const int G = q_heads / kv_heads;
+  const float sl2 = scale * 1.4426950408889634f;
+
+  // 1. the shared prefix, once for every request's queries (tensor cores)
+  PrefillParams pp{};
+  pp.q = q;
+  pp.tables = prefix_blocks;
+  pp.err = err;
+  pp.maxblk = prefix_len / block_size;
+  pp.num_reqs = 1;
+  pp.total_q = num_seqs;
+  pp.max_q_len = num_seqs;
+  pp.q_heads = q_heads;
+  pp.kv_heads = kv_heads;
+  pp.group = G;
+  pp.num_blocks = num_blocks;
+  pp.block_size = block_size;
+  pp.scale_log2 = sl2;
+  pp.causal = 0;
+  pp.prefix_len = prefix_len;
+  pp.key_split = kPrefixKeySplit;
+  pp.max_splits = s.max_splits;
+  pp.part_o = po;
+  pp.part_m = pm;
+  pp.part_l = pl;
+  st = cuda_status(launch_chunked_prefill_tc(km, vm, pp, head_dim, bsub, dtype, cs));
+  if (st != PA_OK) return st;
+
+  // 2. each request's own suffix (paged decode, partials after the prefix's)
+  DecodeParams dp{};
+  dp.q = q;
+  dp.tables = block_tables;
+  dp.lens = context_lens;
+  dp.out = out;
+  dp.part_o = po;
+  dp.part_m = pm;
+  dp.part_l = pl;
+  dp.err = err;
+  dp.maxblk = max_blocks_per_seq;
+  dp.num_seqs = num_seqs;
+  dp.q_heads = q_heads;
+  dp.kv_heads = kv_heads;
+  dp.group = G;
+  dp.num_blocks = num_blocks;
+  dp.block_size = block_size;
+  dp.split_tokens = s.split;
+  dp.max_splits = s.max_splits;
+  dp.grid_splits = s.suffix_splits;
+  dp.tab_entries = s.split / block_size;
+  dp.scale_log2 = sl2;
+  dp.tok_begin = prefix_len;
+  dp.slot_base = s.prefix_splits;
+  dp.always_partial = 1;
+  dp.prefix_blocks = prefix_blocks;
+  dp.prefix_nblk = prefix_len / block_size;
+  st = cuda_status(launch_decode_partial(km, vm, dp, head_dim, bsub, dtype, cs));
+  if (st != PA_OK) return st;
+
+  // 3. log-sum-exp merge of prefix and suffix partials
+  MergeParams mp{};
+  mp.part_o = po;
+  mp.part_m = pm;
+  mp.part_l = pl;
+  mp.lens = context_lens;
+  mp.out = out;
+  mp.num_seqs = num_seqs;
+  mp.q_heads = q_heads;
+  mp.max_splits = s.max_splits;
+  mp.split_tokens = s.split;
+  mp.cap = max_blocks_per_seq * block_size;
+  mp.tok_begin = prefix_len;
+  mp.extra_slots = s.prefix_splits;
+  mp.always = 1;
+  return cuda_status(launch_lse_merge(mp, head_dim, dtype, cs));
 }
 
 int pa_get_device_error(int32_t* host_code, pa_stream stream) {

@@ -49,6 +49,13 @@ struct DecodeParams {
   int maxblk, num_seqs, q_heads, kv_heads, group, num_blocks, block_size, split_tokens, max_splits;
   int tab_entries;  // block-table entries per partition: split_tokens / block_size
   float scale_log2;
+  // Shared-prefix mode: attend only tokens [tok_begin, context_len) (the
+  // request's own suffix), always write partials, to slots slot_base + c, and
+  // check that each table starts with the prefix blocks.
+  int tok_begin, slot_base, always_partial;
+  const int32_t* prefix_blocks;
+  int prefix_nblk;
+  int grid_splits;  // partitions the grid covers (normal mode: max_splits)
 };
 
 struct MergeParams {
@@ -58,6 +65,9 @@ struct MergeParams {
   const int32_t* lens;
   void* out;
   int num_seqs, q_heads, max_splits, split_tokens, cap;
+  // shared-prefix mode: extra_slots partials precede the suffix partitions of
+  // [tok_begin, context_len); every row is merged (even a single slot)
+  int tok_begin, extra_slots, always;
 };
 
 struct PrefillParams {
@@ -69,6 +79,16 @@ struct PrefillParams {
   int* err;
   int maxblk, num_reqs, total_q, max_q_len, q_heads, kv_heads, group, num_blocks, block_size;
   float scale_log2;
+  // Shared-prefix mode (tcgen05 kernel only; causal == 0): one virtual request
+  // whose total_q "queries" are the decode queries of a batch, all seeing keys
+  // [0, prefix_len) of the prefix table (`tables`, one row); grid.z splits the
+  // keys into ranges of key_split; each range writes an unnormalised partial
+  // (o, m in log2 units, l) to slot blockIdx.z of the decode workspace.
+  int causal;
+  int prefix_len, key_split, max_splits;
+  float* part_o;
+  float* part_m;
+  float* part_l;
 };
 
 // Workspace carve-up for decode partials.

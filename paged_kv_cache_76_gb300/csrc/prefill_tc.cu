@@ -94,38 +94,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.z, h = blockIdx.y;
+  const int h = blockIdx.y;
   const int row0 = blockIdx.x * kTcRows;
   const int G = p.group;
 
-  // request geometry (uniform across the CTA); only immutable inputs are read
-  const int qs = __ldg(p.q_start + r), qe = __ldg(p.q_start + r + 1);
-  const int chunk = qe - qs;
-  const int ctx = __ldg(p.lens + r);
-  const int p0 = ctx - chunk;
-  if (qs < 0 || qe < qs || qe > p.total_q || chunk > p.max_q_len || p0 < 0 || ctx > p.maxblk * p.block_size) {
-    griddep_wait();
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
-    return;
+  // geometry (uniform across the CTA); only immutable inputs are read.
+  // Causal mode: request r = blockIdx.z, its chunk starts at absolute position
+  // p0, row (query i, head g) sees keys 0 .. p0+i.  Shared-prefix mode: one
+  // virtual request of total_q queries (the decode batch), keys
+  // [k0, kend) = split blockIdx.z of the prefix, all visible to every row.
+  int r, qs, chunk, p0, k0, kend;
+  if (p.causal) {
+    r = blockIdx.z;
+    qs = __ldg(p.q_start + r);
+    const int qe = __ldg(p.q_start + r + 1);
+    chunk = qe - qs;
+    const int ctx = __ldg(p.lens + r);
+    p0 = ctx - chunk;
+    if (qs < 0 || qe < qs || qe > p.total_q || chunk > p.max_q_len || p0 < 0 || ctx > p.maxblk * p.block_size) {
+      griddep_wait();
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
+      return;
+    }
+    k0 = 0;
+    const int last_row = min(row0 + kTcRows, chunk * G) - 1;
+    kend = p0 + last_row / G + 1;  // keys [0, kend) are visible to some row
+  } else {
+    r = 0;
+    qs = 0;
+    chunk = p.total_q;
+    p0 = 0;
+    k0 = blockIdx.z * p.key_split;
+    kend = min(k0 + p.key_split, p.prefix_len);
   }
   const int rows = chunk * G;
-  if (row0 >= rows) {
+  if (row0 >= rows || k0 >= kend) {
     griddep_wait();
     return;
   }
-  const int last_row = min(row0 + kTcRows, rows) - 1;
-  const int kmax = p0 + last_row / G + 1;  // keys [0, kmax) are visible to some row
-  const int ntiles = (kmax + kTcKeys - 1) / kTcKeys;
+  const int ntiles = (kend - k0 + kTcKeys - 1) / kTcKeys;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTcStages; ++i) {
       mbar_init(bar(B_KFULL + i), 1);
       mbar_init(bar(B_VFULL + i), 1);
       mbar_init(bar(B_KVEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_SEMPTY + i), 4);
       mbar_init(bar(B_PFULL + i), 4);
-
     }
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_QFULL), 4);
@@ -147,7 +165,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     const int32_t* trow = p.tables + (size_t)r * p.maxblk;
-    const int need_blocks = (kmax + p.block_size - 1) / p.block_size;
+    const int need_blocks = (kend + p.block_size - 1) / p.block_size;
     const uint64_t pol = policy_evict_last();  // K/V tiles are re-read by the other row tiles
     int chunk_base = -kTcTableChunk;
     int issued = 0;
@@ -159,8 +177,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         failed = true;
         break;
       }
-      const int ts = j * kTcKeys;
-      const int nvalid = min(kTcKeys, kmax - ts);
+      const int ts = k0 + j * kTcKeys;
+      const int nvalid = min(kTcKeys, kend - ts);
       const int nsub = (nvalid + BSUB - 1) / BSUB;
       const int lb_first = ts / p.block_size;
       const int lb_last = (ts + nvalid - 1) / p.block_size;
@@ -253,7 +271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int grow = row0 + row;
     const bool valid = grow < rows;
     const int qi = grow / G, g = grow % G;
-    const int lim = valid ? p0 + qi : -1;    // last key this row may see
+    const int lim = !valid ? -1 : (p.causal ? p0 + qi : kend - 1);  // last key this row may see
     // Q row -> shared memory (K-major, 128-byte swizzle); padding rows are zero
     {
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.q) +
@@ -279,7 +297,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int b = j & 1, s = j % kTcStages;
       if (!mbar_wait(bar(B_SFULL + b), (j >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      const int ts = j * kTcKeys;
+      const int ts = k0 + j * kTcKeys;
       // every row of this warp sees every key of the tile: no mask needed
       const bool all_full = __all_sync(0xffffffffu, ts + kTcKeys - 1 <= lim);
       const uint32_t scol = tmem + lane_addr + S_COL + b * kTcKeys;
@@ -351,9 +369,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       l += sum;
-      const int nvalid = min(kTcKeys, kmax - ts);
+      const int nvalid = min(kTcKeys, kend - ts);
       if (nvalid < kTcKeys) {
-        // last tile: keys past kmax were loaded from stale slots (or not at
+        // last tile: keys past kend were loaded from stale slots (or not at
         // all); zero their V rows so that p = 0 never meets NaN/Inf
         if (!mbar_wait(bar(B_VFULL + s), (j / kTcStages) & 1)) { ok = false; break; }
         if (row >= nvalid) {
@@ -372,7 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (ok && ntiles > 0) ok = mbar_wait(bar(B_OFULL), (ntiles - 1) & 1);
     if (!ok) {
       if (lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
-    } else {
+    } else if (p.causal) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
@@ -390,6 +408,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                         Elem<T>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
                                         Elem<T>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
         }
+      }
+      tc_fence_before();
+    } else {
+      // shared-prefix partial of this key range: unnormalised o, m, l
+      tc_fence_after();
+      const size_t prow = ((size_t)qi * p.q_heads + h * G + g) * p.max_splits + blockIdx.z;
+      float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tmem_ld32(ocol + 32 * c, ov);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) po[8 * c + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+        }
+      }
+      if (valid) {
+        p.part_m[prow] = m;
+        p.part_l[prow] = l;
       }
       tc_fence_before();
     }
@@ -419,7 +457,8 @@ cudaError_t launch_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
     attr_set[dev] = true;
   }
   const int row_tiles = (p.max_q_len * p.group + kTcRows - 1) / kTcRows;
-  dim3 grid(row_tiles, p.kv_heads, p.num_reqs);
+  const int zdim = p.causal ? p.num_reqs : (p.prefix_len + p.key_split - 1) / p.key_split;
+  dim3 grid(row_tiles, p.kv_heads, zdim);
   return launch_pdl(kern, grid, dim3(kTcThreads), L::BYTES, stream, kmap, vmap, p);
 }
 

@@ -23,6 +23,8 @@ __all__ = [
     "decode_split_tokens",
     "decode_workspace_size",
     "chunked_prefill",
+    "decode_shared_prefix",
+    "decode_shared_prefix_workspace_size",
     "get_device_error",
     "launch_count",
     "dtype_code",
@@ -139,6 +141,33 @@ def lse_merge(workspace, context_lens, q, block_tables, block_size, out, split_t
     check(_lib.lib().pa_lse_merge(ws_ptr, ws_bytes, _i32(context_lens, "context_lens"), B, hq, d,
                                   int(block_tables.shape[1]), block_size, int(split_tokens), _dev(out, "out"),
                                   dtype_code(out.dtype), _stream(stream)), "pa_lse_merge")
+
+
+def decode_shared_prefix_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, prefix_len,
+                                        split_tokens=0) -> int:
+    return int(_lib.lib().pa_decode_shared_prefix_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq,
+                                                                 block_size, prefix_len, split_tokens))
+
+
+def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_tables, context_lens, scale, out=None,
+                         split_tokens=0, workspace=None, stream=None):
+    """pa_decode_shared_prefix: decode whose requests share ``prefix_blocks`` (int32, device)."""
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    B, hq, dq = q.shape
+    if dq != d or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    maxblk = int(block_tables.shape[1])
+    if workspace is None:
+        n = decode_shared_prefix_workspace_size(B, hq, d, maxblk, bs, int(prefix_len), split_tokens)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    check(_lib.lib().pa_decode_shared_prefix(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(prefix_blocks, "prefix_blocks"),
+        int(prefix_len), _i32(block_tables, "block_tables"), maxblk, _i32(context_lens, "context_lens"), B, hq, hkv,
+        d, bs, nb, float(scale), int(split_tokens), workspace.data_ptr(), workspace.numel(), _dev(out, "out"),
+        dtype_code(q.dtype), _stream(stream)), "pa_decode_shared_prefix")
+    return out
 
 
 def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, scale, max_q_len, out=None,

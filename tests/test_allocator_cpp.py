@@ -188,3 +188,23 @@ def test_allocator_under_address_and_ub_sanitizers(tmp_path):
     r = subprocess.run([str(exe), "8000"], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "ok" in r.stdout
+
+
+def test_common_prefix_counts_shared_full_blocks():
+    c = BlockAllocator(64, 4)
+    c.add_seq(0)
+    c.append_slots(0, 22)                 # 5 full blocks + 2 tokens
+    for s, n in ((1, 22), (2, 16), (3, 9)):
+        c.add_seq(s)
+        c.share(s, 0, n)
+    assert c.common_prefix([0, 1]) == 5                # the partial 6th block does not count
+    assert c.common_prefix([0, 1, 2]) == 4
+    assert c.common_prefix([0, 3]) == 2
+    assert c.common_prefix([1]) == 5
+    c.cow(1, 1)                                        # seq 1's second block becomes private
+    assert c.common_prefix([0, 1]) == 1
+    c.add_seq(9)
+    c.append_slots(9, 8)
+    assert c.common_prefix([0, 9]) == 0
+    with pytest.raises(_lib.PAError):
+        c.common_prefix([0, 12345])
