@@ -1,0 +1,491 @@
+// Paged attention of many query rows on the 5th-generation tensor cores
+// (tcgen05 + tensor memory), sm_103a, for blocks of >= 8 tokens: chunked
+// prefill (causal) and the shared-prefix pass of a decode batch (partials).
+//
+// A CTA owns two tiles of 128 rows (A and B) of one (request, KV head); a row
+// is one (query, head of the GQA group) pair, so the whole group shares every
+// K/V tile, and each 128-key K/V tile gathered from the paged cache serves
+// 256 rows.
+//
+// Design points, each measured on GB300:
+//  * S = Q K^T uses N = 128 keys per instruction: at N = 64 an SS MMA is bound
+//    by its 6 KB of shared-memory operand reads and runs at 2/3 rate.
+//  * P stays in tensor memory: the softmax writes P (bf16/fp16) over the
+//    first half of its S columns and O += P V reads A from TMEM, so P never
+//    crosses shared memory (about a quarter of the per-tile SMEM traffic).
+//  * Three producer warps issue the TMA gather: one warp issuing 16-row
+//    boxes moves about 27 B/clk per SM, several warps together more.
+//  * The softmax holds its whole S row in registers (one TMEM round trip per
+//    tile) and uses packed f32x2 arithmetic.
+//
+// Warp roles (384 threads = 12 warps, so that each thread may hold 168
+// registers; one CTA per SM):
+//   warp 0      MMA issuer (one thread), per key tile j:
+//                 S_A(j), S_B(j), P.V_A(j), P.V_B(j)
+//               S_x(j) overwrites P_x(j-1), so it is issued once P.V_x(j-1)
+//               has completed (which overlaps the other tile's MMAs).
+//   warps 1,2   TMA producers of K (half of the tile's blocks each), warp 3
+//               of V; separate 2-stage K and V rings, so a K slot frees as
+//               soon as both S MMAs have read it.
+//   warps 4..7  softmax of tile A, warps 8..11 of tile B: thread = TMEM lane
+//               = row.  It loads its S row, takes the row maximum, writes
+//               P = 2^(s*scale*log2e - m) into TMEM and sums it.  The running
+//               maximum m is raised only when a row maximum exceeds it by
+//               more than 2^8 (O is then rescaled in TMEM); the final O / sum
+//               uses the same m, so this is exact.
+// Q and K are K-major and V is MN-major in the canonical 128-byte-swizzled
+// shared-memory layouts.  Every mbarrier wait is bounded.
+#include <float.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kRows = 128;  // rows per Q tile (M of every MMA)
+constexpr int kKeys = 128;  // keys per K/V tile (N of S, K of P.V)
+constexpr int kKvStages = 2;
+constexpr int kMmaWarp = 0;
+constexpr int kVWarp = 3;  // warps 1, 2: K
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kThreads = 32 * 12;
+constexpr uint32_t kTmem = 512;
+
+__device__ __forceinline__ uint8_t* align1024_tc(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int D, int BSUB>
+struct TcSmem {
+  using Tile = KvTile<D, BSUB, kKeys>;  // D/64 halves x 128 rows x 128 B
+  static constexpr int NH = D / 64;
+  static constexpr int QHALF = kRows * 128;
+  static constexpr int QTILE = NH * QHALF;
+  static constexpr int Q_OFF = 0;  // Q_A, Q_B
+  static constexpr int K_OFF = Q_OFF + 2 * QTILE;
+  static constexpr int V_OFF = K_OFF + kKvStages * Tile::BYTES;
+  static constexpr int BAR_OFF = V_OFF + kKvStages * Tile::BYTES;
+  static constexpr int NBARS = 16;
+  static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int BYTES = SLOT_OFF + 16 + 1024;
+  static_assert(BSUB * 128 >= 1024, "needs blocks of at least 8 tokens (one 8-row swizzle atom per box)");
+  static_assert(BYTES <= 227 * 1024, "shared memory per CTA");
+  static_assert((kKeys / BSUB) * NH <= 32, "the V producer issues one box per lane");
+};
+
+// barrier indices
+constexpr int B_KFULL = 0;    // [2]  two K producer warps arrive (+ TMA bytes)
+constexpr int B_VFULL = 2;    // [2]  the V producer warp arrives (+ TMA bytes)
+constexpr int B_KEMPTY = 4;   // [2]  tcgen05.commit after S_B(j)
+constexpr int B_VEMPTY = 6;   // [2]  tcgen05.commit after P.V_B(j)
+constexpr int B_SFULL = 8;    // [2]  per Q tile
+constexpr int B_PFULL = 10;   // [2]  four softmax warps
+constexpr int B_OFULL = 12;   // [2]  P.V_x(j) complete
+constexpr int B_QFULL = 14;
+constexpr int B_MMADONE = 15;
+
+template <int D, int BSUB, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                    const PrefillParams p) {
+  using L = TcSmem<D, BSUB>;
+  using Tile = typename L::Tile;
+  constexpr int NH = D / 64;
+  constexpr int KSTEPS = D / 16;      // S = Q K^T: K dimension = head_dim
+  constexpr int PSTEPS = kKeys / 16;  // O = P V:   K dimension = keys
+  constexpr int SUBS = kKeys / BSUB;  // boxes per half per tile
+  constexpr int SUBS_W = SUBS / 2;    // ... per K producer warp
+  constexpr uint32_t S_COL = 0;       // S_A, S_B: kKeys columns each; P_x in the first kKeys/2
+  constexpr uint32_t O_COL = 2 * kKeys;
+  constexpr uint32_t IDESC_S = idesc_f16<T>(kRows, kKeys, false);
+  constexpr uint32_t IDESC_O = idesc_f16<T>(kRows, D, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024_tc(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int row0 = blockIdx.x * 2 * kRows;
+  const int G = p.group;
+
+  // geometry (uniform across the CTA); only immutable inputs are read.
+  // Causal: request r = blockIdx.z, chunk at absolute position p0, row
+  // (query i, head g) sees keys 0 .. p0+i.  Shared prefix: one virtual request
+  // of total_q queries (the decode batch); keys [k0, kend) = split blockIdx.z
+  // of the prefix, visible to every row.
+  int r, qs, chunk, p0, k0, kend;
+  if (p.causal) {
+    r = blockIdx.z;
+    qs = __ldg(p.q_start + r);
+    const int qe = __ldg(p.q_start + r + 1);
+    chunk = qe - qs;
+    const int ctx = __ldg(p.lens + r);
+    p0 = ctx - chunk;
+    if (qs < 0 || qe < qs || qe > p.total_q || chunk > p.max_q_len || p0 < 0 || ctx > p.maxblk * p.block_size) {
+      griddep_wait();
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
+      return;
+    }
+    k0 = 0;
+    const int last_row = min(row0 + 2 * kRows, chunk * G) - 1;
+    kend = p0 + last_row / G + 1;
+  } else {
+    r = 0;
+    qs = 0;
+    chunk = p.total_q;
+    p0 = 0;
+    k0 = blockIdx.z * p.key_split;
+    kend = min(k0 + p.key_split, p.prefix_len);
+  }
+  const int rows = chunk * G;
+  if (row0 >= rows || k0 >= kend) {
+    griddep_wait();
+    return;
+  }
+  const int ntiles = (kend - k0 + kKeys - 1) / kKeys;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kKvStages; ++i) {
+      mbar_init(bar(B_KFULL + i), 2);
+      mbar_init(bar(B_VFULL + i), 1);
+      mbar_init(bar(B_KEMPTY + i), 1);
+      mbar_init(bar(B_VEMPTY + i), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(B_SFULL + x), 1);
+      mbar_init(bar(B_PFULL + x), 4);
+      mbar_init(bar(B_OFULL + x), 1);
+    }
+    mbar_init(bar(B_QFULL), 8);
+    mbar_init(bar(B_MMADONE), 1);
+    fence_mbar_init();
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmem);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
+
+  if (warp > kMmaWarp && warp <= kVWarp) {
+    // ---------------------------------------------------------------- producers
+    const int isv = warp == kVWarp;                 // 0: K, 1: V
+    const int sub_lo = isv ? 0 : (warp - 1) * SUBS_W;
+    const int nsubw = isv ? SUBS : SUBS_W;          // this warp's boxes: subs [sub_lo, sub_lo + nsubw), all halves
+    const int my_sub = sub_lo + lane / NH, hf = lane % NH;
+    const bool has_box = lane < nsubw * NH;
+    const int32_t* trow = p.tables + (size_t)r * p.maxblk;
+    const CUtensorMap* map = isv ? &vmap : &kmap;
+    const int full0 = isv ? B_VFULL : B_KFULL, empty0 = isv ? B_VEMPTY : B_KEMPTY;
+    const uint32_t base = smem_u32(smem + (isv ? L::V_OFF : L::K_OFF));
+    const uint64_t pol = policy_evict_last();  // K/V tiles are re-read by the other row tiles
+    int issued = 0;
+    bool failed = false;
+    griddep_wait();  // the cache (this step's reshape_and_cache) comes from the kernel before
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kKvStages;
+      if (j >= kKvStages && !mbar_wait(bar(empty0 + s), ((j / kKvStages) - 1) & 1)) {
+        failed = true;
+        break;
+      }
+      const int ts = k0 + j * kKeys;
+      const int nvalid = min(kKeys, kend - ts);
+      const int nsub = (nvalid + BSUB - 1) / BSUB;
+      const int mine = min(max(nsub - sub_lo, 0), nsubw);
+      if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), mine * NH * Tile::BOX_BYTES);
+      __syncwarp();
+      if (has_box && my_sub < nsub) {
+        const int tok = ts + my_sub * BSUB;
+        int b = __ldg(trow + tok / p.block_size);
+        if (b < 0 || b >= p.num_blocks) {
+          record_error(p.err, PA_DEVERR_BLOCK_ID);
+          b = p.num_blocks;  // rows past the tensor map: TMA zero-fills
+        }
+        tma_load_4d_hint(base + s * Tile::BYTES + Tile::box(hf, my_sub), map, bar(full0 + s), 0, hf, h,
+                         b * p.block_size + tok % p.block_size, pol);
+      }
+      issued = j + 1;
+    }
+    if (failed && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
+    for (int j = issued - kKvStages < 0 ? 0 : issued - kKvStages; j < issued; ++j)  // bounded drain
+      mbar_wait(bar(full0 + j % kKvStages), (j / kKvStages) & 1);
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(B_QFULL), 0);
+      const uint32_t kbase = smem_u32(smem + L::K_OFF), vbase = smem_u32(smem + L::V_OFF);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int s = j % kKvStages;
+        const uint32_t ph = (j / kKvStages) & 1;
+        if (!mbar_wait(bar(B_KFULL + s), ph)) { ok = false; break; }
+        const uint32_t kb = kbase + s * Tile::BYTES;
+        for (int x = 0; x < 2 && ok; ++x) {
+          // S_x(j) overwrites P_x(j-1): wait for P.V_x(j-1)
+          if (j > 0 && !mbar_wait(bar(B_OFULL + x), (j - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(smem + L::Q_OFF + x * L::QTILE);
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * L::QHALF + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
+            tc_mma_f16(tmem + S_COL + x * kKeys, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(B_SFULL + x));
+        }
+        if (!ok) break;
+        tc_commit(bar(B_KEMPTY + s));  // K_j read by both S MMAs
+        if (!mbar_wait(bar(B_VFULL + s), ph)) { ok = false; break; }
+        const uint32_t vb = vbase + s * Tile::BYTES;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (!mbar_wait(bar(B_PFULL + x), j & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < PSTEPS; ++kk) {
+            // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
+            const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
+            tc_mma_f16_ts(tmem + O_COL + x * D, tmem + S_COL + x * kKeys + kk * 8, bd, IDESC_O,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(B_OFULL + x));
+        }
+        if (!ok) break;
+        tc_commit(bar(B_VEMPTY + s));  // V_j read by both P.V MMAs
+      }
+      if (!ok) record_error(p.err, PA_DEVERR_TIMEOUT);
+      tc_commit(bar(B_MMADONE));
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int x = (warp - kSoftmaxWarp0) >> 2;  // Q tile: 0 = A (warps 4..7), 1 = B (warps 8..11)
+    const int quarter = warp & 3;                // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;         // row within the tile == TMEM lane
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int grow = row0 + x * kRows + row;
+    const bool valid = grow < rows;
+    const int qi = grow / G, g = grow % G;
+    const int lim = !valid ? -1 : (p.causal ? p0 + qi : kend - 1);  // last key this row may see
+    {
+      // Q row -> shared memory (K-major, 128-byte swizzle); padding rows are zero
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.q) +
+                                                        ((size_t)(qs + qi) * p.q_heads + h * G + g) * D);
+      uint8_t* qt = smem + L::Q_OFF + x * L::QTILE;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qt + (c >> 3) * L::QHALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QFULL));
+    }
+    griddep_wait();  // before writing outputs
+
+    float m = -INFINITY, l = 0.f;  // running (possibly stale) max in log2 units, row sum
+    const float sl2 = p.scale_log2;
+    constexpr float kRescale = 8.f;
+    const uint32_t scol = tmem + lane_addr + S_COL + x * kKeys;
+    const uint32_t ocol = tmem + lane_addr + O_COL + x * D;
+    bool ok = true;
+
+    for (int j = 0; j < ntiles; ++j) {
+      if (!mbar_wait(bar(B_SFULL + x), j & 1)) { ok = false; break; }
+      tc_fence_after();
+      const int ts = k0 + j * kKeys;
+      const int nvis = lim - ts + 1;  // keys of this tile the row may see (<= 0: none)
+      const bool all_full = __all_sync(0xffffffffu, nvis >= kKeys);
+
+      // the whole S row in registers: one TMEM round trip
+      float sv[kKeys];
+#pragma unroll
+      for (int c = 0; c < kKeys / 32; ++c) tmem_ld32(scol + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
+      tmem_wait_ld();
+      if (!all_full) {
+#pragma unroll
+        for (int e = 0; e < kKeys; ++e) sv[e] = e < nvis ? sv[e] : -INFINITY;
+      }
+      // row maximum: four independent chains of three-input max
+      float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < kKeys; e += 8) {
+        ma = fmax3(ma, sv[e], sv[e + 1]);
+        mb = fmax3(mb, sv[e + 2], sv[e + 3]);
+        mc = fmax3(mc, sv[e + 4], sv[e + 5]);
+        md = fmax3(md, sv[e + 6], sv[e + 7]);
+      }
+      const float mx = fmax3(ma, mb, fmaxf(mc, md)) * sl2;
+      const bool raise = mx > m + kRescale;  // also the first finite max (m = -inf)
+      // O and l are rescaled by 2^(m_old - m_new) when the maximum is raised
+      const float alpha = (raise && m != -INFINITY) ? ex2_approx(m - mx) : 1.f;
+      const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+      if (raise) {
+        l = (m == -INFINITY) ? 0.f : l * alpha;
+        m = mx;
+      }
+      const float neg_m = m == -INFINITY ? 0.f : -m;
+
+      // P = 2^(s*sl2 - m) (masked keys hold -inf: p = 0), written over the
+      // first kKeys/2 S columns; the sum in four packed-pair chains
+      float sx[4] = {0.f, 0.f, 0.f, 0.f}, sy[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kKeys / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float a0, a1;
+          ffma2(a0, a1, sv[32 * c + e], sv[32 * c + e + 1], sl2, sl2, neg_m, neg_m);
+          const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
+          const int k = (e >> 1) & 3;
+          fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
+          pk[e >> 1] = Elem<T>::pack(p0v, p1v);
+        }
+        tmem_st16u(scol + 16 * c, pk);  // keys 32c..32c+31 -> columns 16c..16c+15
+      }
+      const float sum = ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
+      if (rescale) {
+        // rescale O_x in TMEM (warp-collective; after P so that the S row is
+        // no longer live).  P.V_x(j-1) has completed: S_x(j) was issued after it.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(ocol + 32 * c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+          tmem_st32(ocol + 32 * c, ov);
+        }
+      }
+      l += sum;
+      tmem_wait_st();
+      const int nvalid = min(kKeys, kend - ts);
+      if (x == 0 && nvalid < kKeys) {
+        // last key tile: keys past kend came from stale slots (or were not
+        // loaded); zero their V rows so that p = 0 never meets NaN/Inf.  Tile
+        // A's P.V is issued before tile B's, so both see the zeroed rows.
+        const int s = j % kKvStages;
+        if (!mbar_wait(bar(B_VFULL + s), (j / kKvStages) & 1)) { ok = false; break; }
+        if (row >= nvalid) {
+          uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
+#pragma unroll
+          for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(vrow + hf * Tile::HALF + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + x));
+    }
+    if (ok && ntiles > 0) ok = mbar_wait(bar(B_OFULL + x), (ntiles - 1) & 1);
+    if (!ok) {
+      if (lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
+    } else if (p.causal) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
+                                            ((size_t)(qs + qi) * p.q_heads + h * G + g) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tmem_ld32(ocol + 32 * c, ov);  // warp-collective: every lane loads, valid rows store
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[4 * c + q] = make_uint4(Elem<T>::pack(ov[8 * q] * inv, ov[8 * q + 1] * inv),
+                                        Elem<T>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
+                                        Elem<T>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
+                                        Elem<T>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+        }
+      }
+      tc_fence_before();
+    } else {
+      // shared-prefix partial of this key range: unnormalised o, m, l
+      tc_fence_after();
+      const size_t pr = ((size_t)qi * p.q_heads + h * G + g) * p.max_splits + blockIdx.z;
+      float4* po = reinterpret_cast<float4*>(p.part_o + pr * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tmem_ld32(ocol + 32 * c, ov);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            po[8 * c + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+        }
+      }
+      if (valid) {
+        p.part_m[pr] = m;
+        p.part_l[pr] = l;
+      }
+      tc_fence_before();
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  if (warp == kMmaWarp && lane == 0) mbar_wait(bar(B_MMADONE), 0);  // no tcgen05 op still running (bounded)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmem);
+  }
+}
+
+template <int D, int BSUB, typename T>
+cudaError_t launch_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
+                         cudaStream_t stream) {
+  using L = TcSmem<D, BSUB>;
+  auto kern = attn_tc_kernel<D, BSUB, T>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int row_tiles = (p.max_q_len * p.group + 2 * kRows - 1) / (2 * kRows);
+  const int zdim = p.causal ? p.num_reqs : (p.prefix_len + p.key_split - 1) / p.key_split;
+  dim3 grid(row_tiles, p.kv_heads, zdim);
+  return launch_pdl(kern, grid, dim3(kThreads), L::BYTES, stream, kmap, vmap, p);
+}
+
+template <int D, typename T>
+cudaError_t launch_tc_bs(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int bsub,
+                          cudaStream_t stream) {
+  switch (bsub) {
+    case 8: return launch_tc_t<D, 8, T>(kmap, vmap, p, stream);
+    case 16: return launch_tc_t<D, 16, T>(kmap, vmap, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int head_dim,
+                            int bsub, pa_dtype dt, cudaStream_t stream) {
+  if (head_dim == 128) {
+    return dt == PA_BF16 ? launch_tc_bs<128, __nv_bfloat16>(kmap, vmap, p, bsub, stream)
+                         : launch_tc_bs<128, __half>(kmap, vmap, p, bsub, stream);
+  }
+  if (head_dim == 64) {
+    return dt == PA_BF16 ? launch_tc_bs<64, __nv_bfloat16>(kmap, vmap, p, bsub, stream)
+                         : launch_tc_bs<64, __half>(kmap, vmap, p, bsub, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -395,7 +395,7 @@ int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* con
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   // blocks of >= 8 tokens: 5th-generation tensor cores (tcgen05 + TMEM);
   // 4-token blocks: warp-level MMA kernel
-  if (bsub >= 8) return cuda_status(launch_chunked_prefill_tc(km, vm, p, head_dim, bsub, dtype, st_));
+  if (bsub >= 8) return cuda_status(launch_attn_tc(km, vm, p, head_dim, bsub, dtype, st_));
   return cuda_status(launch_chunked_prefill(km, vm, p, head_dim, bsub, dtype, st_));
 }
 
@@ -470,7 +470,7 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   pp.part_o = po;
   pp.part_m = pm;
   pp.part_l = pl;
-  st = cuda_status(launch_chunked_prefill_tc(km, vm, pp, head_dim, bsub, dtype, cs));
+  st = cuda_status(launch_attn_tc(km, vm, pp, head_dim, bsub, dtype, cs));
   if (st != PA_OK) return st;
 
   // 2. each request's own suffix (paged decode, partials after the prefix's)

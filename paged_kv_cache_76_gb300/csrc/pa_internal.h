@@ -106,9 +106,11 @@ cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vm
 cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_chunked_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
                                    int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
-// tcgen05/TMEM variant; needs bsub >= 8 (one 8-row swizzle atom per box)
-cudaError_t launch_chunked_prefill_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
-                                      int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
+// tcgen05/TMEM kernel for blocks of >= 8 tokens (bsub >= 8): chunked prefill
+// (p.causal = 1) and the shared-prefix pass of a decode batch (p.causal = 0,
+// partials).  Two 128-row Q tiles per CTA, 128-key K/V tiles, P kept in TMEM.
+cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int head_dim,
+                           int bsub, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
                                      void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,
                                      cudaStream_t stream);
