@@ -16,17 +16,18 @@
 //  * Three producer warps issue the TMA gather: one warp issuing 16-row
 //    boxes moves about 27 B/clk per SM, several warps together more.
 //  * The softmax holds its whole S row in registers (one TMEM round trip per
-//    tile) and uses packed f32x2 arithmetic.
+//    tile).
 //
 // Warp roles (384 threads = 12 warps, so that each thread may hold 168
 // registers; one CTA per SM):
-//   warp 0      MMA issuer (one thread), per key tile j:
-//                 S_A(j), S_B(j), P.V_A(j), P.V_B(j)
+//   warps 0,1   MMA issuers, one thread per Q tile x: per key tile j,
+//                 S_x(j) = Q_x K_j^T, then O_x += P_x(j) V_j
 //               S_x(j) overwrites P_x(j-1), so it is issued once P.V_x(j-1)
-//               has completed (which overlaps the other tile's MMAs).
-//   warps 1,2   TMA producers of K (half of the tile's blocks each), warp 3
-//               of V; separate 2-stage K and V rings, so a K slot frees as
-//               soon as both S MMAs have read it.
+//               has completed.  The two issuers wait only on their own tile;
+//               the tensor pipe interleaves their MMAs.
+//   warp 2      TMA producer of K, warp 3 of V; separate K (3-stage) and V
+//               (2-stage) rings, so a K slot frees as soon as both S MMAs have
+//               read it.
 //   warps 4..7  softmax of tile A, warps 8..11 of tile B: thread = TMEM lane
 //               = row.  It loads its S row, takes the row maximum, writes
 //               P = 2^(s*scale*log2e - m) into TMEM and sums it.  The running
@@ -46,9 +47,14 @@ namespace {
 
 constexpr int kRows = 128;  // rows per Q tile (M of every MMA)
 constexpr int kKeys = 128;  // keys per K/V tile (N of S, K of P.V)
-constexpr int kKvStages = 2;
-constexpr int kMmaWarp = 0;
-constexpr int kVWarp = 3;  // warps 1, 2: K
+// K ring 3 deep: K(j) is on the critical path (S_A(j) waits for it) and a
+// gathered tile lands a few microseconds after its slot frees; V is needed
+// later (P.V) and gets 2 stages.  Head_dim 128: 64 + 96 + 64 KB of smem.
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kMmaWarp = 0;  // warps 0, 1: MMA issuers of Q tiles A, B (warp 0 owns TMEM)
+constexpr int kKWarp = 2;
+constexpr int kVWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kThreads = 32 * 12;
 constexpr uint32_t kTmem = 512;
@@ -65,9 +71,9 @@ struct TcSmem {
   static constexpr int QTILE = NH * QHALF;
   static constexpr int Q_OFF = 0;  // Q_A, Q_B
   static constexpr int K_OFF = Q_OFF + 2 * QTILE;
-  static constexpr int V_OFF = K_OFF + kKvStages * Tile::BYTES;
-  static constexpr int BAR_OFF = V_OFF + kKvStages * Tile::BYTES;
-  static constexpr int NBARS = 16;
+  static constexpr int V_OFF = K_OFF + kKStages * Tile::BYTES;
+  static constexpr int BAR_OFF = V_OFF + kVStages * Tile::BYTES;
+  static constexpr int NBARS = 2 * kKStages + 2 * kVStages + 10;
   static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = SLOT_OFF + 16 + 1024;
   static_assert(BSUB * 128 >= 1024, "needs blocks of at least 8 tokens (one 8-row swizzle atom per box)");
@@ -76,15 +82,17 @@ struct TcSmem {
 };
 
 // barrier indices
-constexpr int B_KFULL = 0;    // [2]  two K producer warps arrive (+ TMA bytes)
-constexpr int B_VFULL = 2;    // [2]  the V producer warp arrives (+ TMA bytes)
-constexpr int B_KEMPTY = 4;   // [2]  tcgen05.commit after S_B(j)
-constexpr int B_VEMPTY = 6;   // [2]  tcgen05.commit after P.V_B(j)
-constexpr int B_SFULL = 8;    // [2]  per Q tile
-constexpr int B_PFULL = 10;   // [2]  four softmax warps
-constexpr int B_OFULL = 12;   // [2]  P.V_x(j) complete
-constexpr int B_QFULL = 14;
-constexpr int B_MMADONE = 15;
+constexpr int B_KFULL = 0;                     // [kKStages] the K producer warp arrives (+ TMA bytes)
+constexpr int B_KEMPTY = B_KFULL + kKStages;   // [kKStages] one tcgen05.commit per issuer after S_x(j)
+constexpr int B_VFULL = B_KEMPTY + kKStages;   // [kVStages] the V producer warp arrives (+ TMA bytes)
+constexpr int B_VEMPTY = B_VFULL + kVStages;   // [kVStages] one tcgen05.commit per issuer after P.V_x(j)
+constexpr int B_SFULL = B_VEMPTY + kVStages;   // [2] per Q tile
+constexpr int B_PLO = B_SFULL + 2;             // [2] P_x keys 0..63 in TMEM (four softmax warps)
+constexpr int B_PHI = B_PLO + 2;               // [2] P_x keys 64..127
+constexpr int B_OFULL = B_PHI + 2;             // [2] P.V_x(j) complete
+constexpr int B_QFULL = B_OFULL + 2;
+constexpr int B_MMADONE = B_QFULL + 1;
+static_assert(B_MMADONE + 1 == 2 * kKStages + 2 * kVStages + 10, "barrier count");
 
 template <int D, int BSUB, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,7 +104,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int KSTEPS = D / 16;      // S = Q K^T: K dimension = head_dim
   constexpr int PSTEPS = kKeys / 16;  // O = P V:   K dimension = keys
   constexpr int SUBS = kKeys / BSUB;  // boxes per half per tile
-  constexpr int SUBS_W = SUBS / 2;    // ... per K producer warp
   constexpr uint32_t S_COL = 0;       // S_A, S_B: kKeys columns each; P_x in the first kKeys/2
   constexpr uint32_t O_COL = 2 * kKeys;
   constexpr uint32_t IDESC_S = idesc_f16<T>(kRows, kKeys, false);
@@ -150,19 +157,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (kend - k0 + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kKvStages; ++i) {
-      mbar_init(bar(B_KFULL + i), 2);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(bar(B_KFULL + i), 1);
+      mbar_init(bar(B_KEMPTY + i), 2);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(bar(B_VFULL + i), 1);
-      mbar_init(bar(B_KEMPTY + i), 1);
-      mbar_init(bar(B_VEMPTY + i), 1);
+      mbar_init(bar(B_VEMPTY + i), 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(B_SFULL + x), 1);
-      mbar_init(bar(B_PFULL + x), 4);
+      mbar_init(bar(B_PLO + x), 4);
+      mbar_init(bar(B_PHI + x), 4);
       mbar_init(bar(B_OFULL + x), 1);
     }
     mbar_init(bar(B_QFULL), 8);
-    mbar_init(bar(B_MMADONE), 1);
+    mbar_init(bar(B_MMADONE), 2);
     fence_mbar_init();
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
@@ -177,11 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   griddep_launch_dependents();
 
-  if (warp > kMmaWarp && warp <= kVWarp) {
+  if (warp == kKWarp || warp == kVWarp) {
     // ---------------------------------------------------------------- producers
-    const int isv = warp == kVWarp;                 // 0: K, 1: V
-    const int sub_lo = isv ? 0 : (warp - 1) * SUBS_W;
-    const int nsubw = isv ? SUBS : SUBS_W;          // this warp's boxes: subs [sub_lo, sub_lo + nsubw), all halves
+    const int isv = warp == kVWarp;  // 0: K, 1: V
+    const int sub_lo = 0;
+    const int nsubw = SUBS;          // one box per lane: subs [0, SUBS) x halves
     const int my_sub = sub_lo + lane / NH, hf = lane % NH;
     const bool has_box = lane < nsubw * NH;
     const int32_t* trow = p.tables + (size_t)r * p.maxblk;
@@ -189,12 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int full0 = isv ? B_VFULL : B_KFULL, empty0 = isv ? B_VEMPTY : B_KEMPTY;
     const uint32_t base = smem_u32(smem + (isv ? L::V_OFF : L::K_OFF));
     const uint64_t pol = policy_evict_last();  // K/V tiles are re-read by the other row tiles
+    const int nst = isv ? kVStages : kKStages;
     int issued = 0;
     bool failed = false;
     griddep_wait();  // the cache (this step's reshape_and_cache) comes from the kernel before
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j % kKvStages;
-      if (j >= kKvStages && !mbar_wait(bar(empty0 + s), ((j / kKvStages) - 1) & 1)) {
+      const int s = j % nst;
+      if (j >= nst && !mbar_wait(bar(empty0 + s), ((j / nst) - 1) & 1)) {
         failed = true;
         break;
       }
@@ -217,49 +228,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       issued = j + 1;
     }
     if (failed && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
-    for (int j = issued - kKvStages < 0 ? 0 : issued - kKvStages; j < issued; ++j)  // bounded drain
-      mbar_wait(bar(full0 + j % kKvStages), (j / kKvStages) & 1);
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
+    for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)  // bounded drain
+      mbar_wait(bar(full0 + j % nst), (j / nst) & 1);
+  } else if (warp < kKWarp) {
+    // ---------------------------------------------------------------- MMA issuers
+    // One thread per Q tile: warp 0 issues tile A's MMAs, warp 1 tile B's.
+    // tcgen05.mma issue blocks while the tensor pipe is busy, so a single
+    // issuer serialises its waits behind the other tile's MMAs; two issuers
+    // wait only on their own tile, and the pipe interleaves their work.
     if (lane == 0) {
+      const int x = warp;
       bool ok = mbar_wait(bar(B_QFULL), 0);
       const uint32_t kbase = smem_u32(smem + L::K_OFF), vbase = smem_u32(smem + L::V_OFF);
+      const uint32_t qa = smem_u32(smem + L::Q_OFF + x * L::QTILE);
+      const uint32_t sd = tmem + S_COL + x * kKeys, od = tmem + O_COL + x * D;
+      // Tile B starts half a key tile behind tile A (once P_A(0) is being
+      // written), so that the two softmaxes alternate instead of overlapping.
+      if (x == 1 && ntiles > 0) ok = ok && mbar_wait(bar(B_PLO), 0);
       for (int j = 0; ok && j < ntiles; ++j) {
-        const int s = j % kKvStages;
-        const uint32_t ph = (j / kKvStages) & 1;
-        if (!mbar_wait(bar(B_KFULL + s), ph)) { ok = false; break; }
-        const uint32_t kb = kbase + s * Tile::BYTES;
-        for (int x = 0; x < 2 && ok; ++x) {
-          // S_x(j) overwrites P_x(j-1): wait for P.V_x(j-1)
-          if (j > 0 && !mbar_wait(bar(B_OFULL + x), (j - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qa = smem_u32(smem + L::Q_OFF + x * L::QTILE);
+        const int sk = j % kKStages, sv = j % kVStages;
+        // S_x(j) = Q_x K_j^T.  It overwrites P_x(j-1): wait for P.V_x(j-1).
+        if (!mbar_wait(bar(B_KFULL + sk), (j / kKStages) & 1)) { ok = false; break; }
+        if (j > 0 && !mbar_wait(bar(B_OFULL + x), (j - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = kbase + sk * Tile::BYTES;
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * L::QHALF + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
-            tc_mma_f16(tmem + S_COL + x * kKeys, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(B_SFULL + x));
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * L::QHALF + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
+          tc_mma_f16(sd, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        tc_commit(bar(B_KEMPTY + s));  // K_j read by both S MMAs
-        if (!mbar_wait(bar(B_VFULL + s), ph)) { ok = false; break; }
-        const uint32_t vb = vbase + s * Tile::BYTES;
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (!mbar_wait(bar(B_PFULL + x), j & 1)) { ok = false; break; }
+        tc_commit(bar(B_SFULL + x));
+        tc_commit(bar(B_KEMPTY + sk));  // this issuer is done with K_j
+        // O_x += P_x(j) V_j in two halves of 64 keys, each as soon as its P
+        // half is in TMEM
+        if (!mbar_wait(bar(B_VFULL + sv), (j / kVStages) & 1)) { ok = false; break; }
+        const uint32_t vb = vbase + sv * Tile::BYTES;
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          if (!mbar_wait(bar((hh ? B_PHI : B_PLO) + x), j & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < PSTEPS; ++kk) {
+          for (int k4 = 0; k4 < PSTEPS / 2; ++k4) {
             // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
+            const int kk = hh * (PSTEPS / 2) + k4;
             const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
-            tc_mma_f16_ts(tmem + O_COL + x * D, tmem + S_COL + x * kKeys + kk * 8, bd, IDESC_O,
-                          (j > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_f16_ts(od, sd + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar(B_OFULL + x));
         }
         if (!ok) break;
-        tc_commit(bar(B_VEMPTY + s));  // V_j read by both P.V MMAs
+        tc_commit(bar(B_OFULL + x));
+        tc_commit(bar(B_VEMPTY + sv));  // this issuer is done with V_j
       }
       if (!ok) record_error(p.err, PA_DEVERR_TIMEOUT);
       tc_commit(bar(B_MMADONE));
@@ -334,58 +352,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float neg_m = m == -INFINITY ? 0.f : -m;
 
       // P = 2^(s*sl2 - m) (masked keys hold -inf: p = 0), written over the
-      // first kKeys/2 S columns; the sum in four packed-pair chains
+      // first kKeys/2 S columns in two halves of 64 keys; each half is
+      // signalled on its own so that P.V can start on the first.  The sum runs
+      // in four packed-pair chains.
       float sx[4] = {0.f, 0.f, 0.f, 0.f}, sy[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float a0, a1;
-          ffma2(a0, a1, sv[32 * c + e], sv[32 * c + e + 1], sl2, sl2, neg_m, neg_m);
-          const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
-          const int k = (e >> 1) & 3;
-          fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
-          pk[e >> 1] = Elem<T>::pack(p0v, p1v);
-        }
-        tmem_st16u(scol + 16 * c, pk);  // keys 32c..32c+31 -> columns 16c..16c+15
-      }
-      const float sum = ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
-      if (rescale) {
-        // rescale O_x in TMEM (warp-collective; after P so that the S row is
-        // no longer live).  P.V_x(j-1) has completed: S_x(j) was issued after it.
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld32(ocol + 32 * c, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-          tmem_st32(ocol + 32 * c, ov);
-        }
-      }
-      l += sum;
-      tmem_wait_st();
       const int nvalid = min(kKeys, kend - ts);
-      if (x == 0 && nvalid < kKeys) {
-        // last key tile: keys past kend came from stale slots (or were not
-        // loaded); zero their V rows so that p = 0 never meets NaN/Inf.  Tile
-        // A's P.V is issued before tile B's, so both see the zeroed rows.
-        const int s = j % kKvStages;
-        if (!mbar_wait(bar(B_VFULL + s), (j / kKvStages) & 1)) { ok = false; break; }
-        if (row >= nvalid) {
-          uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
 #pragma unroll
-          for (int hf = 0; hf < NH; ++hf)
+      for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(vrow + hf * Tile::HALF + c * 16) = make_uint4(0, 0, 0, 0);
+        for (int cc = 0; cc < kKeys / 64; ++cc) {
+          const int c = hh * (kKeys / 64) + cc;
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float a0, a1;
+            ffma2(a0, a1, sv[32 * c + e], sv[32 * c + e + 1], sl2, sl2, neg_m, neg_m);
+            const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
+            const int k = (e >> 1) & 3;
+            fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
+            pk[e >> 1] = Elem<T>::pack(p0v, p1v);
+          }
+          tmem_st16u(scol + 16 * c, pk);  // keys 32c..32c+31 -> columns 16c..16c+15
         }
-        fence_proxy_async_smem();
+        if (hh == 0) {
+          if (rescale) {
+            // rescale O_x in TMEM before P.V_x(j) starts (warp-collective).
+            // P.V_x(j-1) has completed: S_x(j) was issued after it.
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+              float ov[16];
+              tmem_ld16(ocol + 16 * c, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+              tmem_st16u(ocol + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(ov));
+            }
+          }
+          if (nvalid < kKeys) {
+            // last key tile: keys past kend came from stale slots (or were not
+            // loaded); zero their V rows so that p = 0 never meets NaN/Inf.
+            // Both Q tiles' softmax warps write the same zeros (either P.V
+            // may run first); each P.V starts only after its own group's.
+            const int s = j % kVStages;
+            if (!mbar_wait(bar(B_VFULL + s), (j / kVStages) & 1)) {
+              ok = false;
+            } else if (row >= nvalid) {
+              uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
+#pragma unroll
+              for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  *reinterpret_cast<uint4*>(vrow + hf * Tile::HALF + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar((hh ? B_PHI : B_PLO) + x));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + x));
+      l += ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
+      if (!ok) break;
     }
     if (ok && ntiles > 0) ok = mbar_wait(bar(B_OFULL + x), (ntiles - 1) & 1);
     if (!ok) {
@@ -435,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------------ teardown
-  if (warp == kMmaWarp && lane == 0) mbar_wait(bar(B_MMADONE), 0);  // no tcgen05 op still running (bounded)
+  if (warp == kMmaWarp && lane == 0) mbar_wait(bar(B_MMADONE), 0);  // both issuers' tcgen05 ops done (bounded)
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
