@@ -234,8 +234,11 @@ class Step:
         dv = views(self.d_out, ooffs, outs)
         hv = views(self.h_outbuf, ooffs, outs)
         self.side = None
+        self.prefill_ctas = 0
         if self.pre and self.dec and overlap_streams:
-            self.side = torch.cuda.Stream(device)
+            # prefill (tensor-bound) on a second stream at the highest priority,
+            # so that its CTAs take their SMs first; decode (HBM-bound) fills the rest
+            self.side = torch.cuda.Stream(device, priority=torch.cuda.Stream.priority_range()[1])
             self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
         self.out_dec = dv.get("dec")
         self.out_pre = dv.get("pre")
@@ -255,7 +258,8 @@ class Step:
             self.ev_fork.record(stream)
             self.side.wait_event(self.ev_fork)
             o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
-                              d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=self.side)
+                              d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=self.side,
+                              max_ctas=self.prefill_ctas)
             self.ev_join.record(self.side)
         elif self.pre:
             o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
@@ -279,6 +283,38 @@ class Step:
                         split_tokens=self.split, stream=stream)
         if overlap:
             stream.wait_event(self.ev_join)
+
+    def calibrate_prefill_ctas(self, stream, sms: int, reps: int = 3) -> int:
+        """SMs to leave to the prefill when it runs beside decode.
+
+        Decode is bound by HBM and keeps its speed on fewer SMs, so the prefill
+        gets about as many SMs as it needs to finish with the decode: time each
+        part alone (uncapped, `reps` runs, after one untimed run) and give the
+        prefill 1.25 x SMs x t_prefill / t_decode CTAs, within [SMs/8, SMs/2].
+        """
+        o, d, wl = self.ops, self.d, self.wl
+        def timed(fn):
+            fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+        def pre():
+            o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
+                              d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=stream)
+        def dec():
+            saved, self.pre = self.pre, False
+            try:
+                self.run(stream)
+            finally:
+                self.pre = saved
+        t_pre, t_dec = timed(pre), timed(dec)
+        cap = int(round(1.25 * sms * t_pre / max(t_dec, 1e-6)))
+        self.prefill_ctas = max(max(1, sms // 8), min(sms // 2, cap))
+        return self.prefill_ctas
 
     def run_e2e(self, stream):
         """Host buffers in, host buffers out: one copy each way inside the step."""
@@ -412,6 +448,8 @@ def main():
     ap.add_argument("--serial", action="store_true", help="run prefill and decode on one stream, one after the other")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="decode a shared prefix per request instead of once for the batch")
+    ap.add_argument("--prefill-ctas", type=int, default=None,
+                    help="CTAs for a prefill running beside decode (0: one per work unit; default: calibrated)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -441,6 +479,12 @@ def main():
         return reference_arm(args, step, ws, rank, peak)
 
     stream = torch.cuda.Stream(device)
+    if step.side is not None:
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        if args.prefill_ctas is not None:
+            step.prefill_ctas = args.prefill_ctas
+        else:
+            step.calibrate_prefill_ctas(stream, sms)
     nb = step.bytes_breakdown()
     total_bytes = sum(v for k, v in nb.items() if k not in ("decode_unique", "prefill_flops"))
     with torch.cuda.stream(stream):
@@ -564,7 +608,8 @@ def main():
             "bytes_per_step": nb,
             "l2": f"inputs larger than L2: {total_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2",
             "parallelism": f"replicas x{ws}",
-            "streams": "prefill on a second stream concurrent with decode" if step.side is not None else "one",
+            "streams": (f"prefill on a second, highest-priority stream over {step.prefill_ctas or 'all'} CTAs, "
+                        f"concurrent with decode" if step.side is not None else "one"),
         },
         "gpu_launches": int(launches),
         "clocks": clk,

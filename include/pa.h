@@ -225,12 +225,19 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
  *   q, out        [total_q][q_heads][head_dim]
  *   q_start       int32 [num_reqs + 1], non-decreasing, q_start[num_reqs] <= total_q
  *   max_q_len     host-side upper bound of any chunk length (sizes the grid)
+ *   max_ctas      with blocks of >= 8 tokens the work is cut into units of
+ *                 256 (query, group head) rows of one (request, KV head);
+ *                 at most max_ctas CTAs (one per SM) loop over them.  <= 0:
+ *                 one CTA per unit.  A caller that runs decode concurrently
+ *                 on another stream can leave the remaining SMs to it (decode
+ *                 is bound by HBM, not by SM count).  Ignored for 4-token
+ *                 blocks.
  * A chunk longer than max_q_len or a context shorter than its chunk records
  * PA_DEVERR_QUERY_RANGE and that request is skipped.
  * ------------------------------------------------------------------------- */
 int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* context_lens,
                        const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                       int max_blocks_per_seq, int num_reqs, int total_q, int max_q_len,
+                       int max_blocks_per_seq, int num_reqs, int total_q, int max_q_len, int max_ctas,
                        int q_heads, int kv_heads, int head_dim, int block_size, int num_blocks,
                        float scale, void* out, pa_dtype dtype, pa_stream stream);
 

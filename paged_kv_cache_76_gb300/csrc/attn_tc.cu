@@ -73,7 +73,7 @@ struct TcSmem {
   static constexpr int K_OFF = Q_OFF + 2 * QTILE;
   static constexpr int V_OFF = K_OFF + kKStages * Tile::BYTES;
   static constexpr int BAR_OFF = V_OFF + kVStages * Tile::BYTES;
-  static constexpr int NBARS = 2 * kKStages + 2 * kVStages + 10;
+  static constexpr int NBARS = 2 * kKStages + 2 * kVStages + 11;
   static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = SLOT_OFF + 16 + 1024;
   static_assert(BSUB * 128 >= 1024, "needs blocks of at least 8 tokens (one 8-row swizzle atom per box)");
@@ -90,9 +90,60 @@ constexpr int B_SFULL = B_VEMPTY + kVStages;   // [2] per Q tile
 constexpr int B_PLO = B_SFULL + 2;             // [2] P_x keys 0..63 in TMEM (four softmax warps)
 constexpr int B_PHI = B_PLO + 2;               // [2] P_x keys 64..127
 constexpr int B_OFULL = B_PHI + 2;             // [2] P.V_x(j) complete
-constexpr int B_QFULL = B_OFULL + 2;
-constexpr int B_MMADONE = B_QFULL + 1;
-static_assert(B_MMADONE + 1 == 2 * kKStages + 2 * kVStages + 10, "barrier count");
+constexpr int B_QFULL = B_OFULL + 2;            // [2] Q_x of the next work unit in smem (four softmax warps)
+constexpr int B_MMADONE = B_QFULL + 2;
+static_assert(B_MMADONE + 1 == 2 * kKStages + 2 * kVStages + 11, "barrier count");
+
+// One work unit: a tile of 2 x 128 rows of one (request, KV head) for the
+// causal prefill, or of one (prefix key range, KV head) for the shared-prefix
+// pass.  Units are numbered z-major, then head, then row tile in reverse (the
+// last row tiles of a causal chunk see the most keys, so they come first).
+struct TcUnit {
+  int z, h, row0, r, qs, chunk, p0, k0, kend, rows, ntiles;
+};
+
+// Geometry of unit u from immutable inputs only.  false: the request's
+// q_start/context_lens are inconsistent (the unit is skipped).
+__device__ __forceinline__ bool tc_unit(const PrefillParams& p, int u, int row_tiles, TcUnit& w) {
+  const int per_z = row_tiles * p.kv_heads;
+  w.z = u / per_z;
+  const int rem = u - w.z * per_z;
+  w.h = rem / row_tiles;
+  w.row0 = (row_tiles - 1 - (rem - w.h * row_tiles)) * 2 * kRows;
+  w.ntiles = 0;
+  const int G = p.group;
+  if (p.causal) {
+    // request r = z, chunk at absolute position p0, row (query i, head g)
+    // sees keys 0 .. p0+i
+    w.r = w.z;
+    w.qs = __ldg(p.q_start + w.r);
+    const int qe = __ldg(p.q_start + w.r + 1);
+    w.chunk = qe - w.qs;
+    const int ctx = __ldg(p.lens + w.r);
+    w.p0 = ctx - w.chunk;
+    if (w.qs < 0 || qe < w.qs || qe > p.total_q || w.chunk > p.max_q_len || w.p0 < 0 ||
+        ctx > p.maxblk * p.block_size)
+      return false;
+    w.k0 = 0;
+    w.rows = w.chunk * G;
+    if (w.row0 >= w.rows) return true;
+    const int last_row = min(w.row0 + 2 * kRows, w.rows) - 1;
+    w.kend = w.p0 + last_row / G + 1;
+  } else {
+    // one virtual request of total_q queries (the decode batch); keys
+    // [k0, kend) = split z of the prefix, visible to every row
+    w.r = 0;
+    w.qs = 0;
+    w.chunk = p.total_q;
+    w.p0 = 0;
+    w.k0 = w.z * p.key_split;
+    w.kend = min(w.k0 + p.key_split, p.prefix_len);
+    w.rows = w.chunk * G;
+    if (w.row0 >= w.rows || w.k0 >= w.kend) return true;
+  }
+  w.ntiles = (w.kend - w.k0 + kKeys - 1) / kKeys;
+  return true;
+}
 
 template <int D, int BSUB, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -116,45 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int row0 = blockIdx.x * 2 * kRows;
   const int G = p.group;
-
-  // geometry (uniform across the CTA); only immutable inputs are read.
-  // Causal: request r = blockIdx.z, chunk at absolute position p0, row
-  // (query i, head g) sees keys 0 .. p0+i.  Shared prefix: one virtual request
-  // of total_q queries (the decode batch); keys [k0, kend) = split blockIdx.z
-  // of the prefix, visible to every row.
-  int r, qs, chunk, p0, k0, kend;
-  if (p.causal) {
-    r = blockIdx.z;
-    qs = __ldg(p.q_start + r);
-    const int qe = __ldg(p.q_start + r + 1);
-    chunk = qe - qs;
-    const int ctx = __ldg(p.lens + r);
-    p0 = ctx - chunk;
-    if (qs < 0 || qe < qs || qe > p.total_q || chunk > p.max_q_len || p0 < 0 || ctx > p.maxblk * p.block_size) {
-      griddep_wait();
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
-      return;
-    }
-    k0 = 0;
-    const int last_row = min(row0 + 2 * kRows, chunk * G) - 1;
-    kend = p0 + last_row / G + 1;
-  } else {
-    r = 0;
-    qs = 0;
-    chunk = p.total_q;
-    p0 = 0;
-    k0 = blockIdx.z * p.key_split;
-    kend = min(k0 + p.key_split, p.prefix_len);
-  }
-  const int rows = chunk * G;
-  if (row0 >= rows || k0 >= kend) {
-    griddep_wait();
-    return;
-  }
-  const int ntiles = (kend - k0 + kKeys - 1) / kKeys;
+  // CTA b (linear block index) takes units b, b + nctas, ...
+  const int row_tiles = (p.max_q_len * G + 2 * kRows - 1) / (2 * kRows);
+  const int nunits = row_tiles * p.kv_heads * (p.causal ? p.num_reqs : (p.prefix_len + p.key_split - 1) / p.key_split);
+  const int cta0 = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int nctas = gridDim.x * gridDim.y * gridDim.z;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -171,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_PHI + x), 4);
       mbar_init(bar(B_OFULL + x), 1);
     }
-    mbar_init(bar(B_QFULL), 8);
+    mbar_init(bar(B_QFULL), 4);
+    mbar_init(bar(B_QFULL + 1), 4);
     mbar_init(bar(B_MMADONE), 2);
     fence_mbar_init();
     prefetch_tensormap(&kmap);
@@ -190,46 +209,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kKWarp || warp == kVWarp) {
     // ---------------------------------------------------------------- producers
     const int isv = warp == kVWarp;  // 0: K, 1: V
-    const int sub_lo = 0;
-    const int nsubw = SUBS;          // one box per lane: subs [0, SUBS) x halves
-    const int my_sub = sub_lo + lane / NH, hf = lane % NH;
-    const bool has_box = lane < nsubw * NH;
-    const int32_t* trow = p.tables + (size_t)r * p.maxblk;
+    const int my_sub = lane / NH, hf = lane % NH;  // one box per lane: subs [0, SUBS) x halves
+    const bool has_box = lane < SUBS * NH;
     const CUtensorMap* map = isv ? &vmap : &kmap;
     const int full0 = isv ? B_VFULL : B_KFULL, empty0 = isv ? B_VEMPTY : B_KEMPTY;
     const uint32_t base = smem_u32(smem + (isv ? L::V_OFF : L::K_OFF));
     const uint64_t pol = policy_evict_last();  // K/V tiles are re-read by the other row tiles
     const int nst = isv ? kVStages : kKStages;
-    int issued = 0;
+    int gt = 0;  // K/V tiles issued by this CTA (ring position and phase)
     bool failed = false;
     griddep_wait();  // the cache (this step's reshape_and_cache) comes from the kernel before
-    for (int j = 0; j < ntiles; ++j) {
-      const int s = j % nst;
-      if (j >= nst && !mbar_wait(bar(empty0 + s), ((j / nst) - 1) & 1)) {
-        failed = true;
-        break;
-      }
-      const int ts = k0 + j * kKeys;
-      const int nvalid = min(kKeys, kend - ts);
-      const int nsub = (nvalid + BSUB - 1) / BSUB;
-      const int mine = min(max(nsub - sub_lo, 0), nsubw);
-      if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), mine * NH * Tile::BOX_BYTES);
-      __syncwarp();
-      if (has_box && my_sub < nsub) {
-        const int tok = ts + my_sub * BSUB;
-        int b = __ldg(trow + tok / p.block_size);
-        if (b < 0 || b >= p.num_blocks) {
-          record_error(p.err, PA_DEVERR_BLOCK_ID);
-          b = p.num_blocks;  // rows past the tensor map: TMA zero-fills
+    for (int u = cta0; u < nunits && !failed; u += nctas) {
+      TcUnit w;
+      if (!tc_unit(p, u, row_tiles, w) || w.ntiles <= 0) continue;
+      const int32_t* trow = p.tables + (size_t)w.r * p.maxblk;
+      for (int j = 0; j < w.ntiles; ++j, ++gt) {
+        const int s = gt % nst;
+        if (gt >= nst && !mbar_wait(bar(empty0 + s), ((gt / nst) - 1) & 1)) {
+          failed = true;
+          break;
         }
-        tma_load_4d_hint(base + s * Tile::BYTES + Tile::box(hf, my_sub), map, bar(full0 + s), 0, hf, h,
-                         b * p.block_size + tok % p.block_size, pol);
+        const int ts = w.k0 + j * kKeys;
+        const int nvalid = min(kKeys, w.kend - ts);
+        const int nsub = (nvalid + BSUB - 1) / BSUB;
+        if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), nsub * NH * Tile::BOX_BYTES);
+        __syncwarp();
+        if (has_box && my_sub < nsub) {
+          const int tok = ts + my_sub * BSUB;
+          int b = __ldg(trow + tok / p.block_size);
+          if (b < 0 || b >= p.num_blocks) {
+            record_error(p.err, PA_DEVERR_BLOCK_ID);
+            b = p.num_blocks;  // rows past the tensor map: TMA zero-fills
+          }
+          tma_load_4d_hint(base + s * Tile::BYTES + Tile::box(hf, my_sub), map, bar(full0 + s), 0, hf, w.h,
+                           b * p.block_size + tok % p.block_size, pol);
+        }
       }
-      issued = j + 1;
     }
     if (failed && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
-    for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)  // bounded drain
-      mbar_wait(bar(full0 + j % nst), (j / nst) & 1);
+    for (int t = gt - nst < 0 ? 0 : gt - nst; t < gt; ++t)  // loads in flight land before exit (bounded)
+      mbar_wait(bar(full0 + t % nst), (t / nst) & 1);
   } else if (warp < kKWarp) {
     // ---------------------------------------------------------------- MMA issuers
     // One thread per Q tile: warp 0 issues tile A's MMAs, warp 1 tile B's.
@@ -238,46 +257,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     // wait only on their own tile, and the pipe interleaves their work.
     if (lane == 0) {
       const int x = warp;
-      bool ok = mbar_wait(bar(B_QFULL), 0);
+      bool ok = true;
       const uint32_t kbase = smem_u32(smem + L::K_OFF), vbase = smem_u32(smem + L::V_OFF);
       const uint32_t qa = smem_u32(smem + L::Q_OFF + x * L::QTILE);
       const uint32_t sd = tmem + S_COL + x * kKeys, od = tmem + O_COL + x * D;
-      // Tile B starts half a key tile behind tile A (once P_A(0) is being
-      // written), so that the two softmaxes alternate instead of overlapping.
-      if (x == 1 && ntiles > 0) ok = ok && mbar_wait(bar(B_PLO), 0);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int sk = j % kKStages, sv = j % kVStages;
-        // S_x(j) = Q_x K_j^T.  It overwrites P_x(j-1): wait for P.V_x(j-1).
-        if (!mbar_wait(bar(B_KFULL + sk), (j / kKStages) & 1)) { ok = false; break; }
-        if (j > 0 && !mbar_wait(bar(B_OFULL + x), (j - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kb = kbase + sk * Tile::BYTES;
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-          const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * L::QHALF + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
-          tc_mma_f16(sd, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(B_SFULL + x));
-        tc_commit(bar(B_KEMPTY + sk));  // this issuer is done with K_j
-        // O_x += P_x(j) V_j in two halves of 64 keys, each as soon as its P
-        // half is in TMEM
-        if (!mbar_wait(bar(B_VFULL + sv), (j / kVStages) & 1)) { ok = false; break; }
-        const uint32_t vb = vbase + sv * Tile::BYTES;
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          if (!mbar_wait(bar((hh ? B_PHI : B_PLO) + x), j & 1)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int k4 = 0; k4 < PSTEPS / 2; ++k4) {
-            // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
-            const int kk = hh * (PSTEPS / 2) + k4;
-            const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
-            tc_mma_f16_ts(od, sd + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+      int gt = 0, nu = 0;  // key tiles and units processed by this CTA
+      for (int u = cta0; ok && u < nunits; u += nctas) {
+        TcUnit w;
+        if (!tc_unit(p, u, row_tiles, w)) {
+          if (x == 0) {
+            griddep_wait();
+            record_error(p.err, PA_DEVERR_QUERY_RANGE);
           }
+          continue;
         }
-        if (!ok) break;
-        tc_commit(bar(B_OFULL + x));
-        tc_commit(bar(B_VEMPTY + sv));  // this issuer is done with V_j
+        if (w.ntiles <= 0) continue;
+        // Q_x of this unit is in smem; the softmax warps have also finished
+        // the previous unit (its last P.V completed and O_x was read out).
+        if (!mbar_wait(bar(B_QFULL + x), nu & 1)) { ok = false; break; }
+        // Tile B starts half a key tile behind tile A (once P_A(0) is being
+        // written), so that the two softmaxes alternate instead of overlapping.
+        if (x == 1 && nu == 0 && !mbar_wait(bar(B_PLO), 0)) { ok = false; break; }
+        ++nu;
+        for (int j = 0; ok && j < w.ntiles; ++j, ++gt) {
+          const int sk = gt % kKStages, sv = gt % kVStages;
+          // S_x(j) = Q_x K_j^T.  It overwrites P_x(j-1): wait for P.V_x(j-1).
+          if (!mbar_wait(bar(B_KFULL + sk), (gt / kKStages) & 1)) { ok = false; break; }
+          if (j > 0 && !mbar_wait(bar(B_OFULL + x), (gt - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = kbase + sk * Tile::BYTES;
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * L::QHALF + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
+            tc_mma_f16(sd, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(B_SFULL + x));
+          tc_commit(bar(B_KEMPTY + sk));  // this issuer is done with K_j
+          // O_x += P_x(j) V_j in two halves of 64 keys, each as soon as its P
+          // half is in TMEM
+          if (!mbar_wait(bar(B_VFULL + sv), (gt / kVStages) & 1)) { ok = false; break; }
+          const uint32_t vb = vbase + sv * Tile::BYTES;
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            if (!mbar_wait(bar((hh ? B_PHI : B_PLO) + x), gt & 1)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int k4 = 0; k4 < PSTEPS / 2; ++k4) {
+              // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
+              const int kk = hh * (PSTEPS / 2) + k4;
+              const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
+              tc_mma_f16_ts(od, sd + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar(B_OFULL + x));
+          tc_commit(bar(B_VEMPTY + sv));  // this issuer is done with V_j
+        }
       }
       if (!ok) record_error(p.err, PA_DEVERR_TIMEOUT);
       tc_commit(bar(B_MMADONE));
@@ -288,178 +323,182 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;                // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;         // row within the tile == TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const int grow = row0 + x * kRows + row;
-    const bool valid = grow < rows;
-    const int qi = grow / G, g = grow % G;
-    const int lim = !valid ? -1 : (p.causal ? p0 + qi : kend - 1);  // last key this row may see
-    {
-      // Q row -> shared memory (K-major, 128-byte swizzle); padding rows are zero
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.q) +
-                                                        ((size_t)(qs + qi) * p.q_heads + h * G + g) * D);
-      uint8_t* qt = smem + L::Q_OFF + x * L::QTILE;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qt + (c >> 3) * L::QHALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_QFULL));
-    }
-    griddep_wait();  // before writing outputs
-
-    float m = -INFINITY, l = 0.f;  // running (possibly stale) max in log2 units, row sum
     const float sl2 = p.scale_log2;
     constexpr float kRescale = 8.f;
     const uint32_t scol = tmem + lane_addr + S_COL + x * kKeys;
     const uint32_t ocol = tmem + lane_addr + O_COL + x * D;
+    uint8_t* qt = smem + L::Q_OFF + x * L::QTILE;
     bool ok = true;
-
-    for (int j = 0; j < ntiles; ++j) {
-      if (!mbar_wait(bar(B_SFULL + x), j & 1)) { ok = false; break; }
-      tc_fence_after();
-      const int ts = k0 + j * kKeys;
-      const int nvis = lim - ts + 1;  // keys of this tile the row may see (<= 0: none)
-      const bool all_full = __all_sync(0xffffffffu, nvis >= kKeys);
-
-      // the whole S row in registers: one TMEM round trip
-      float sv[kKeys];
+    int gt = 0;  // key tiles processed by this CTA
+    for (int u = cta0; ok && u < nunits; u += nctas) {
+      TcUnit w;
+      if (!tc_unit(p, u, row_tiles, w) || w.ntiles <= 0) continue;
+      const int grow = w.row0 + x * kRows + row;
+      const bool valid = grow < w.rows;
+      const int qi = grow / G, g = grow % G;
+      const int lim = !valid ? -1 : (p.causal ? w.p0 + qi : w.kend - 1);  // last key this row may see
+      {
+        // Q row -> shared memory (K-major, 128-byte swizzle); padding rows are
+        // zero.  The previous unit's S MMAs have completed (its last P.V did).
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.q) +
+                                                          ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D);
 #pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) tmem_ld32(scol + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
-      tmem_wait_ld();
-      if (!all_full) {
-#pragma unroll
-        for (int e = 0; e < kKeys; ++e) sv[e] = e < nvis ? sv[e] : -INFINITY;
-      }
-      // row maximum: four independent chains of three-input max
-      float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < kKeys; e += 8) {
-        ma = fmax3(ma, sv[e], sv[e + 1]);
-        mb = fmax3(mb, sv[e + 2], sv[e + 3]);
-        mc = fmax3(mc, sv[e + 4], sv[e + 5]);
-        md = fmax3(md, sv[e + 6], sv[e + 7]);
-      }
-      const float mx = fmax3(ma, mb, fmaxf(mc, md)) * sl2;
-      const bool raise = mx > m + kRescale;  // also the first finite max (m = -inf)
-      // O and l are rescaled by 2^(m_old - m_new) when the maximum is raised
-      const float alpha = (raise && m != -INFINITY) ? ex2_approx(m - mx) : 1.f;
-      const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
-      if (raise) {
-        l = (m == -INFINITY) ? 0.f : l * alpha;
-        m = mx;
-      }
-      const float neg_m = m == -INFINITY ? 0.f : -m;
-
-      // P = 2^(s*sl2 - m) (masked keys hold -inf: p = 0), written over the
-      // first kKeys/2 S columns in two halves of 64 keys; each half is
-      // signalled on its own so that P.V can start on the first.  The sum runs
-      // in four packed-pair chains.
-      float sx[4] = {0.f, 0.f, 0.f, 0.f}, sy[4] = {0.f, 0.f, 0.f, 0.f};
-      const int nvalid = min(kKeys, kend - ts);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int cc = 0; cc < kKeys / 64; ++cc) {
-          const int c = hh * (kKeys / 64) + cc;
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float a0, a1;
-            ffma2(a0, a1, sv[32 * c + e], sv[32 * c + e + 1], sl2, sl2, neg_m, neg_m);
-            const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
-            const int k = (e >> 1) & 3;
-            fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
-            pk[e >> 1] = Elem<T>::pack(p0v, p1v);
-          }
-          tmem_st16u(scol + 16 * c, pk);  // keys 32c..32c+31 -> columns 16c..16c+15
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(qt + (c >> 3) * L::QHALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
         }
-        if (hh == 0) {
-          if (rescale) {
-            // rescale O_x in TMEM before P.V_x(j) starts (warp-collective).
-            // P.V_x(j-1) has completed: S_x(j) was issued after it.
-#pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-              float ov[16];
-              tmem_ld16(ocol + 16 * c, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) ov[e] *= alpha;
-              tmem_st16u(ocol + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(ov));
-            }
-          }
-          if (nvalid < kKeys) {
-            // last key tile: keys past kend came from stale slots (or were not
-            // loaded); zero their V rows so that p = 0 never meets NaN/Inf.
-            // Both Q tiles' softmax warps write the same zeros (either P.V
-            // may run first); each P.V starts only after its own group's.
-            const int s = j % kVStages;
-            if (!mbar_wait(bar(B_VFULL + s), (j / kVStages) & 1)) {
-              ok = false;
-            } else if (row >= nvalid) {
-              uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
-#pragma unroll
-              for (int hf = 0; hf < NH; ++hf)
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  *reinterpret_cast<uint4*>(vrow + hf * Tile::HALF + c * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar((hh ? B_PHI : B_PLO) + x));
+        if (lane == 0) mbar_arrive(bar(B_QFULL + x));
       }
-      l += ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
+      griddep_wait();  // before writing outputs (a no-op after the first unit)
+
+      float m = -INFINITY, l = 0.f;  // running (possibly stale) max in log2 units, row sum
+      for (int j = 0; j < w.ntiles; ++j, ++gt) {
+        if (!mbar_wait(bar(B_SFULL + x), gt & 1)) { ok = false; break; }
+        tc_fence_after();
+        const int ts = w.k0 + j * kKeys;
+        const int nvis = lim - ts + 1;  // keys of this tile the row may see (<= 0: none)
+        const bool all_full = __all_sync(0xffffffffu, nvis >= kKeys);
+
+        // the whole S row in registers: one TMEM round trip
+        float sv[kKeys];
+#pragma unroll
+        for (int c = 0; c < kKeys / 32; ++c) tmem_ld32(scol + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
+        tmem_wait_ld();
+        if (!all_full) {
+#pragma unroll
+          for (int e = 0; e < kKeys; ++e) sv[e] = e < nvis ? sv[e] : -INFINITY;
+        }
+        // row maximum: four independent chains of three-input max
+        float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kKeys; e += 8) {
+          ma = fmax3(ma, sv[e], sv[e + 1]);
+          mb = fmax3(mb, sv[e + 2], sv[e + 3]);
+          mc = fmax3(mc, sv[e + 4], sv[e + 5]);
+          md = fmax3(md, sv[e + 6], sv[e + 7]);
+        }
+        const float mx = fmax3(ma, mb, fmaxf(mc, md)) * sl2;
+        const bool raise = mx > m + kRescale;  // also the first finite max (m = -inf)
+        // O and l are rescaled by 2^(m_old - m_new) when the maximum is raised
+        const float alpha = (raise && m != -INFINITY) ? ex2_approx(m - mx) : 1.f;
+        const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+        if (raise) {
+          l = (m == -INFINITY) ? 0.f : l * alpha;
+          m = mx;
+        }
+        const float neg_m = m == -INFINITY ? 0.f : -m;
+
+        // P = 2^(s*sl2 - m) (masked keys hold -inf: p = 0), written over the
+        // first kKeys/2 S columns in two halves of 64 keys; each half is
+        // signalled on its own so that P.V can start on the first.  The sum
+        // runs in four packed-pair chains.
+        float sx[4] = {0.f, 0.f, 0.f, 0.f}, sy[4] = {0.f, 0.f, 0.f, 0.f};
+        const int nvalid = min(kKeys, w.kend - ts);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int cc = 0; cc < kKeys / 64; ++cc) {
+            const int c = hh * (kKeys / 64) + cc;
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float a0, a1;
+              ffma2(a0, a1, sv[32 * c + e], sv[32 * c + e + 1], sl2, sl2, neg_m, neg_m);
+              const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
+              const int k = (e >> 1) & 3;
+              fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
+              pk[e >> 1] = Elem<T>::pack(p0v, p1v);
+            }
+            tmem_st16u(scol + 16 * c, pk);  // keys 32c..32c+31 -> columns 16c..16c+15
+          }
+          if (hh == 0) {
+            if (rescale) {
+              // rescale O_x in TMEM before P.V_x(j) starts (warp-collective).
+              // P.V_x(j-1) has completed: S_x(j) was issued after it.
+#pragma unroll
+              for (int c = 0; c < D / 16; ++c) {
+                float ov[16];
+                tmem_ld16(ocol + 16 * c, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+                tmem_st16u(ocol + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(ov));
+              }
+            }
+            if (nvalid < kKeys) {
+              // last key tile: keys past kend came from stale slots (or were
+              // not loaded); zero their V rows so that p = 0 never meets
+              // NaN/Inf.  Both Q tiles' softmax warps write the same zeros
+              // (either P.V may run first); each P.V starts only after its own
+              // group's.
+              const int s = gt % kVStages;
+              if (!mbar_wait(bar(B_VFULL + s), (gt / kVStages) & 1)) {
+                ok = false;
+              } else if (row >= nvalid) {
+                uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
+#pragma unroll
+                for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+                  for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(vrow + hf * Tile::HALF + c * 16) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar((hh ? B_PHI : B_PLO) + x));
+        }
+        l += ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
+        if (!ok) break;
+      }
+      if (ok) ok = mbar_wait(bar(B_OFULL + x), (gt - 1) & 1);  // the unit's last P.V_x
       if (!ok) break;
-    }
-    if (ok && ntiles > 0) ok = mbar_wait(bar(B_OFULL + x), (ntiles - 1) & 1);
-    if (!ok) {
-      if (lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
-    } else if (p.causal) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
-                                            ((size_t)(qs + qi) * p.q_heads + h * G + g) * D);
+      if (p.causal) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
+                                              ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float ov[32];
-        tmem_ld32(ocol + 32 * c, ov);  // warp-collective: every lane loads, valid rows store
-        tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(ocol + 32 * c, ov);  // warp-collective: every lane loads, valid rows store
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[4 * c + q] = make_uint4(Elem<T>::pack(ov[8 * q] * inv, ov[8 * q + 1] * inv),
+                                          Elem<T>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
+                                          Elem<T>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
+                                          Elem<T>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+          }
+        }
+      } else {
+        // shared-prefix partial of this key range: unnormalised o, m, l
+        const size_t pr = ((size_t)qi * p.q_heads + w.h * G + g) * p.max_splits + w.z;
+        float4* po = reinterpret_cast<float4*>(p.part_o + pr * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(ocol + 32 * c, ov);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              po[8 * c + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+          }
+        }
         if (valid) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[4 * c + q] = make_uint4(Elem<T>::pack(ov[8 * q] * inv, ov[8 * q + 1] * inv),
-                                        Elem<T>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
-                                        Elem<T>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
-                                        Elem<T>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+          p.part_m[pr] = m;
+          p.part_l[pr] = l;
         }
       }
-      tc_fence_before();
-    } else {
-      // shared-prefix partial of this key range: unnormalised o, m, l
-      tc_fence_after();
-      const size_t pr = ((size_t)qi * p.q_heads + h * G + g) * p.max_splits + blockIdx.z;
-      float4* po = reinterpret_cast<float4*>(p.part_o + pr * D);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float ov[32];
-        tmem_ld32(ocol + 32 * c, ov);
-        tmem_wait_ld();
-        if (valid) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            po[8 * c + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
-        }
-      }
-      if (valid) {
-        p.part_m[pr] = m;
-        p.part_l[pr] = l;
-      }
-      tc_fence_before();
+      tc_fence_before();  // O_x read out before the next unit's P.V overwrites it
     }
+    if (!ok && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
   }
 
   // ------------------------------------------------------------------ teardown
@@ -487,7 +526,12 @@ cudaError_t launch_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   }
   const int row_tiles = (p.max_q_len * p.group + 2 * kRows - 1) / (2 * kRows);
   const int zdim = p.causal ? p.num_reqs : (p.prefix_len + p.key_split - 1) / p.key_split;
-  dim3 grid(row_tiles, p.kv_heads, zdim);
+  const long long nunits = (long long)row_tiles * p.kv_heads * zdim;
+  if (nunits <= 0) return cudaSuccess;
+  if (nunits > INT32_MAX) return cudaErrorInvalidValue;
+  // one CTA per unit: a (row tile, head, request) grid, whose linear order is
+  // the unit order; capped: a 1-D grid of max_ctas persistent CTAs
+  const dim3 grid = p.max_ctas > 0 && p.max_ctas < nunits ? dim3(p.max_ctas) : dim3(row_tiles, p.kv_heads, zdim);
   return launch_pdl(kern, grid, dim3(kThreads), L::BYTES, stream, kmap, vmap, p);
 }
 

@@ -355,8 +355,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
 
 int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* context_lens, const void* k_cache,
                        const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq, int num_reqs,
-                       int total_q, int max_q_len, int q_heads, int kv_heads, int head_dim, int block_size,
-                       int num_blocks, float scale, void* out, pa_dtype dtype, pa_stream stream) {
+                       int total_q, int max_q_len, int max_ctas, int q_heads, int kv_heads, int head_dim,
+                       int block_size, int num_blocks, float scale, void* out, pa_dtype dtype, pa_stream stream) {
   int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
   if (st != PA_OK) return st;
   if (num_reqs < 0 || num_reqs > 65535 || total_q < 0 || max_q_len < 0 || q_heads <= 0 ||
@@ -391,6 +391,7 @@ int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* con
   p.block_size = block_size;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = 1;
+  p.max_ctas = max_ctas;
   const int bsub = block_size < 16 ? block_size : 16;
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   // blocks of >= 8 tokens: 5th-generation tensor cores (tcgen05 + TMEM);

@@ -86,6 +86,9 @@ struct PrefillParams {
   // (o, m in log2 units, l) to slot blockIdx.z of the decode workspace.
   int causal;
   int prefix_len, key_split, max_splits;
+  // tcgen05 path: CTAs launched (each takes work units b, b + gridDim.x, ...);
+  // <= 0 launches one CTA per unit
+  int max_ctas;
   float* part_o;
   float* part_m;
   float* part_l;

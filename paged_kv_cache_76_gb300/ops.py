@@ -171,7 +171,8 @@ def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_t
 
 
 def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, scale, max_q_len, out=None,
-                    stream=None):
+                    stream=None, max_ctas=0):
+    """pa_chunked_prefill; ``max_ctas`` > 0 caps the CTAs (SMs) the tensor-core path uses."""
     nb, bs, hkv, d = _cache_dims(k_cache)
     T, hq, dq = q.shape
     if dq != d:
@@ -184,7 +185,7 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
     check(_lib.lib().pa_chunked_prefill(
         _dev(q, "q"), _i32(q_start, "q_start"), _i32(context_lens, "context_lens"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _i32(block_tables, "block_tables"), int(block_tables.shape[1]), R, T,
-        int(max_q_len), hq, hkv, d, bs, nb, float(scale), _dev(out, "out"), dtype_code(q.dtype),
+        int(max_q_len), int(max_ctas), hq, hkv, d, bs, nb, float(scale), _dev(out, "out"), dtype_code(q.dtype),
         _stream(stream)), "pa_chunked_prefill")
     return out
 

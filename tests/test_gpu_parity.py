@@ -328,6 +328,43 @@ def test_chunked_prefill_matches_the_oracle(case):
     no_device_error()
 
 
+@pytest.mark.parametrize("max_ctas", [1, 2, 3, 7])
+def test_chunked_prefill_with_few_ctas_matches_one_cta_per_unit(max_ctas):
+    """The tensor-core path with max_ctas CTAs looping over work units (each
+    CTA carries its barrier phases and TMEM across several units, some of them
+    empty) gives bit-identical output to one CTA per unit, and matches the
+    oracle."""
+    o = ops()
+    hq, hkv, d, bs = 16, 2, 128, 16
+    hists, chunks = [300, 0, 41, 1000], [97, 200, 16, 130]
+    rng = np.random.default_rng(5)
+    needed = sum(-(-(h + c) // bs) for h, c in zip(hists, chunks)) + 4
+    nb = int(1.5 * needed)
+    setup, step, prefill = [], [], []
+    for i, (h, c) in enumerate(zip(hists, chunks)):
+        setup.append(("add", i))
+        if h:
+            setup.append(("append", i, h))
+        step.append(("append", i, c))
+        prefill.append((i, c, h + c))
+    wl = W.Workload(name="prefill_few_ctas", dtype="bf16", q_heads=hq, kv_heads=hkv, head_dim=d, block_size=bs,
+                    num_blocks=nb, scale=1.0 / np.sqrt(d), free_order=rng.permutation(nb).astype(np.int32),
+                    setup_ops=setup, step_ops=step, prefill=prefill, seed=11)
+    vals = W.make_values(wl)
+    dev = DeviceStep(wl, vals)
+    ref = oracle_step(wl, vals)
+    dev.run()
+    no_device_error()
+    full = dev.out_prefill.clone()
+    out = torch.full_like(full, float("nan"))
+    o.chunked_prefill(dev.q_prefill, dev.q_start, dev.pre_lens, dev.k_cache, dev.v_cache, dev.pre_tables,
+                      wl.scale, dev.max_q_len, out=out, max_ctas=max_ctas)
+    torch.cuda.synchronize()
+    no_device_error()
+    assert torch.equal(out, full)
+    assert_close(out, ref["prefill"], f"prefill max_ctas={max_ctas}")
+
+
 def test_mixed_prefill_and_decode_step():
     wl = W.mixed_prefill_decode(n_prefill=2, chunk=128, hist_lo=0, hist_hi=700, n_decode=12, dec_lo=256,
                                 dec_hi=2000)
