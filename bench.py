@@ -58,6 +58,17 @@ def dist_env():
     return ws, rank, local
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed alone)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -262,8 +273,12 @@ class Step:
                               max_ctas=self.prefill_ctas)
             self.ev_join.record(self.side)
         elif self.pre:
+            if ev is not None and not self.dec:
+                ev[0].record(stream)
             o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
                               d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=stream)
+            if ev is not None and not self.dec:
+                ev[1].record(stream)
         if self.dec and self.prefix_len:
             if ev is not None:
                 ev[0].record(stream)
@@ -496,24 +511,40 @@ def main():
         raise RuntimeError("device error recorded during warm-up")
 
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = None
+    if total_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     clocks = ClockSampler(torch.cuda.current_device() if ws == 1 else local)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
     launches0 = ops.launch_count()
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for i in range(args.steps):
-            step.run(stream)
-        t_end.record(stream)
+    if flush is None:
+        # inputs larger than L2: the K steps back to back in one event pair
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(args.steps):
+                step.run(stream)
+            t_end.record(stream)
+    else:
+        # a step that fits in L2: each step in its own event pair, with a
+        # write of a buffer twice the L2 between steps (outside the pairs)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                pairs[i][0].record(stream)
+                step.run(stream)
+                pairs[i][1].record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     launches = ops.launch_count() - launches0
     clk = clocks.stop()
     if ws > 1:
         torch.distributed.barrier()
-    ms = t_start.elapsed_time(t_end)
+    ms = t_start.elapsed_time(t_end) if flush is None else sum(a.elapsed_time(b) for a, b in pairs)
     if ops.get_device_error(stream) != 0:
         raise RuntimeError("device error recorded during the timed region")
     t = torch.tensor([ms], dtype=torch.float64, device=device)
@@ -526,11 +557,13 @@ def main():
     # bracketed by CUDA events on its stream.  (Kept out of the region above:
     # an event between two kernels ends their programmatic-launch overlap.)
     dec_ms = None
-    if step.dec:
+    if step.dec or step.pre:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         with torch.cuda.stream(stream):
             for i in range(args.steps):
+                if flush is not None:
+                    flush.fill_(i & 0xFF)
                 step.run(stream, evs[i])
         stream.synchronize()
         dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
@@ -606,7 +639,10 @@ def main():
             "prefill_chunks": step.chunks if step.pre else None,
             "copy_pairs": step.n_pairs,
             "bytes_per_step": nb,
-            "l2": f"inputs larger than L2: {total_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2",
+            "l2": (f"inputs larger than L2: {total_bytes / 1e6:.0f} MB moved per step vs {L2_BYTES / 1e6:.0f} MB L2"
+                   if flush is None else
+                   f"L2 flushed between steps ({2 * L2_BYTES / 1e6:.0f} MB written outside each step's event pair; "
+                   f"{total_bytes / 1e6:.1f} MB moved per step)"),
             "parallelism": f"replicas x{ws}",
             "streams": (f"prefill on a second, highest-priority stream over {step.prefill_ctas or 'all'} CTAs, "
                         f"concurrent with decode" if step.side is not None else "one"),
@@ -657,6 +693,25 @@ def main():
             res["roofline"]["unique_bytes_per_launch"] = nb["decode_unique"]
             res["roofline"]["achieved_unique"] = round(nb["decode_unique"] / (dec_ms * 1e-3) / 1e9, 1)
             res["roofline"]["frac_unique"] = round(nb["decode_unique"] / (dec_ms * 1e-3) / 1e9 / peak, 4)
+    elif step.pre:
+        # prefill alone: the tcgen05 kernel is tensor-bound; causal QK^T + PV
+        # flops of the visible (query, key) pairs against the measured bf16 peak
+        tpeak, tkind = measured_tensor_peak()
+        fl = nb["prefill_flops"]
+        res["roofline"] = {
+            "kernel": "attn_tc_kernel" if wl.block_size >= 8 else "chunked_prefill_kernel",
+            "bound": "tensor",
+            "achieved": round(fl / (dec_ms * 1e-3) / 1e12, 1),
+            "peak": tpeak,
+            "peak_kind": tkind,
+            "unit": "TFLOP/s",
+            "frac": round(fl / (dec_ms * 1e-3) / 1e12 / tpeak, 4),
+            "traffic": None,
+            "algorithmic_flops_per_launch": fl,
+            "avg_launch_ms": round(dec_ms, 5),
+            "timing": "CUDA events around each of K chunked-prefill launches on the bench stream, in a second "
+                      "pass of the same K steps",
+        }
     res["e2e"] = {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                   "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps, "mode": e2e_mode,
                   "ms_per_step": round(e2e_s / args.e2e_steps * 1e3, 4)}

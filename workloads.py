@@ -255,12 +255,33 @@ def mixed_prefill_decode(seed: int = 0, n_prefill: int = 4, chunk: int = 512, hi
     )
 
 
+def mixed_prefill_part(seed: int = 0) -> Workload:
+    """The prefill half of mixed_prefill_decode alone (same 4 chunks and
+    histories; pool sized for them): a tensor-core workload for profiling."""
+    wl = mixed_prefill_decode(seed=seed, n_decode=0)
+    wl.name = "mixed_prefill_part"
+    wl.note = "prefill chunks of the mixed step only"
+    return wl
+
+
+def mixed_decode_part_small(seed: int = 0) -> Workload:
+    """A 24-request decode shaped like mixed_prefill_decode's decode half
+    (28/4 heads, D=128, bs=16, contexts U{256..16384}), with a pool small
+    enough for multi-pass profiler captures."""
+    wl = mixed_prefill_decode(seed=seed, n_prefill=0, n_decode=24)
+    wl.name = "mixed_decode_part_small"
+    wl.note = "decode of the mixed step's shape, 24 requests"
+    return wl
+
+
 WORKLOADS = {
     "tiny_paged_decode": tiny_paged_decode,
     "llama8b_gqa_decode": llama8b_gqa_decode,
     "long_context_splitk_decode": long_context_splitk_decode,
     "prefix_shared_cow_decode": prefix_shared_cow_decode,
     "mixed_prefill_decode": mixed_prefill_decode,
+    "mixed_prefill_part": mixed_prefill_part,
+    "mixed_decode_part_small": mixed_decode_part_small,
 }
 
 
