@@ -404,6 +404,85 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
     o[d] = Elem<T>::from((((s_acc[0][d] + s_acc[1][d]) + s_acc[2][d]) + s_acc[3][d]) * inv);
 }
 
+// The same merge with one warp per row, for at most 32 partitions: lane c
+// holds m_c and l_c, each lane owns D/32 output dims, and the o partials are
+// loaded eight partitions at a time ahead of the sums, so a row costs about
+// one round trip to L2.  Partitions are added in order (deterministic).
+template <int D, typename T>
+__global__ void __launch_bounds__(256) lse_merge_warp_kernel(const MergeParams p) {
+  constexpr int V = D / 32;
+  constexpr int CH = 8;  // o partials in flight per lane
+  griddep_wait();        // the partials come from the kernel before this one
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= p.num_seqs * p.q_heads) return;
+  const int r = row / p.q_heads;
+  int ctx = __ldg(p.lens + r);
+  ctx = ctx < p.tok_begin ? p.tok_begin : (ctx > p.cap ? p.cap : ctx);
+  const int nsplit = p.extra_slots + (ctx - p.tok_begin + p.split_tokens - 1) / p.split_tokens;
+  if (nsplit <= 1 && !p.always) return;  // pa_decode_partial wrote this row directly
+  const float* pm = p.part_m + (size_t)row * p.max_splits;
+  const float* pl = p.part_l + (size_t)row * p.max_splits;
+  const float* po = p.part_o + (size_t)row * p.max_splits * D + lane * V;
+  const float mc = lane < nsplit ? pm[lane] : -INFINITY;
+  const float lc = lane < nsplit ? pl[lane] : 0.f;
+  float x[CH][V];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    if (c < nsplit) {
+      if constexpr (V == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(po + (size_t)c * D);
+        x[c][0] = v.x, x[c][1] = v.y, x[c][2] = v.z, x[c][3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(po + (size_t)c * D);
+        x[c][0] = v.x, x[c][1] = v.y;
+      }
+    }
+  }
+  float M = mc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w = lane < nsplit ? exp2f(mc - M) : 0.f;
+  float den = w * lc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  float a[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) a[i] = 0.f;
+  for (int c0 = 0; c0 < nsplit; c0 += CH) {
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const float wc = __shfl_sync(0xffffffffu, w, (c0 + c) & 31);
+      if (c0 + c < nsplit) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) a[i] += wc * x[c][i];
+      }
+    }
+    // next chunk of o partials
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int cc = c0 + CH + c;
+      if (cc < nsplit) {
+        if constexpr (V == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(po + (size_t)cc * D);
+          x[c][0] = v.x, x[c][1] = v.y, x[c][2] = v.z, x[c][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(po + (size_t)cc * D);
+          x[c][0] = v.x, x[c][1] = v.y;
+        }
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  T* o = reinterpret_cast<T*>(p.out) + (size_t)row * D + lane * V;
+  if constexpr (V == 4) {
+    *reinterpret_cast<uint2*>(o) = make_uint2(Elem<T>::pack(a[0] * inv, a[1] * inv), Elem<T>::pack(a[2] * inv, a[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(o) = Elem<T>::pack(a[0] * inv, a[1] * inv);
+  }
+}
+
 template <int D, int BSUB, int NT, typename T>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                             cudaStream_t stream) {
@@ -457,6 +536,16 @@ cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vm
 }
 
 cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream) {
+  if (p.max_splits <= 32) {  // one warp per row
+    const dim3 grid((p.num_seqs * p.q_heads + 7) / 8), block(256);
+    if (head_dim == 128)
+      return dt == PA_BF16 ? launch_pdl(lse_merge_warp_kernel<128, __nv_bfloat16>, grid, block, 0, stream, p)
+                           : launch_pdl(lse_merge_warp_kernel<128, __half>, grid, block, 0, stream, p);
+    if (head_dim == 64)
+      return dt == PA_BF16 ? launch_pdl(lse_merge_warp_kernel<64, __nv_bfloat16>, grid, block, 0, stream, p)
+                           : launch_pdl(lse_merge_warp_kernel<64, __half>, grid, block, 0, stream, p);
+    return cudaErrorInvalidValue;
+  }
   const dim3 grid(p.num_seqs * p.q_heads), block(128);
   if (head_dim == 128)
     return dt == PA_BF16 ? launch_pdl(lse_merge_kernel<128, __nv_bfloat16>, grid, block, 0, stream, p)
