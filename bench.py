@@ -194,6 +194,9 @@ class Step:
                 if nshared >= 8:
                     self.prefix_len = nshared * wl.block_size
                     self.h["prefix_blocks"] = torch.tensor(t[0, :nshared], dtype=torch.int32).pin_memory()
+                    # the suffix partition: the workload's, else the call's automatic choice
+                    self.split = ops.decode_shared_prefix_split_tokens(maxblk, wl.block_size, self.prefix_len,
+                                                                       wl.split_tokens)
                     n = ops.decode_shared_prefix_workspace_size(len(wl.decode_seqs), wl.q_heads, wl.head_dim, maxblk,
                                                                 wl.block_size, self.prefix_len, self.split)
             self.workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None

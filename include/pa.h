@@ -206,6 +206,13 @@ int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* c
 size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq,
                                               int block_size, int prefix_len, int split_tokens);
 
+/* The partition size pa_decode_shared_prefix uses for the suffixes: split_tokens
+ * if it is > 0, else about a quarter of the suffix bound
+ * (max_blocks_per_seq * block_size - prefix_len), at least 128 tokens and at
+ * most pa_decode_split_tokens(max_blocks_per_seq, block_size, 0).  Negative:
+ * a pa_status error for invalid arguments. */
+int pa_decode_shared_prefix_split_tokens(int max_blocks_per_seq, int block_size, int prefix_len, int split_tokens);
+
 int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* prefix_blocks,
                             int prefix_len, const int32_t* block_tables, int max_blocks_per_seq,
                             const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads, int head_dim,

@@ -25,6 +25,7 @@ __all__ = [
     "chunked_prefill",
     "decode_shared_prefix",
     "decode_shared_prefix_workspace_size",
+    "decode_shared_prefix_split_tokens",
     "get_device_error",
     "launch_count",
     "dtype_code",
@@ -147,6 +148,13 @@ def decode_shared_prefix_workspace_size(num_seqs, q_heads, head_dim, max_blocks_
                                         split_tokens=0) -> int:
     return int(_lib.lib().pa_decode_shared_prefix_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq,
                                                                  block_size, prefix_len, split_tokens))
+
+
+def decode_shared_prefix_split_tokens(max_blocks_per_seq, block_size, prefix_len, split_tokens=0) -> int:
+    """Suffix partition size pa_decode_shared_prefix uses (0: its automatic choice)."""
+    return check(_lib.lib().pa_decode_shared_prefix_split_tokens(int(max_blocks_per_seq), int(block_size),
+                                                                 int(prefix_len), int(split_tokens)),
+                 "pa_decode_shared_prefix_split_tokens")
 
 
 def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_tables, context_lens, scale, out=None,

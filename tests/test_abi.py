@@ -45,6 +45,12 @@ def test_host_only_calls(lib):
     assert lib.pa_decode_split_tokens(256, 16, 24) == _lib.PA_ERR_INVALID      # not a multiple of 16
     assert lib.pa_decode_split_tokens(256, 32, 48) == _lib.PA_ERR_INVALID      # not a multiple of bs=32
     assert lib.pa_decode_split_tokens(256, 4, 2048) == _lib.PA_ERR_INVALID     # > 256 * bs
+    # shared-prefix suffixes: a quarter of the suffix bound, >= 128, <= the decode default
+    assert lib.pa_decode_shared_prefix_split_tokens(160, 16, 2048, 0) == 128    # suffix bound 512
+    assert lib.pa_decode_shared_prefix_split_tokens(256, 16, 1024, 0) == 384    # bound 3072 -> 768, capped
+    assert lib.pa_decode_shared_prefix_split_tokens(114, 16, 1024, 0) == 208    # bound 800 -> 200 -> 208
+    assert lib.pa_decode_shared_prefix_split_tokens(160, 16, 2048, 64) == 64    # explicit
+    assert lib.pa_decode_shared_prefix_split_tokens(160, 16, 2050, 0) == _lib.PA_ERR_INVALID
     # one partition needs no scratch; several need o + m + l per (seq, head, partition)
     assert lib.pa_decode_workspace_size(64, 32, 128, 24, 16, 0) == 0
     ws = lib.pa_decode_workspace_size(8, 64, 128, 8192, 16, 512)
