@@ -30,10 +30,57 @@ Readings (the pages disagree or are silent):
   table shares that block; otherwise the caller copies it first (cow).
 * cow on a block with refcount 1 is a no-op that returns (b, b).
 * Every operation either succeeds fully or leaves the state unchanged.
+
+Automatic prefix caching ("Khám phá vLLM … phần 2", prefix caching;
+"2.1 PagedAttention" §9.2-9.3), when enabled:
+
+* only full blocks are cached.  Block i of a request gets the hash
+  H(h_{i-1}, its token ids), chained from the previous block's hash, with a
+  per-request salt in place of h_{-1} (the pages fold a cache salt into the
+  first block's hash so that only requests with the same salt share blocks).
+  H is 64-bit FNV-1a over the parent hash (8 bytes, little-endian) followed
+  by the token ids (4 bytes each, little-endian, two's complement); the pages
+  leave the function open (Python's hash or SHA-256), FNV-1a is a published
+  one that a C implementation can reproduce exactly.
+* a new request looks its prompt's full blocks up in order and stops at the
+  first miss (find_longest_cache_hit); hits are touched.  Reading: the hit
+  is capped at floor((n-1)/bs) blocks of an n-token prompt, so that at least
+  one prompt token is computed (the model needs it to produce the next
+  token); the pages' example always continues past the cached prefix.
+* a block is registered (hash -> block) when it becomes full through an
+  append that carries token ids; if that hash is already cached by another
+  block, the new block stays unregistered (the first one remains the cached
+  copy).  Appends without token ids end the request's hashing.
+* a freed zero-count block with a hash goes to the tail of the free queue,
+  without one to the head (the free_blocks rule above), so cached blocks are
+  evicted in release order, the first block of a request last.
+* a cached block loses its hash only when the free queue hands it out again
+  (popleft): its map entry is removed then.
 """
 from __future__ import annotations
 
-__all__ = ["NoFreeBlocks", "AllocError", "FreeBlockQueue", "BlockPool", "SequenceManager"]
+__all__ = ["NoFreeBlocks", "AllocError", "FreeBlockQueue", "BlockPool", "SequenceManager", "fnv1a64",
+           "block_hash"]
+
+FNV64_OFFSET = 0xCBF29CE484222325
+FNV64_PRIME = 0x100000001B3
+MASK64 = (1 << 64) - 1
+
+
+def fnv1a64(data: bytes) -> int:
+    """64-bit FNV-1a: for each byte, xor it in, then multiply by the FNV prime."""
+    h = FNV64_OFFSET
+    for byte in data:
+        h ^= byte
+        h = (h * FNV64_PRIME) & MASK64
+    return h
+
+
+def block_hash(parent: int, tokens) -> int:
+    """Chained hash of one full block: FNV-1a of parent (8 bytes LE) + token ids (4 bytes LE each)."""
+    data = (parent & MASK64).to_bytes(8, "little") + b"".join(
+        (int(t) & 0xFFFFFFFF).to_bytes(4, "little") for t in tokens)
+    return fnv1a64(data)
 
 
 class NoFreeBlocks(Exception):
@@ -130,6 +177,9 @@ class BlockPool:
         self.ref_cnt = [0] * num_blocks
         self.block_hash = [None] * num_blocks
         self.free_block_queue = FreeBlockQueue(order)
+        self.caching = False
+        self.cached_block_hash_to_block = {}
+        self.evictions = 0
 
     def get_num_free_blocks(self):
         return len(self.free_block_queue)
@@ -141,6 +191,13 @@ class BlockPool:
         for b in blocks:
             assert self.ref_cnt[b] == 0
             self.ref_cnt[b] += 1
+            h = self.block_hash[b]
+            if h is not None:
+                # a cached block about to be overwritten: it leaves the cache
+                if self.cached_block_hash_to_block.get(h) == b:
+                    del self.cached_block_hash_to_block[h]
+                self.block_hash[b] = None
+                self.evictions += 1
         return blocks
 
     def free_blocks(self, ordered_blocks):
@@ -171,6 +228,17 @@ class SequenceManager:
         self.num_tokens = {}
         self.cow_copies = 0
         self.alloc_failures = 0
+        # prefix caching: per request the salt, the hash of its last full
+        # block (the salt before the first) and the token ids of its partial
+        # last block (None: its tokens are not known, nothing more is hashed)
+        self.salt = {}
+        self.parent = {}
+        self.pending = {}
+        self.lookup_blocks = 0
+        self.hit_blocks = 0
+
+    def enable_prefix_caching(self):
+        self.pool.caching = True
 
     # -- queries -----------------------------------------------------------
     def num_free(self):
@@ -198,14 +266,71 @@ class SequenceManager:
         if seq not in self.tables:
             raise AllocError(f"unknown sequence {seq}")
 
-    def add_seq(self, seq):
+    def add_seq(self, seq, salt=0):
         if seq in self.tables:
             raise AllocError(f"sequence {seq} exists")
         self.tables[seq] = []
         self.num_tokens[seq] = 0
+        self.salt[seq] = salt
+        self.parent[seq] = salt
+        self.pending[seq] = []
+
+    def add_seq_cached(self, seq, tokens, salt=0):
+        """New request with prompt ``tokens``: its table starts with the longest
+        run of cached full blocks of the prompt (at most floor((n-1)/bs)).
+        Returns the number of prompt tokens covered (a multiple of bs)."""
+        self.add_seq(seq, salt)
+        if not self.pool.caching:
+            return 0
+        bs = self.block_size
+        nfull = (len(tokens) - 1) // bs if len(tokens) > 0 else 0
+        parent, hits = salt, []
+        for i in range(nfull):
+            h = block_hash(parent, tokens[i * bs:(i + 1) * bs])
+            self.lookup_blocks += 1
+            b = self.pool.cached_block_hash_to_block.get(h)
+            if b is None:
+                break
+            hits.append(b)
+            parent = h
+        self.hit_blocks += len(hits)
+        self.pool.touch(hits)
+        self.tables[seq] = hits
+        self.num_tokens[seq] = len(hits) * bs
+        self.parent[seq] = parent
+        return len(hits) * bs
 
     def append_slots(self, seq, n):
         """Give the next ``n`` tokens of ``seq`` their slots, growing on demand."""
+        slots = self._grow(seq, n)
+        if n > 0:
+            self.pending[seq] = None  # token ids unknown: no more hashing for seq
+        return slots
+
+    def append_tokens(self, seq, tokens):
+        """append_slots for tokens whose ids are known: every block they fill is
+        hashed and, with prefix caching on, registered unless its hash is
+        already cached."""
+        tokens = [int(t) for t in tokens]
+        slots = self._grow(seq, len(tokens))
+        pend = self.pending[seq]
+        if pend is None:
+            return slots
+        bs = self.block_size
+        first = self.num_tokens[seq] - len(tokens)  # index of tokens[0] in seq
+        for i, t in enumerate(tokens):
+            pend.append(t)
+            if len(pend) == bs:
+                h = block_hash(self.parent[seq], pend)
+                b = self.tables[seq][(first + i) // bs]
+                if self.pool.caching and h not in self.pool.cached_block_hash_to_block:
+                    self.pool.cached_block_hash_to_block[h] = b
+                    self.pool.block_hash[b] = h
+                self.parent[seq] = h
+                pend.clear()
+        return slots
+
+    def _grow(self, seq, n):
         self._need(seq)
         if n < 0:
             raise AllocError("negative token count")
@@ -238,6 +363,14 @@ class SequenceManager:
         self.pool.touch(blocks)
         self.tables[dst] = list(blocks)
         self.num_tokens[dst] = n_tokens
+        # dst continues the hash chain only from a full, hashed last block
+        self.salt[dst] = self.salt[src]
+        if n_tokens == 0:
+            self.parent[dst], self.pending[dst] = self.salt[src], []
+        elif n_tokens % self.block_size == 0 and self.pool.block_hash[blocks[-1]] is not None:
+            self.parent[dst], self.pending[dst] = self.pool.block_hash[blocks[-1]], []
+        else:
+            self.pending[dst] = None
 
     def cow(self, seq, logical_block):
         """Make ``seq``'s logical block private; return (src, dst) to copy."""
@@ -263,6 +396,7 @@ class SequenceManager:
         self.pool.free_blocks(list(reversed(self.tables[seq])))
         del self.tables[seq]
         del self.num_tokens[seq]
+        del self.salt[seq], self.parent[seq], self.pending[seq]
 
     # -- workload scripts ------------------------------------------------------
     def run(self, ops):
@@ -274,6 +408,12 @@ class SequenceManager:
                 self.add_seq(op[1])
             elif kind == "append":
                 slots.extend(self.append_slots(op[1], op[2]))
+            elif kind == "enable_caching":
+                self.enable_prefix_caching()
+            elif kind == "add_cached":  # (kind, seq, prompt tokens, salt)
+                self.add_seq_cached(op[1], op[2], op[3] if len(op) > 3 else 0)
+            elif kind == "append_tokens":  # (kind, seq, token ids)
+                slots.extend(self.append_tokens(op[1], op[2]))
             elif kind == "share":
                 self.share(op[1], op[2], op[3])
             elif kind == "cow":
