@@ -363,6 +363,53 @@ int pa_alloc_ref(const pa_alloc* a, int block_id);
 int pa_alloc_free_list(const pa_alloc* a, int32_t* out, int cap);
 int pa_alloc_get_stats(const pa_alloc* a, pa_alloc_stats* out);
 
+/* ----------------------------------------------------------------------------
+ * Automatic prefix caching ("Khám phá vLLM … phần 2", prefix caching;
+ * "2.1 PagedAttention" §9.2-§9.3).  Off until pa_alloc_enable_prefix_caching.
+ *
+ * Only FULL blocks are cached.  Block i of a sequence has the chained hash
+ * h_i = pa_block_hash(h_{i-1}, its block_size token ids), with the sequence's
+ * salt as h_{-1}; the allocator keeps a map hash -> block.
+ *  - pa_alloc_add_seq_cached: a new sequence whose table starts with the
+ *    longest run of cached blocks matching its prompt's full blocks, looked up
+ *    in order up to the first miss, at most floor((n_tokens-1)/block_size)
+ *    blocks (at least one prompt token is left to compute).  Hit blocks get
+ *    refcount +1 and, if they were free, leave the free queue.
+ *    *n_cached_out = tokens covered (a multiple of block_size).
+ *  - pa_alloc_append_tokens: pa_alloc_append_slots for tokens whose ids are
+ *    known; each block they fill is registered (hash -> block) unless that
+ *    hash is already cached.  After pa_alloc_append_slots (ids unknown) a
+ *    sequence registers nothing more.
+ *  - Freeing: blocks whose count reaches zero go to the HEAD of the free queue
+ *    if they carry no hash (as above) and to the TAIL if they do, in release
+ *    order, so cached blocks are evicted oldest-released first and a
+ *    request's first block last.
+ *  - A cached block loses its hash only when the free queue hands it out
+ *    again (new block, CoW copy); its map entry is removed then.
+ *  - pa_alloc_share continues the hash chain into dst only when the shared
+ *    part ends on a full, hashed block.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int64_t lookup_blocks;  /* prompt blocks looked up by pa_alloc_add_seq_cached */
+  int64_t hit_blocks;     /* ... of which were found                          */
+  int64_t evictions;      /* cached blocks handed out again (hash dropped)     */
+  int64_t cached_blocks;  /* entries in the hash map now                       */
+} pa_prefix_cache_stats;
+
+/* 64-bit FNV-1a over parent (8 bytes, little-endian) followed by the n token
+ * ids (4 bytes each, little-endian, two's complement). */
+uint64_t pa_block_hash(uint64_t parent, const int32_t* tokens, int n);
+int pa_alloc_enable_prefix_caching(pa_alloc* a);
+/* seq_id must be new; tokens may be NULL when n_tokens == 0; n_cached_out may
+ * be NULL.  With caching off this is pa_alloc_add_seq and *n_cached_out = 0. */
+int pa_alloc_add_seq_cached(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, uint64_t salt,
+                            int* n_cached_out);
+/* Errors as pa_alloc_append_slots; tokens may be NULL when n_tokens == 0. */
+int pa_alloc_append_tokens(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, int32_t* slots_out);
+/* *is_cached_out = 1 and *hash_out = its hash if block_id is in the map, else 0. */
+int pa_alloc_block_hash(const pa_alloc* a, int block_id, uint64_t* hash_out, int* is_cached_out);
+int pa_alloc_get_prefix_cache_stats(const pa_alloc* a, pa_prefix_cache_stats* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,6 +49,10 @@ class AllocStats(C.Structure):
         "waste_slots")]
 
 
+class PrefixCacheStats(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("lookup_blocks", "hit_blocks", "evictions", "cached_blocks")]
+
+
 _P = C.c_void_p
 _I = C.c_int
 _I32P = C.POINTER(C.c_int32)
@@ -88,6 +92,12 @@ PROTOTYPES = {
     "pa_alloc_ref": (_I, [_P, _I]),
     "pa_alloc_free_list": (_I, [_P, _I32P, _I]),
     "pa_alloc_get_stats": (_I, [_P, C.POINTER(AllocStats)]),
+    "pa_block_hash": (C.c_uint64, [C.c_uint64, _I32P, _I]),
+    "pa_alloc_enable_prefix_caching": (_I, [_P]),
+    "pa_alloc_add_seq_cached": (_I, [_P, _I, _I32P, _I, C.c_uint64, C.POINTER(_I)]),
+    "pa_alloc_append_tokens": (_I, [_P, _I, _I32P, _I, _I32P]),
+    "pa_alloc_block_hash": (_I, [_P, _I, C.POINTER(C.c_uint64), C.POINTER(_I)]),
+    "pa_alloc_get_prefix_cache_stats": (_I, [_P, C.POINTER(PrefixCacheStats)]),
 }
 
 _lock = threading.Lock()

@@ -99,6 +99,36 @@ class BlockAllocator:
                                             C.byref(n)), "pa_alloc_common_prefix")
         return int(n.value)
 
+    # -- automatic prefix caching -------------------------------------------
+    def enable_prefix_caching(self):
+        _chk(self._L.pa_alloc_enable_prefix_caching(self._h), "pa_alloc_enable_prefix_caching")
+
+    def add_seq_cached(self, seq: int, tokens, salt: int = 0) -> int:
+        """New sequence whose table starts with its prompt's cached blocks; returns the tokens covered."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = C.c_int(0)
+        _chk(self._L.pa_alloc_add_seq_cached(self._h, int(seq), _i32p(t) if t.size else None, int(t.size),
+                                             int(salt) & 0xFFFFFFFFFFFFFFFF, C.byref(n)), "pa_alloc_add_seq_cached")
+        return int(n.value)
+
+    def append_tokens(self, seq: int, tokens) -> np.ndarray:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = np.empty(t.size, dtype=np.int32)
+        _chk(self._L.pa_alloc_append_tokens(self._h, int(seq), _i32p(t) if t.size else None, int(t.size),
+                                            _i32p(out)), "pa_alloc_append_tokens")
+        return out
+
+    def block_hash(self, block: int):
+        """The block's cached hash, or None if it is not in the cache."""
+        h, c = C.c_uint64(0), C.c_int(0)
+        _chk(self._L.pa_alloc_block_hash(self._h, int(block), C.byref(h), C.byref(c)), "pa_alloc_block_hash")
+        return int(h.value) if c.value else None
+
+    def prefix_cache_stats(self) -> dict:
+        s = _lib.PrefixCacheStats()
+        _chk(self._L.pa_alloc_get_prefix_cache_stats(self._h, C.byref(s)), "pa_alloc_get_prefix_cache_stats")
+        return {name: int(getattr(s, name)) for name, _ in s._fields_}
+
     def seq_len(self, seq: int) -> int:
         v = C.c_int64(0)
         _chk(self._L.pa_alloc_seq_len(self._h, int(seq), C.byref(v)), "pa_alloc_seq_len")
@@ -137,6 +167,12 @@ class BlockAllocator:
                     pairs.append((s, d))
             elif kind == "free":
                 self.free_seq(op[1])
+            elif kind == "enable_caching":
+                self.enable_prefix_caching()
+            elif kind == "add_cached":
+                self.add_seq_cached(op[1], op[2], op[3] if len(op) > 3 else 0)
+            elif kind == "append_tokens":
+                slots.extend(self.append_tokens(op[1], op[2]).tolist())
             else:
                 raise ValueError(f"unknown op {kind}")
         return slots, pairs

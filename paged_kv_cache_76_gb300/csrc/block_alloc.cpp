@@ -11,7 +11,12 @@
 //  * sharing (many tables point at one block) and Copy-on-Write (§6);
 //  * release in reverse order; zero-count blocks go to the head of the queue
 //    in that order (the free_blocks rule of §9.3 for blocks without a prefix
-//    hash), so the tail block of a finished request is reused first.
+//    hash), so the tail block of a finished request is reused first;
+//  * automatic prefix caching (off by default): full blocks carry a chained
+//    64-bit FNV-1a hash of their token ids, a hash -> block map finds them
+//    again for a new request's prompt, freed hashed blocks go to the tail of
+//    the queue, and a cached block loses its hash only when the queue hands
+//    it out again ("Khám phá vLLM … phần 2", prefix caching).
 // Every entry point validates first and mutates only once success is certain.
 #include <algorithm>
 #include <cstdint>
@@ -26,7 +31,30 @@ namespace {
 struct Seq {
   std::vector<int32_t> blocks;
   int64_t num_tokens = 0;
+  // prefix caching: salt, hash of the last full block (salt before the
+  // first), token ids of the partial last block; hashable = ids known
+  uint64_t salt = 0, parent = 0;
+  std::vector<int32_t> pending;
+  bool hashable = true;
 };
+
+// 64-bit FNV-1a: for each byte, xor it into the state, then multiply by the prime.
+constexpr uint64_t kFnvOffset = 0xcbf29ce484222325ull;
+constexpr uint64_t kFnvPrime = 0x100000001b3ull;
+
+inline uint64_t fnv_bytes(uint64_t h, uint64_t v, int nbytes) {  // v's low nbytes, little-endian
+  for (int i = 0; i < nbytes; ++i) {
+    h ^= (v >> (8 * i)) & 0xffu;
+    h *= kFnvPrime;
+  }
+  return h;
+}
+
+uint64_t hash_block(uint64_t parent, const int32_t* tokens, int64_t n) {
+  uint64_t h = fnv_bytes(kFnvOffset, parent, 8);
+  for (int64_t i = 0; i < n; ++i) h = fnv_bytes(h, (uint32_t)tokens[i], 4);
+  return h;
+}
 
 }  // namespace
 
@@ -40,6 +68,12 @@ struct pa_alloc {
   std::unordered_map<int, Seq> seqs;
   int64_t cow_copies = 0;
   int64_t alloc_failures = 0;
+  // prefix caching
+  bool caching = false;
+  std::vector<uint64_t> hash;
+  std::vector<uint8_t> has_hash;
+  std::unordered_map<uint64_t, int32_t> cached;
+  int64_t lookup_blocks = 0, hit_blocks = 0, evictions = 0;
 
   void push_back(int32_t b) {
     prev[b] = tail;
@@ -71,6 +105,24 @@ struct pa_alloc {
     unlink(b);
     return b;
   }
+  // a block from the head of the queue for new use (refcount 0 -> 1); a
+  // cached block leaves the cache here
+  int32_t take() {
+    const int32_t b = pop_front();
+    if (has_hash[b]) {
+      auto it = cached.find(hash[b]);
+      if (it != cached.end() && it->second == b) cached.erase(it);
+      has_hash[b] = 0;
+      ++evictions;
+    }
+    ref[b] = 1;
+    return b;
+  }
+  // touch: one more reference; a free block leaves the queue
+  void touch(int32_t b) {
+    if (ref[b] == 0 && in_free[b]) unlink(b);
+    ref[b] += 1;
+  }
   Seq* find(int id) {
     auto it = seqs.find(id);
     return it == seqs.end() ? nullptr : &it->second;
@@ -82,6 +134,26 @@ struct pa_alloc {
 };
 
 static inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Slots for the next n tokens of s, taking blocks as the last one fills.
+static int grow(pa_alloc* a, Seq* s, int n_tokens, int32_t* slots_out) {
+  const int64_t bs = a->block_size;
+  const int64_t cur = s->num_tokens;
+  if (n_tokens > 0 && cur % bs != 0 && a->ref[s->blocks.back()] > 1) return PA_ERR_SHARED_BLOCK;
+  if (cur + n_tokens > (int64_t)INT32_MAX) return PA_ERR_INVALID;
+  const int64_t need = cdiv64(cur + n_tokens, bs) - (int64_t)s->blocks.size();
+  if (need > a->num_free) {
+    ++a->alloc_failures;
+    return PA_ERR_NO_FREE_BLOCKS;
+  }
+  for (int64_t i = 0; i < need; ++i) s->blocks.push_back(a->take());
+  if (slots_out) {
+    for (int64_t t = cur; t < cur + n_tokens; ++t)
+      slots_out[t - cur] = (int32_t)((int64_t)s->blocks[t / bs] * bs + t % bs);
+  }
+  s->num_tokens = cur + n_tokens;
+  return PA_OK;
+}
 
 extern "C" {
 
@@ -104,6 +176,8 @@ int pa_alloc_create(int num_blocks, int block_size, const int32_t* initial_free_
   a->prev.assign(num_blocks, -1);
   a->next.assign(num_blocks, -1);
   a->in_free.assign(num_blocks, 0);
+  a->hash.assign(num_blocks, 0);
+  a->has_hash.assign(num_blocks, 0);
   for (int i = 0; i < num_blocks; ++i) a->push_back(initial_free_order ? initial_free_order[i] : i);
   *out = a;
   return PA_OK;
@@ -121,26 +195,12 @@ int pa_alloc_append_slots(pa_alloc* a, int seq_id, int n_tokens, int32_t* slots_
   if (!a || n_tokens < 0) return PA_ERR_INVALID;
   Seq* s = a->find(seq_id);
   if (!s) return PA_ERR_INVALID;
-  const int64_t bs = a->block_size;
-  const int64_t cur = s->num_tokens;
-  if (n_tokens > 0 && cur % bs != 0 && a->ref[s->blocks.back()] > 1) return PA_ERR_SHARED_BLOCK;
-  const int64_t need = cdiv64(cur + n_tokens, bs) - (int64_t)s->blocks.size();
-  if (need > a->num_free) {
-    ++a->alloc_failures;
-    return PA_ERR_NO_FREE_BLOCKS;
+  const int st = grow(a, s, n_tokens, slots_out);
+  if (st == PA_OK && n_tokens > 0) {  // token ids unknown: nothing more is hashed
+    s->hashable = false;
+    s->pending.clear();
   }
-  if ((cur + n_tokens) * 1 > (int64_t)INT32_MAX) return PA_ERR_INVALID;
-  for (int64_t i = 0; i < need; ++i) {
-    int32_t b = a->pop_front();
-    a->ref[b] += 1;  // was 0: every queued block is unreferenced
-    s->blocks.push_back(b);
-  }
-  if (slots_out) {
-    for (int64_t t = cur; t < cur + n_tokens; ++t)
-      slots_out[t - cur] = (int32_t)((int64_t)s->blocks[t / bs] * bs + t % bs);
-  }
-  s->num_tokens = cur + n_tokens;
-  return PA_OK;
+  return st;
 }
 
 int pa_alloc_share(pa_alloc* a, int dst_seq, int src_seq, int n_tokens) {
@@ -151,11 +211,20 @@ int pa_alloc_share(pa_alloc* a, int dst_seq, int src_seq, int n_tokens) {
   if (n_tokens < 0 || n_tokens > s->num_tokens) return PA_ERR_INVALID;
   const int64_t nblk = cdiv64(n_tokens, a->block_size);
   d->blocks.assign(s->blocks.begin(), s->blocks.begin() + nblk);
-  for (int32_t b : d->blocks) {
-    if (a->ref[b] == 0 && a->in_free[b]) a->unlink(b);  // touch: revive a free block
-    a->ref[b] += 1;
-  }
+  for (int32_t b : d->blocks) a->touch(b);
   d->num_tokens = n_tokens;
+  // the hash chain continues into dst only from a full, hashed last block
+  d->salt = s->salt;
+  d->pending.clear();
+  if (n_tokens == 0) {
+    d->parent = s->salt;
+    d->hashable = true;
+  } else if (n_tokens % a->block_size == 0 && a->has_hash[d->blocks.back()]) {
+    d->parent = a->hash[d->blocks.back()];
+    d->hashable = true;
+  } else {
+    d->hashable = false;
+  }
   return PA_OK;
 }
 
@@ -172,8 +241,7 @@ int pa_alloc_cow(pa_alloc* a, int seq_id, int logical_block, int32_t* src_dst_ou
     ++a->alloc_failures;
     return PA_ERR_NO_FREE_BLOCKS;
   }
-  const int32_t n = a->pop_front();
-  a->ref[n] = 1;
+  const int32_t n = a->take();
   a->ref[b] -= 1;
   s->blocks[logical_block] = n;
   ++a->cow_copies;
@@ -189,13 +257,16 @@ int pa_alloc_free_seq(pa_alloc* a, int seq_id) {
   const std::vector<int32_t>& blocks = it->second.blocks;
   // reverse order: tail block first; zero-count blocks are prepended keeping
   // that order, i.e. pushed to the front from the last of them to the first
-  std::vector<int32_t> to_free;
-  to_free.reserve(blocks.size());
+  // (blocks without a hash); blocks with a hash are appended at the tail in
+  // release order, so they are evicted last and a request's first block last
+  std::vector<int32_t> no_hash, with_hash;
+  no_hash.reserve(blocks.size());
   for (auto rit = blocks.rbegin(); rit != blocks.rend(); ++rit) {
     a->ref[*rit] -= 1;
-    if (a->ref[*rit] == 0) to_free.push_back(*rit);
+    if (a->ref[*rit] == 0) (a->has_hash[*rit] ? with_hash : no_hash).push_back(*rit);
   }
-  for (auto rit = to_free.rbegin(); rit != to_free.rend(); ++rit) a->push_front(*rit);
+  for (auto rit = no_hash.rbegin(); rit != no_hash.rend(); ++rit) a->push_front(*rit);
+  for (int32_t b : with_hash) a->push_back(b);
   a->seqs.erase(it);
   return PA_OK;
 }
@@ -283,6 +354,88 @@ int pa_alloc_get_stats(const pa_alloc* a, pa_alloc_stats* out) {
   for (const auto& kv : a->seqs)
     st.waste_slots += (int64_t)kv.second.blocks.size() * a->block_size - kv.second.num_tokens;
   *out = st;
+  return PA_OK;
+}
+
+uint64_t pa_block_hash(uint64_t parent, const int32_t* tokens, int n) {
+  return hash_block(parent, tokens, (tokens && n > 0) ? n : 0);
+}
+
+int pa_alloc_enable_prefix_caching(pa_alloc* a) {
+  if (!a) return PA_ERR_INVALID;
+  a->caching = true;
+  return PA_OK;
+}
+
+int pa_alloc_add_seq_cached(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, uint64_t salt,
+                            int* n_cached_out) {
+  if (!a || seq_id < 0 || a->find(seq_id) || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID;
+  const int64_t bs = a->block_size;
+  // longest run of cached prompt blocks, looked up in order (nothing changes yet)
+  std::vector<int32_t> hits;
+  uint64_t parent = salt;
+  if (a->caching && n_tokens > 0) {
+    const int64_t nfull = (int64_t)(n_tokens - 1) / bs;  // leave >= 1 token to compute
+    for (int64_t i = 0; i < nfull; ++i) {
+      const uint64_t h = hash_block(parent, tokens + i * bs, bs);
+      ++a->lookup_blocks;
+      auto it = a->cached.find(h);
+      if (it == a->cached.end()) break;
+      hits.push_back(it->second);
+      parent = h;
+    }
+  }
+  a->hit_blocks += (int64_t)hits.size();
+  Seq sq;
+  sq.salt = salt;
+  sq.parent = parent;
+  sq.blocks = hits;
+  sq.num_tokens = (int64_t)hits.size() * bs;
+  for (int32_t b : hits) a->touch(b);
+  a->seqs.emplace(seq_id, std::move(sq));
+  if (n_cached_out) *n_cached_out = (int)(hits.size() * bs);
+  return PA_OK;
+}
+
+int pa_alloc_append_tokens(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, int32_t* slots_out) {
+  if (!a || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID;
+  Seq* s = a->find(seq_id);
+  if (!s) return PA_ERR_INVALID;
+  const int64_t first = s->num_tokens;
+  const int st = grow(a, s, n_tokens, slots_out);
+  if (st != PA_OK || !s->hashable) return st;
+  // register every block these tokens fill (unless its hash is already cached)
+  const int64_t bs = a->block_size;
+  for (int i = 0; i < n_tokens; ++i) {
+    s->pending.push_back(tokens[i]);
+    if ((int64_t)s->pending.size() == bs) {
+      const uint64_t h = hash_block(s->parent, s->pending.data(), bs);
+      const int32_t b = s->blocks[(first + i) / bs];
+      if (a->caching && a->cached.find(h) == a->cached.end()) {
+        a->cached.emplace(h, b);
+        a->hash[b] = h;
+        a->has_hash[b] = 1;
+      }
+      s->parent = h;
+      s->pending.clear();
+    }
+  }
+  return PA_OK;
+}
+
+int pa_alloc_block_hash(const pa_alloc* a, int block_id, uint64_t* hash_out, int* is_cached_out) {
+  if (!a || block_id < 0 || block_id >= a->num_blocks || !is_cached_out) return PA_ERR_INVALID;
+  *is_cached_out = a->has_hash[block_id] ? 1 : 0;
+  if (hash_out) *hash_out = a->has_hash[block_id] ? a->hash[block_id] : 0;
+  return PA_OK;
+}
+
+int pa_alloc_get_prefix_cache_stats(const pa_alloc* a, pa_prefix_cache_stats* out) {
+  if (!a || !out) return PA_ERR_INVALID;
+  out->lookup_blocks = a->lookup_blocks;
+  out->hit_blocks = a->hit_blocks;
+  out->evictions = a->evictions;
+  out->cached_blocks = (int64_t)a->cached.size();
   return PA_OK;
 }
 

@@ -4,7 +4,9 @@
 //   * refcount of every block == number of tables holding it;
 //   * the free queue holds exactly the blocks with refcount 0, once each;
 //   * each table has ceil(len / block_size) entries;
-//   * a failed call changes nothing (checked via a snapshot).
+//   * a failed call changes nothing (checked via a snapshot);
+//   * with prefix caching on: the number of blocks carrying a hash equals the
+//     map size the stats report.
 #include <algorithm>
 #include <cstdint>
 #include <cstdio>
@@ -73,12 +75,18 @@ int main(int argc, char** argv) {
     std::shuffle(order.begin(), order.end(), rng);
     pa_alloc* a = nullptr;
     if (pa_alloc_create(g_nb, g_bs, order.data(), &a) != PA_OK) return 1;
+    if (round % 2 == 0 && pa_alloc_enable_prefix_caching(a) != PA_OK) return 1;
+    std::vector<std::vector<int32_t>> prompts(4);
+    for (auto& p : prompts) {
+      p.resize(1 + rng() % (4 * g_bs + 3));
+      for (auto& t : p) t = (int32_t)(rng() % 3);
+    }
     std::vector<int> live;
     int next = 0;
     std::vector<int32_t> slots(4096);
     for (int i = 0; i < steps / 8; ++i) {
       Snapshot before = snap(a, live);
-      int op = rng() % 7, rc = PA_OK;
+      int op = rng() % 9, rc = PA_OK;
       int id = live.empty() ? -1 : live[rng() % live.size()];
       if (op == 0 || live.empty()) {
         rc = pa_alloc_add_seq(a, next);
@@ -101,6 +109,20 @@ int main(int argc, char** argv) {
       } else if (op == 5) {
         rc = pa_alloc_free_seq(a, id);
         if (rc == PA_OK) live.erase(std::find(live.begin(), live.end(), id));
+      } else if (op == 7) {
+        const auto& p = prompts[rng() % prompts.size()];
+        int got = -1;
+        rc = pa_alloc_add_seq_cached(a, next, p.data(), (int)p.size(), rng() % 2, &got);
+        if (rc == PA_OK) {
+          live.push_back(next++);
+          if (got < 0 || got % g_bs != 0 || got > (int)p.size() - 1) { std::printf("bad hit length\n"); return 6; }
+          before = snap(a, live);
+          rc = pa_alloc_append_tokens(a, next - 1, p.data() + got, (int)p.size() - got, slots.data());
+        }
+      } else if (op == 8) {
+        std::vector<int32_t> t(rng() % (2 * g_bs + 2));
+        for (auto& x : t) x = (int32_t)(rng() % 3);
+        rc = pa_alloc_append_tokens(a, id, t.data(), (int)t.size(), slots.data());
       } else {
         rc = pa_alloc_free_seq(a, 1 << 20);  // unknown: must fail without effect
         if (rc == PA_OK) return 4;
@@ -109,6 +131,15 @@ int main(int argc, char** argv) {
       Snapshot after = snap(a, live);
       if (rc != PA_OK && !(after == before)) { std::printf("failed call changed state (op %d rc %d)\n", op, rc); return 5; }
       check_invariants(after);
+      pa_prefix_cache_stats pst;
+      if (pa_alloc_get_prefix_cache_stats(a, &pst) != PA_OK) return 7;
+      int64_t hashed = 0;
+      for (int b = 0; b < g_nb; ++b) {
+        int c = 0;
+        if (pa_alloc_block_hash(a, b, nullptr, &c) != PA_OK) return 7;
+        hashed += c;
+      }
+      if (hashed != pst.cached_blocks) { std::printf("hash count %lld vs map %lld\n", (long long)hashed, (long long)pst.cached_blocks); return 8; }
     }
     pa_alloc_destroy(a);
   }

@@ -208,3 +208,86 @@ def test_common_prefix_counts_shared_full_blocks():
     assert c.common_prefix([0, 9]) == 0
     with pytest.raises(_lib.PAError):
         c.common_prefix([0, 12345])
+
+
+# ---------------------------------------------------------------- prefix caching
+def test_block_hash_matches_the_oracle():
+    from oracle.block_pool import block_hash
+    rng = np.random.default_rng(7)
+    L = _lib.lib()
+    for _ in range(50):
+        parent = int(rng.integers(0, 2**63)) * 2 + int(rng.integers(0, 2))
+        toks = rng.integers(-2**31, 2**31, size=int(rng.integers(0, 20)), dtype=np.int64).astype(np.int32)
+        ptr = toks.ctypes.data_as(_lib.C.POINTER(_lib.C.c_int32)) if toks.size else None
+        assert L.pa_block_hash(parent, ptr, int(toks.size)) == block_hash(parent, toks.tolist())
+
+
+def assert_same_cache(c: BlockAllocator, o: SequenceManager):
+    assert_same(c, o)
+    for b in range(c.num_blocks):
+        assert c.block_hash(b) == o.pool.block_hash[b]
+    st = c.prefix_cache_stats()
+    assert st == {"lookup_blocks": o.lookup_blocks, "hit_blocks": o.hit_blocks, "evictions": o.pool.evictions,
+                  "cached_blocks": len(o.pool.cached_block_hash_to_block)}
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefix_cache_scripts_match_the_oracle_bit_exactly(seed):
+    rng = np.random.default_rng(100 + seed)
+    nb = int(rng.integers(12, 60))
+    bs = int(rng.choice([1, 2, 4, 16]))
+    order = rng.permutation(nb).astype(np.int32)
+    c = BlockAllocator(nb, bs, order)
+    o = SequenceManager(nb, bs, order)
+    if seed % 4 != 3:  # one script in four runs with caching off
+        c.enable_prefix_caching()
+        o.enable_prefix_caching()
+    prompts = [rng.integers(0, 3, size=int(rng.integers(1, 4 * bs + 3))).tolist() for _ in range(5)]
+    live, next_id = [], 0
+    for step in range(500):
+        kind = rng.choice(["add_cached", "add_cached", "append_tokens", "append_tokens", "append", "share",
+                           "cow", "free", "free"])
+        if kind == "add_cached" or not live:
+            p = prompts[int(rng.integers(len(prompts)))] + rng.integers(0, 3, size=int(rng.integers(0, 3))).tolist()
+            salt = int(rng.integers(0, 2))
+            rc, ro = _do(c, "add_seq_cached", next_id, p, salt), _do(o, "add_seq_cached", next_id, p, salt)
+            assert rc == ro, (step, rc, ro)
+            live.append(next_id)
+            next_id += 1
+            if rc[0] == "ok":  # the prompt's uncached tokens
+                rest = p[rc[1]:]
+                rc, ro = _do(c, "append_tokens", next_id - 1, rest), _do(o, "append_tokens", next_id - 1, rest)
+                if rc[0] == "ok" and ro[0] == "ok":
+                    assert rc[1].tolist() == ro[1]
+            pair = (rc, ro)
+        elif kind == "append_tokens":
+            s = int(rng.choice(live))
+            t = rng.integers(0, 3, size=int(rng.integers(0, 2 * bs + 2))).tolist()
+            rc, ro = _do(c, "append_tokens", s, t), _do(o, "append_tokens", s, t)
+            if rc[0] == "ok" and ro[0] == "ok":
+                assert rc[1].tolist() == ro[1]
+            pair = (rc, ro)
+        elif kind == "append":
+            s = int(rng.choice(live))
+            n = int(rng.integers(0, bs + 2))
+            pair = (_do(c, "append_slots", s, n), _do(o, "append_slots", s, n))
+        elif kind == "share":
+            src = int(rng.choice(live))
+            n = int(rng.integers(0, o.num_tokens[src] + 1))
+            _do(c, "add_seq", next_id), _do(o, "add_seq", next_id)
+            pair = (_do(c, "share", next_id, src, n), _do(o, "share", next_id, src, n))
+            live.append(next_id)
+            next_id += 1
+        elif kind == "cow":
+            s = int(rng.choice(live))
+            lb = int(rng.integers(0, len(o.tables[s]) + 1))
+            rc, ro = _do(c, "cow", s, lb), _do(o, "cow", s, lb)
+            if rc[0] == "ok" and ro[0] == "ok":
+                assert tuple(rc[1]) == tuple(ro[1])
+            pair = (rc, ro)
+        else:
+            s = int(rng.choice(live))
+            pair = (_do(c, "free_seq", s), _do(o, "free_seq", s))
+            live.remove(s)
+        assert pair[0][0] == pair[1][0], (step, kind, pair)
+        assert_same_cache(c, o)
