@@ -56,6 +56,21 @@ Automatic prefix caching ("Khám phá vLLM … phần 2", prefix caching;
   evicted in release order, the first block of a request last.
 * a cached block loses its hash only when the free queue hands it out again
   (popleft): its map entry is removed then.
+
+Swapping ("2.1 PagedAttention" §7, preemption by swapping), when a swap pool
+of CPU blocks is set up:
+
+* swap_out copies every block of a request into CPU blocks taken from the
+  head of the swap pool's free queue (one per logical block, in order, shared
+  blocks included) and then releases its GPU blocks exactly as free_seq
+  would.  The request keeps its id and token count; its table now lists its
+  CPU blocks and it can neither grow nor be shared or copied until swap_in.
+* swap_in takes one GPU block per CPU block from the head of the free queue
+  (new private blocks: sharing is not restored, cached hashes are not
+  carried over) and returns the CPU blocks to the head of the swap pool's
+  queue in reverse order.  Both return the (source, destination) pairs the
+  caller copies with swap_blocks before reusing the source blocks.
+* free_seq on a swapped-out request returns its CPU blocks.
 """
 from __future__ import annotations
 
@@ -236,9 +251,57 @@ class SequenceManager:
         self.pending = {}
         self.lookup_blocks = 0
         self.hit_blocks = 0
+        # swapping: the swap pool's free queue and the swapped-out requests
+        self.cpu_free = None
+        self.on_cpu = set()
 
     def enable_prefix_caching(self):
         self.pool.caching = True
+
+    def enable_swap(self, num_cpu_blocks):
+        if num_cpu_blocks <= 0 or self.cpu_free is not None:
+            raise AllocError("swap pool: positive size, set once")
+        self.cpu_free = FreeBlockQueue(range(num_cpu_blocks))
+
+    def num_free_cpu(self):
+        return len(self.cpu_free) if self.cpu_free is not None else 0
+
+    def _resident(self, seq):
+        self._need(seq)
+        if seq in self.on_cpu:
+            raise AllocError(f"sequence {seq} is swapped out")
+
+    def swap_out(self, seq):
+        """Move ``seq`` to the swap pool; returns its (gpu, cpu) block pairs."""
+        self._resident(seq)
+        if self.cpu_free is None:
+            raise AllocError("no swap pool")
+        table = self.tables[seq]
+        if len(table) > len(self.cpu_free):
+            self.alloc_failures += 1
+            raise NoFreeBlocks(f"need {len(table)} swap blocks, have {len(self.cpu_free)}")
+        cpu = self.cpu_free.popleft_n(len(table))
+        pairs = list(zip(table, cpu))
+        self.pool.free_blocks(list(reversed(table)))
+        self.tables[seq] = cpu
+        self.on_cpu.add(seq)
+        return pairs
+
+    def swap_in(self, seq):
+        """Bring ``seq`` back into GPU blocks; returns its (cpu, gpu) block pairs."""
+        self._need(seq)
+        if seq not in self.on_cpu:
+            raise AllocError(f"sequence {seq} is not swapped out")
+        cpu = self.tables[seq]
+        if len(cpu) > self.num_free():
+            self.alloc_failures += 1
+            raise NoFreeBlocks(f"need {len(cpu)}, have {self.num_free()}")
+        gpu = self.pool.get_new_blocks(len(cpu))
+        pairs = list(zip(cpu, gpu))
+        self.cpu_free.prepend_n(list(reversed(cpu)))
+        self.tables[seq] = gpu
+        self.on_cpu.discard(seq)
+        return pairs
 
     # -- queries -----------------------------------------------------------
     def num_free(self):
@@ -302,6 +365,7 @@ class SequenceManager:
 
     def append_slots(self, seq, n):
         """Give the next ``n`` tokens of ``seq`` their slots, growing on demand."""
+        self._resident(seq)
         slots = self._grow(seq, n)
         if n > 0:
             self.pending[seq] = None  # token ids unknown: no more hashing for seq
@@ -312,6 +376,7 @@ class SequenceManager:
         hashed and, with prefix caching on, registered unless its hash is
         already cached."""
         tokens = [int(t) for t in tokens]
+        self._resident(seq)
         slots = self._grow(seq, len(tokens))
         pend = self.pending[seq]
         if pend is None:
@@ -352,8 +417,8 @@ class SequenceManager:
 
     def share(self, dst, src, n_tokens):
         """``dst`` (empty) starts with the first ``n_tokens`` of ``src``'s KV."""
-        self._need(dst)
-        self._need(src)
+        self._resident(dst)
+        self._resident(src)
         if self.tables[dst] or self.num_tokens[dst]:
             raise AllocError("share target must be empty")
         if not 0 <= n_tokens <= self.num_tokens[src]:
@@ -374,7 +439,7 @@ class SequenceManager:
 
     def cow(self, seq, logical_block):
         """Make ``seq``'s logical block private; return (src, dst) to copy."""
-        self._need(seq)
+        self._resident(seq)
         table = self.tables[seq]
         if not 0 <= logical_block < len(table):
             raise AllocError("logical block out of range")
@@ -393,7 +458,11 @@ class SequenceManager:
     def free_seq(self, seq):
         """Release ``seq``: its blocks in reverse order, tail block first."""
         self._need(seq)
-        self.pool.free_blocks(list(reversed(self.tables[seq])))
+        if seq in self.on_cpu:
+            self.cpu_free.prepend_n(list(reversed(self.tables[seq])))
+            self.on_cpu.discard(seq)
+        else:
+            self.pool.free_blocks(list(reversed(self.tables[seq])))
         del self.tables[seq]
         del self.num_tokens[seq]
         del self.salt[seq], self.parent[seq], self.pending[seq]
@@ -414,6 +483,10 @@ class SequenceManager:
                 self.add_seq_cached(op[1], op[2], op[3] if len(op) > 3 else 0)
             elif kind == "append_tokens":  # (kind, seq, token ids)
                 slots.extend(self.append_tokens(op[1], op[2]))
+            elif kind == "swap_out":
+                self.swap_out(op[1])
+            elif kind == "swap_in":
+                self.swap_in(op[1])
             elif kind == "share":
                 self.share(op[1], op[2], op[3])
             elif kind == "cow":

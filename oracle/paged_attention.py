@@ -26,6 +26,7 @@ __all__ = [
     "slots_for",
     "reshape_and_cache",
     "copy_blocks",
+    "swap_blocks",
     "gather_context",
     "decode",
     "decode_split_partials",
@@ -93,6 +94,27 @@ def copy_blocks(k_cache, v_cache, pairs):
         k_cache[d] = k_cache[s]
         v_cache[d] = v_cache[s]
     return k_cache, v_cache
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
+    """Swap step of preemption: block ``d`` of the destination pool becomes a
+    copy of block ``s`` of the source pool, for each (s, d).
+
+    "2.1 PagedAttention" §7: a preempted request's KV blocks are copied from
+    GPU memory to CPU memory (swap out) and back when it resumes (swap in),
+    each time into whatever blocks the other pool hands out.  Destinations may
+    not repeat.  Returns new destination arrays; the source is not changed.
+    """
+    dst_k = np.array(dst_k, copy=True)
+    dst_v = np.array(dst_v, copy=True)
+    pairs = [(int(s), int(d)) for s, d in pairs]
+    dsts = [d for _, d in pairs]
+    if len(set(dsts)) != len(dsts):
+        raise ValueError("swap_blocks pairs must have distinct destinations")
+    for s, d in pairs:
+        dst_k[d] = src_k[s]
+        dst_v[d] = src_v[s]
+    return dst_k, dst_v
 
 
 def gather_context(cache, block_table_row, length: int, block_size: int) -> np.ndarray:
