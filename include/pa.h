@@ -122,6 +122,31 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
                    int block_size, int kv_heads, int head_dim, pa_dtype dtype, pa_stream stream);
 
 /* ----------------------------------------------------------------------------
+ * pa_swap_blocks - the device half of preemption by swapping.
+ *
+ * "2.1 PagedAttention" §7: when the GPU pool runs short, a request's blocks
+ * are copied to a pool in CPU memory and its GPU blocks are released; later
+ * they are copied back into fresh GPU blocks (pa_alloc_swap_out /
+ * pa_alloc_swap_in do the bookkeeping and produce the pairs).  For each pair
+ * p: block pairs[2p+1] of (dst_k, dst_v) becomes a bit-exact copy of block
+ * pairs[2p] of (src_k, src_v).  Both pools have the KV-cache layout
+ * [num_*_blocks][block_size][kv_heads][head_dim].
+ *   src_*, dst_*  device memory or PAGE-LOCKED host memory (cudaHostAlloc /
+ *          cudaHostRegister, mapped); the kernel reads and writes host memory
+ *          directly over the CPU-GPU link.  Pageable host memory is rejected
+ *          with PA_ERR_INVALID.  All four 16-byte aligned.
+ *   pairs  int32 [num_pairs][2] (src, dst), device or page-locked host
+ *          memory.  dst ids must not repeat.  A src id outside
+ *          [0, num_src_blocks) or a dst id outside [0, num_dst_blocks)
+ *          records PA_DEVERR_BLOCK_ID and the pair is skipped.
+ * The call is asynchronous on stream; host buffers must stay alive and
+ * untouched until it completes.  num_pairs == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* pairs,
+                   int num_pairs, int num_src_blocks, int num_dst_blocks, int block_size, int kv_heads,
+                   int head_dim, pa_dtype dtype, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
  * Paged decode attention (one query token per request).
  *
  * "2.1 PagedAttention" §3 and §5: the kernel reads the request's whole KV
@@ -409,6 +434,37 @@ int pa_alloc_append_tokens(pa_alloc* a, int seq_id, const int32_t* tokens, int n
 /* *is_cached_out = 1 and *hash_out = its hash if block_id is in the map, else 0. */
 int pa_alloc_block_hash(const pa_alloc* a, int block_id, uint64_t* hash_out, int* is_cached_out);
 int pa_alloc_get_prefix_cache_stats(const pa_alloc* a, pa_prefix_cache_stats* out);
+
+/* ----------------------------------------------------------------------------
+ * Preemption by swapping ("2.1 PagedAttention" §7).  Off until
+ * pa_alloc_enable_swap gives the size of the CPU swap pool (its own free
+ * queue of ids 0..num_cpu_blocks-1, handed out from the head).
+ *  - pa_alloc_swap_out: the sequence's table moves to swap blocks taken from
+ *    the swap pool's head, one per GPU block in logical order; its GPU blocks
+ *    are released exactly as pa_alloc_free_seq releases them (a block another
+ *    sequence shares stays with that sequence; a cached block keeps its
+ *    hash).  pairs_out[i] = (gpu block, swap block) for logical block i: run
+ *    pa_swap_blocks(gpu pool -> swap pool) on them BEFORE anything writes the
+ *    released GPU blocks.
+ *  - pa_alloc_swap_in: the sequence gets new GPU blocks from the free queue
+ *    (as appends do); pairs_out[i] = (swap block, gpu block); its swap blocks
+ *    return to the swap pool's head, its last block first.  Run
+ *    pa_swap_blocks(swap pool -> gpu pool) before the sequence is read.
+ *  - While swapped out a sequence can only be swapped in, freed (its swap
+ *    blocks return to the swap pool's head) or queried; append, share, CoW,
+ *    table building and common-prefix calls on it return PA_ERR_INVALID.
+ *    Its block table then lists swap-pool ids.
+ * cap is the capacity of pairs_out in pairs; *n_out (may be NULL) = the number
+ * of pairs needed, also when cap is too small (PA_ERR_INVALID).  A shortage of
+ * swap blocks (swap_out) or GPU blocks (swap_in) returns PA_ERR_NO_FREE_BLOCKS
+ * and changes nothing.
+ * ------------------------------------------------------------------------- */
+int pa_alloc_enable_swap(pa_alloc* a, int num_cpu_blocks);
+int pa_alloc_num_free_cpu(const pa_alloc* a);
+/* 1 if seq_id is swapped out, 0 if resident, PA_ERR_INVALID if unknown. */
+int pa_alloc_is_swapped(const pa_alloc* a, int seq_id);
+int pa_alloc_swap_out(pa_alloc* a, int seq_id, int32_t* pairs_out, int cap, int* n_out);
+int pa_alloc_swap_in(pa_alloc* a, int seq_id, int32_t* pairs_out, int cap, int* n_out);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,7 @@ PROTOTYPES = {
     "pa_launch_count": (C.c_uint64, []),
     "pa_reshape_and_cache": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pa_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pa_decode_split_tokens": (_I, [_I, _I, _I]),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "pa_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I, _P]),
@@ -98,6 +99,11 @@ PROTOTYPES = {
     "pa_alloc_append_tokens": (_I, [_P, _I, _I32P, _I, _I32P]),
     "pa_alloc_block_hash": (_I, [_P, _I, C.POINTER(C.c_uint64), C.POINTER(_I)]),
     "pa_alloc_get_prefix_cache_stats": (_I, [_P, C.POINTER(PrefixCacheStats)]),
+    "pa_alloc_enable_swap": (_I, [_P, _I]),
+    "pa_alloc_num_free_cpu": (_I, [_P]),
+    "pa_alloc_is_swapped": (_I, [_P, _I]),
+    "pa_alloc_swap_out": (_I, [_P, _I, _I32P, _I, C.POINTER(_I)]),
+    "pa_alloc_swap_in": (_I, [_P, _I, _I32P, _I, C.POINTER(_I)]),
 }
 
 _lock = threading.Lock()

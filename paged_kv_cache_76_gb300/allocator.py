@@ -129,6 +129,31 @@ class BlockAllocator:
         _chk(self._L.pa_alloc_get_prefix_cache_stats(self._h, C.byref(s)), "pa_alloc_get_prefix_cache_stats")
         return {name: int(getattr(s, name)) for name, _ in s._fields_}
 
+    # -- preemption by swapping ----------------------------------------------
+    def enable_swap(self, num_cpu_blocks: int):
+        _chk(self._L.pa_alloc_enable_swap(self._h, int(num_cpu_blocks)), "pa_alloc_enable_swap")
+
+    def num_free_cpu(self) -> int:
+        return _chk(self._L.pa_alloc_num_free_cpu(self._h), "pa_alloc_num_free_cpu")
+
+    def is_swapped(self, seq: int) -> bool:
+        return bool(_chk(self._L.pa_alloc_is_swapped(self._h, int(seq)), "pa_alloc_is_swapped"))
+
+    def _swap(self, fn, seq, what):
+        n = C.c_int(0)
+        cap = len(self.block_table(seq))
+        out = np.empty((max(cap, 1), 2), dtype=np.int32)
+        _chk(fn(self._h, int(seq), _i32p(out), cap, C.byref(n)), what)
+        return out[:n.value]
+
+    def swap_out(self, seq: int) -> np.ndarray:
+        """Move ``seq`` to the swap pool; int32 [n, 2] (gpu block, swap block) pairs."""
+        return self._swap(self._L.pa_alloc_swap_out, seq, "pa_alloc_swap_out")
+
+    def swap_in(self, seq: int) -> np.ndarray:
+        """Bring ``seq`` back into new GPU blocks; int32 [n, 2] (swap block, gpu block) pairs."""
+        return self._swap(self._L.pa_alloc_swap_in, seq, "pa_alloc_swap_in")
+
     def seq_len(self, seq: int) -> int:
         v = C.c_int64(0)
         _chk(self._L.pa_alloc_seq_len(self._h, int(seq), C.byref(v)), "pa_alloc_seq_len")
@@ -173,6 +198,10 @@ class BlockAllocator:
                 self.add_seq_cached(op[1], op[2], op[3] if len(op) > 3 else 0)
             elif kind == "append_tokens":
                 slots.extend(self.append_tokens(op[1], op[2]).tolist())
+            elif kind == "swap_out":
+                self.swap_out(op[1])
+            elif kind == "swap_in":
+                self.swap_in(op[1])
             else:
                 raise ValueError(f"unknown op {kind}")
         return slots, pairs

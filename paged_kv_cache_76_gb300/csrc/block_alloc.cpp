@@ -16,7 +16,11 @@
 //    64-bit FNV-1a hash of their token ids, a hash -> block map finds them
 //    again for a new request's prompt, freed hashed blocks go to the tail of
 //    the queue, and a cached block loses its hash only when the queue hands
-//    it out again ("Khám phá vLLM … phần 2", prefix caching).
+//    it out again ("Khám phá vLLM … phần 2", prefix caching);
+//  * preemption by swapping (§7): a second pool of CPU blocks with its own
+//    free queue; swap-out moves a request's blocks there (pairs for the
+//    copy) and releases its GPU blocks as a free would, swap-in takes new GPU
+//    blocks and returns the CPU ones.
 // Every entry point validates first and mutates only once success is certain.
 #include <algorithm>
 #include <cstdint>
@@ -36,6 +40,40 @@ struct Seq {
   uint64_t salt = 0, parent = 0;
   std::vector<int32_t> pending;
   bool hashable = true;
+  bool swapped = false;  // blocks are CPU (swap-pool) blocks
+};
+
+// Free queue of the swap pool: the same intrusive doubly linked list.
+struct Queue {
+  std::vector<int32_t> prev, next;
+  int32_t head = -1, tail = -1, n = 0;
+  void init(int32_t count) {
+    prev.assign(count, -1);
+    next.assign(count, -1);
+    head = tail = -1;
+    n = 0;
+    for (int32_t b = 0; b < count; ++b) {
+      prev[b] = tail;
+      if (tail < 0) head = b; else next[tail] = b;
+      tail = b;
+      ++n;
+    }
+  }
+  int32_t pop_front() {
+    const int32_t b = head;
+    head = next[b];
+    if (head < 0) tail = -1; else prev[head] = -1;
+    next[b] = -1;
+    --n;
+    return b;
+  }
+  void push_front(int32_t b) {
+    next[b] = head;
+    prev[b] = -1;
+    if (head < 0) tail = b; else prev[head] = b;
+    head = b;
+    ++n;
+  }
 };
 
 // 64-bit FNV-1a: for each byte, xor it into the state, then multiply by the prime.
@@ -74,6 +112,9 @@ struct pa_alloc {
   std::vector<uint8_t> has_hash;
   std::unordered_map<uint64_t, int32_t> cached;
   int64_t lookup_blocks = 0, hit_blocks = 0, evictions = 0;
+  // swap pool (0 blocks: none)
+  int32_t num_cpu_blocks = 0;
+  Queue cpu;
 
   void push_back(int32_t b) {
     prev[b] = tail;
@@ -194,7 +235,7 @@ int pa_alloc_add_seq(pa_alloc* a, int seq_id) {
 int pa_alloc_append_slots(pa_alloc* a, int seq_id, int n_tokens, int32_t* slots_out) {
   if (!a || n_tokens < 0) return PA_ERR_INVALID;
   Seq* s = a->find(seq_id);
-  if (!s) return PA_ERR_INVALID;
+  if (!s || s->swapped) return PA_ERR_INVALID;
   const int st = grow(a, s, n_tokens, slots_out);
   if (st == PA_OK && n_tokens > 0) {  // token ids unknown: nothing more is hashed
     s->hashable = false;
@@ -207,7 +248,7 @@ int pa_alloc_share(pa_alloc* a, int dst_seq, int src_seq, int n_tokens) {
   if (!a || dst_seq == src_seq) return PA_ERR_INVALID;
   Seq* d = a->find(dst_seq);
   Seq* s = a->find(src_seq);
-  if (!d || !s || !d->blocks.empty() || d->num_tokens != 0) return PA_ERR_INVALID;
+  if (!d || !s || d->swapped || s->swapped || !d->blocks.empty() || d->num_tokens != 0) return PA_ERR_INVALID;
   if (n_tokens < 0 || n_tokens > s->num_tokens) return PA_ERR_INVALID;
   const int64_t nblk = cdiv64(n_tokens, a->block_size);
   d->blocks.assign(s->blocks.begin(), s->blocks.begin() + nblk);
@@ -231,7 +272,7 @@ int pa_alloc_share(pa_alloc* a, int dst_seq, int src_seq, int n_tokens) {
 int pa_alloc_cow(pa_alloc* a, int seq_id, int logical_block, int32_t* src_dst_out) {
   if (!a || !src_dst_out) return PA_ERR_INVALID;
   Seq* s = a->find(seq_id);
-  if (!s || logical_block < 0 || logical_block >= (int)s->blocks.size()) return PA_ERR_INVALID;
+  if (!s || s->swapped || logical_block < 0 || logical_block >= (int)s->blocks.size()) return PA_ERR_INVALID;
   const int32_t b = s->blocks[logical_block];
   if (a->ref[b] == 1) {
     src_dst_out[0] = src_dst_out[1] = b;
@@ -255,6 +296,11 @@ int pa_alloc_free_seq(pa_alloc* a, int seq_id) {
   auto it = a->seqs.find(seq_id);
   if (it == a->seqs.end()) return PA_ERR_INVALID;
   const std::vector<int32_t>& blocks = it->second.blocks;
+  if (it->second.swapped) {  // swap-pool blocks back to that pool's head, last first
+    for (int32_t c : blocks) a->cpu.push_front(c);
+    a->seqs.erase(it);
+    return PA_OK;
+  }
   // reverse order: tail block first; zero-count blocks are prepended keeping
   // that order, i.e. pushed to the front from the last of them to the first
   // (blocks without a hash); blocks with a hash are appended at the tail in
@@ -287,7 +333,7 @@ int pa_alloc_build_tables(const pa_alloc* a, const int* seq_ids, int n, int32_t*
   if (!a || n < 0 || max_blocks_per_seq < 0 || (n > 0 && (!seq_ids || !out))) return PA_ERR_INVALID;
   for (int i = 0; i < n; ++i) {
     const Seq* s = a->find(seq_ids[i]);
-    if (!s || (int64_t)s->blocks.size() > max_blocks_per_seq || s->num_tokens > INT32_MAX)
+    if (!s || s->swapped || (int64_t)s->blocks.size() > max_blocks_per_seq || s->num_tokens > INT32_MAX)
       return PA_ERR_INVALID;
   }
   for (int i = 0; i < n; ++i) {
@@ -303,11 +349,11 @@ int pa_alloc_build_tables(const pa_alloc* a, const int* seq_ids, int n, int32_t*
 int pa_alloc_common_prefix(const pa_alloc* a, const int* seq_ids, int n, int* n_blocks_out) {
   if (!a || n <= 0 || !seq_ids || !n_blocks_out) return PA_ERR_INVALID;
   const Seq* first = a->find(seq_ids[0]);
-  if (!first) return PA_ERR_INVALID;
+  if (!first || first->swapped) return PA_ERR_INVALID;
   int64_t common = first->num_tokens / a->block_size;  // full blocks only
   for (int i = 1; i < n; ++i) {
     const Seq* s = a->find(seq_ids[i]);
-    if (!s) return PA_ERR_INVALID;
+    if (!s || s->swapped) return PA_ERR_INVALID;
     common = std::min<int64_t>(common, s->num_tokens / a->block_size);
     int64_t k = 0;
     while (k < common && s->blocks[k] == first->blocks[k]) ++k;
@@ -357,6 +403,74 @@ int pa_alloc_get_stats(const pa_alloc* a, pa_alloc_stats* out) {
   return PA_OK;
 }
 
+int pa_alloc_enable_swap(pa_alloc* a, int num_cpu_blocks) {
+  if (!a || num_cpu_blocks <= 0 || a->num_cpu_blocks > 0) return PA_ERR_INVALID;
+  a->num_cpu_blocks = num_cpu_blocks;
+  a->cpu.init(num_cpu_blocks);
+  return PA_OK;
+}
+
+int pa_alloc_num_free_cpu(const pa_alloc* a) { return a ? a->cpu.n : PA_ERR_INVALID; }
+
+int pa_alloc_is_swapped(const pa_alloc* a, int seq_id) {
+  if (!a) return PA_ERR_INVALID;
+  const Seq* s = a->find(seq_id);
+  return s ? (s->swapped ? 1 : 0) : PA_ERR_INVALID;
+}
+
+int pa_alloc_swap_out(pa_alloc* a, int seq_id, int32_t* pairs_out, int cap, int* n_out) {
+  if (!a || a->num_cpu_blocks <= 0) return PA_ERR_INVALID;
+  Seq* s = a->find(seq_id);
+  if (!s || s->swapped) return PA_ERR_INVALID;
+  const int n = (int)s->blocks.size();
+  if (n_out) *n_out = n;
+  if (n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID;
+  if (n > a->cpu.n) {
+    ++a->alloc_failures;
+    return PA_ERR_NO_FREE_BLOCKS;
+  }
+  std::vector<int32_t> cpu_blocks(n);
+  for (int i = 0; i < n; ++i) {
+    cpu_blocks[i] = a->cpu.pop_front();
+    pairs_out[2 * i] = s->blocks[i];
+    pairs_out[2 * i + 1] = cpu_blocks[i];
+  }
+  // release the GPU blocks exactly as pa_alloc_free_seq does
+  std::vector<int32_t> no_hash, with_hash;
+  for (auto rit = s->blocks.rbegin(); rit != s->blocks.rend(); ++rit) {
+    a->ref[*rit] -= 1;
+    if (a->ref[*rit] == 0) (a->has_hash[*rit] ? with_hash : no_hash).push_back(*rit);
+  }
+  for (auto rit = no_hash.rbegin(); rit != no_hash.rend(); ++rit) a->push_front(*rit);
+  for (int32_t b : with_hash) a->push_back(b);
+  s->blocks = std::move(cpu_blocks);
+  s->swapped = true;
+  return PA_OK;
+}
+
+int pa_alloc_swap_in(pa_alloc* a, int seq_id, int32_t* pairs_out, int cap, int* n_out) {
+  if (!a) return PA_ERR_INVALID;
+  Seq* s = a->find(seq_id);
+  if (!s || !s->swapped) return PA_ERR_INVALID;
+  const int n = (int)s->blocks.size();
+  if (n_out) *n_out = n;
+  if (n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID;
+  if (n > a->num_free) {
+    ++a->alloc_failures;
+    return PA_ERR_NO_FREE_BLOCKS;
+  }
+  std::vector<int32_t> gpu_blocks(n);
+  for (int i = 0; i < n; ++i) {
+    gpu_blocks[i] = a->take();
+    pairs_out[2 * i] = s->blocks[i];
+    pairs_out[2 * i + 1] = gpu_blocks[i];
+  }
+  for (int32_t c : s->blocks) a->cpu.push_front(c);  // last block ends at the head
+  s->blocks = std::move(gpu_blocks);
+  s->swapped = false;
+  return PA_OK;
+}
+
 uint64_t pa_block_hash(uint64_t parent, const int32_t* tokens, int n) {
   return hash_block(parent, tokens, (tokens && n > 0) ? n : 0);
 }
@@ -400,7 +514,7 @@ int pa_alloc_add_seq_cached(pa_alloc* a, int seq_id, const int32_t* tokens, int 
 int pa_alloc_append_tokens(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, int32_t* slots_out) {
   if (!a || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID;
   Seq* s = a->find(seq_id);
-  if (!s) return PA_ERR_INVALID;
+  if (!s || s->swapped) return PA_ERR_INVALID;
   const int64_t first = s->num_tokens;
   const int st = grow(a, s, n_tokens, slots_out);
   if (st != PA_OK || !s->hashable) return st;

@@ -73,7 +73,65 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Swap step of preemption: block dst of one pool becomes a copy of block src
+// of another; either pool may be page-locked host memory read or written
+// directly by the kernel (over NVLink-C2C on Grace-Blackwell).  Four 16-byte
+// vectors per thread are loaded before any is stored, to keep enough
+// requests in flight across the host link.
+__global__ void __launch_bounds__(256)
+    swap_blocks_kernel(const uint4* __restrict__ sk, const uint4* __restrict__ sv, uint4* __restrict__ dk,
+                       uint4* __restrict__ dv, const int32_t* __restrict__ pairs, int num_pairs, int64_t block_vecs,
+                       int num_src, int num_dst, int* err) {
+  constexpr int U = 4;
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
+    const int src = pairs[2 * pi], dst = pairs[2 * pi + 1];
+    if (src < 0 || src >= num_src || dst < 0 || dst >= num_dst) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+      continue;
+    }
+    const uint4* ks = sk + (int64_t)src * block_vecs;
+    const uint4* vs = sv + (int64_t)src * block_vecs;
+    uint4* kd = dk + (int64_t)dst * block_vecs;
+    uint4* vd = dv + (int64_t)dst * block_vecs;
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x * U + threadIdx.x; i0 < block_vecs;
+         i0 += (int64_t)gridDim.x * blockDim.x * U) {
+      uint4 a[U], b[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + (int64_t)u * blockDim.x;
+        if (i < block_vecs) {
+          a[u] = ks[i];
+          b[u] = vs[i];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = i0 + (int64_t)u * blockDim.x;
+        if (i < block_vecs) {
+          kd[i] = a[u];
+          vd[i] = b[u];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* pairs,
+                               int num_pairs, int num_src, int num_dst, int64_t block_bytes, int* err,
+                               cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int64_t block_vecs = block_bytes / 16;
+  int64_t bx = (block_vecs + 1023) / 1024;
+  if (bx > 8) bx = 8;
+  const int by = num_pairs < 65535 ? num_pairs : 65535;
+  return launch_pdl(swap_blocks_kernel, dim3((unsigned)bx, by), dim3(256), 0, stream,
+                    static_cast<const uint4*>(src_k), static_cast<const uint4*>(src_v), static_cast<uint4*>(dst_k),
+                    static_cast<uint4*>(dst_v), pairs, num_pairs, block_vecs, num_src, num_dst, err);
+}
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
                                      void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,

@@ -142,6 +142,26 @@ int check_kv_shape(int num_blocks, int block_size, int kv_heads, int head_dim, p
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
+// The address a kernel dereferences for p: device or managed memory as is,
+// page-locked host memory through its mapped device address; nullptr for
+// pageable host memory (or anything CUDA does not know).
+const void* device_view(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return p;
+    case cudaMemoryTypeHost:
+      return at.devicePointer;
+    default:
+      return nullptr;
+  }
+}
+
 struct DecodeSetup {
   int split, max_splits;
   DecodeWorkspace ws;
@@ -253,6 +273,30 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
   int* err = device_error_ptr();
   if (!err) return PA_ERR_CUDA;
   return cuda_status(launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks,
+                                        (int64_t)block_size * kv_heads * head_dim * 2, err,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* pairs,
+                   int num_pairs, int num_src_blocks, int num_dst_blocks, int block_size, int kv_heads, int head_dim,
+                   pa_dtype dtype, pa_stream stream) {
+  int st = check_kv_shape(num_src_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  st = check_kv_shape(num_dst_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return PA_ERR_INVALID;
+  if (num_pairs == 0) return PA_OK;
+  if (!src_k || !src_v || !dst_k || !dst_v || !pairs) return PA_ERR_INVALID;
+  if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v)) return PA_ERR_INVALID;
+  const void* sk = device_view(src_k);
+  const void* sv = device_view(src_v);
+  void* dk = const_cast<void*>(device_view(dst_k));
+  void* dv = const_cast<void*>(device_view(dst_v));
+  const int32_t* pr = static_cast<const int32_t*>(device_view(pairs));
+  if (!sk || !sv || !dk || !dv || !pr) return PA_ERR_INVALID;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  return cuda_status(launch_swap_blocks(sk, sv, dk, dv, pr, num_pairs, num_src_blocks, num_dst_blocks,
                                         (int64_t)block_size * kv_heads * head_dim * 2, err,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -117,6 +117,11 @@ cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, con
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
                                      void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,
                                      cudaStream_t stream);
+// pointers as the kernel dereferences them (host pools through their mapped
+// device addresses); block_bytes = one block of K (or V)
+cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* pairs,
+                               int num_pairs, int num_src, int num_dst, int64_t block_bytes, int* err,
+                               cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, int64_t block_bytes, int* err, cudaStream_t stream);
 

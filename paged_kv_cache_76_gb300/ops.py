@@ -17,6 +17,7 @@ from ._lib import PA_BF16, PA_FP16, check
 __all__ = [
     "reshape_and_cache",
     "copy_blocks",
+    "swap_blocks",
     "decode",
     "decode_partial",
     "lse_merge",
@@ -85,6 +86,31 @@ def copy_blocks(k_cache, v_cache, pairs, stream=None):
     check(_lib.lib().pa_copy_blocks(
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(pairs, "pairs"), int(pairs.shape[0]),
         nb, bs, hkv, d, dtype_code(k_cache.dtype), _stream(stream)), "pa_copy_blocks")
+
+
+def _dev_or_pinned(t: torch.Tensor, name: str):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    return t.data_ptr()
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs, stream=None):
+    """Copy blocks between two pools of the cache layout, either of which may
+    live in pinned host memory (``pin_memory=True``); ``pairs``: int32 [n, 2]
+    (src, dst), on the device or pinned.  Asynchronous on ``stream``."""
+    if src_v.shape != src_k.shape or dst_v.shape != dst_k.shape or src_k.shape[1:] != dst_k.shape[1:] \
+            or src_k.dtype != dst_k.dtype or src_v.dtype != src_k.dtype or dst_v.dtype != dst_k.dtype:
+        raise ValueError("the pools must agree in block shape and dtype")
+    if pairs.dtype != torch.int32:
+        raise TypeError("pairs must be int32")
+    ns, bs, hkv, d = _cache_dims(src_k)
+    nd = dst_k.shape[0]
+    check(_lib.lib().pa_swap_blocks(
+        _dev_or_pinned(src_k, "src_k"), _dev_or_pinned(src_v, "src_v"), _dev_or_pinned(dst_k, "dst_k"),
+        _dev_or_pinned(dst_v, "dst_v"), _dev_or_pinned(pairs, "pairs"), int(pairs.shape[0]), ns, nd, bs, hkv, d,
+        dtype_code(src_k.dtype), _stream(stream)), "pa_swap_blocks")
 
 
 def decode_split_tokens(max_blocks_per_seq: int, block_size: int, split_tokens: int = 0) -> int:

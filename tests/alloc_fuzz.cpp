@@ -6,7 +6,9 @@
 //   * each table has ceil(len / block_size) entries;
 //   * a failed call changes nothing (checked via a snapshot);
 //   * with prefix caching on: the number of blocks carrying a hash equals the
-//     map size the stats report.
+//     map size the stats report;
+//   * with swapping on: swapped-out tables hold swap-pool ids, each once, and
+//     those plus the swap pool's free count cover the swap pool exactly.
 #include <algorithm>
 #include <cstdint>
 #include <cstdio>
@@ -21,12 +23,15 @@ struct Snapshot {
   std::vector<int32_t> free_list, refs;
   std::map<int, std::vector<int32_t>> tables;
   std::map<int, int64_t> lens;
+  std::map<int, int> swapped;
+  int free_cpu = 0;
   bool operator==(const Snapshot& o) const {
-    return free_list == o.free_list && refs == o.refs && tables == o.tables && lens == o.lens;
+    return free_list == o.free_list && refs == o.refs && tables == o.tables && lens == o.lens &&
+           swapped == o.swapped && free_cpu == o.free_cpu;
   }
 };
 
-static int g_nb, g_bs;
+static int g_nb, g_bs, g_ncpu;
 
 static Snapshot snap(pa_alloc* a, const std::vector<int>& live) {
   Snapshot s;
@@ -44,16 +49,27 @@ static Snapshot snap(pa_alloc* a, const std::vector<int>& live) {
     int64_t len = 0;
     pa_alloc_seq_len(a, id, &len);
     s.lens[id] = len;
+    s.swapped[id] = pa_alloc_is_swapped(a, id);
   }
+  s.free_cpu = pa_alloc_num_free_cpu(a);
   return s;
 }
 
 static void check_invariants(const Snapshot& s) {
-  std::vector<int> count(g_nb, 0), in_free(g_nb, 0);
+  std::vector<int> count(g_nb, 0), in_free(g_nb, 0), cpu_count(g_ncpu, 0);
+  int on_cpu = 0;
   for (auto& kv : s.tables) {
     if ((int64_t)kv.second.size() != (s.lens.at(kv.first) + g_bs - 1) / g_bs) { std::printf("table size\n"); std::exit(3); }
+    if (s.swapped.at(kv.first)) {
+      for (int32_t c : kv.second) {
+        if (c < 0 || c >= g_ncpu || cpu_count[c]++) { std::printf("swap id %d\n", c); std::exit(3); }
+        ++on_cpu;
+      }
+      continue;
+    }
     for (int32_t b : kv.second) count[b]++;
   }
+  if (on_cpu + s.free_cpu != g_ncpu) { std::printf("swap pool %d + %d != %d\n", on_cpu, s.free_cpu, g_ncpu); std::exit(3); }
   for (int32_t b : s.free_list) {
     if (in_free[b]++) { std::printf("duplicate in free list\n"); std::exit(3); }
   }
@@ -76,6 +92,8 @@ int main(int argc, char** argv) {
     pa_alloc* a = nullptr;
     if (pa_alloc_create(g_nb, g_bs, order.data(), &a) != PA_OK) return 1;
     if (round % 2 == 0 && pa_alloc_enable_prefix_caching(a) != PA_OK) return 1;
+    g_ncpu = round % 4 < 2 ? 2 + (int)(rng() % 40) : 0;
+    if (g_ncpu && pa_alloc_enable_swap(a, g_ncpu) != PA_OK) return 1;
     std::vector<std::vector<int32_t>> prompts(4);
     for (auto& p : prompts) {
       p.resize(1 + rng() % (4 * g_bs + 3));
@@ -86,7 +104,7 @@ int main(int argc, char** argv) {
     std::vector<int32_t> slots(4096);
     for (int i = 0; i < steps / 8; ++i) {
       Snapshot before = snap(a, live);
-      int op = rng() % 9, rc = PA_OK;
+      int op = rng() % 11, rc = PA_OK;
       int id = live.empty() ? -1 : live[rng() % live.size()];
       if (op == 0 || live.empty()) {
         rc = pa_alloc_add_seq(a, next);
@@ -123,6 +141,16 @@ int main(int argc, char** argv) {
         std::vector<int32_t> t(rng() % (2 * g_bs + 2));
         for (auto& x : t) x = (int32_t)(rng() % 3);
         rc = pa_alloc_append_tokens(a, id, t.data(), (int)t.size(), slots.data());
+      } else if (op == 9 || op == 10) {
+        std::vector<int32_t> pairs(2 * 4096);
+        int n = -1;
+        rc = (op == 9 ? pa_alloc_swap_out : pa_alloc_swap_in)(a, id, pairs.data(), 4096, &n);
+        if (rc == PA_OK) {
+          const auto& t = before.tables.at(id);
+          if (n != (int)t.size()) { std::printf("swap pair count\n"); return 9; }
+          for (int k = 0; k < n; ++k)
+            if (pairs[2 * k] != t[k]) { std::printf("swap pair source\n"); return 9; }
+        }
       } else {
         rc = pa_alloc_free_seq(a, 1 << 20);  // unknown: must fail without effect
         if (rc == PA_OK) return 4;

@@ -291,3 +291,99 @@ def test_prefix_cache_scripts_match_the_oracle_bit_exactly(seed):
             live.remove(s)
         assert pair[0][0] == pair[1][0], (step, kind, pair)
         assert_same_cache(c, o)
+
+
+# ---------------------------------------------------------------- swapping
+def assert_same_swap(c: BlockAllocator, o: SequenceManager):
+    assert_same(c, o)
+    assert c.num_free_cpu() == o.num_free_cpu()
+    for s in o.tables:
+        assert c.is_swapped(s) == (s in o.on_cpu)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_swap_scripts_match_the_oracle_bit_exactly(seed):
+    rng = np.random.default_rng(300 + seed)
+    nb = int(rng.integers(8, 48))
+    ncpu = int(rng.integers(2, 40))
+    bs = int(rng.choice([1, 2, 4, 16]))
+    order = rng.permutation(nb).astype(np.int32)
+    c = BlockAllocator(nb, bs, order)
+    o = SequenceManager(nb, bs, order)
+    caching = seed % 2 == 0
+    for m in (c, o):
+        if caching:
+            m.enable_prefix_caching()
+        m.enable_swap(ncpu)
+    prompts = [rng.integers(0, 3, size=int(rng.integers(1, 3 * bs + 3))).tolist() for _ in range(4)]
+    live, next_id = [], 0
+    for step in range(500):
+        kind = rng.choice(["add", "append", "append", "share", "cow", "free", "swap_out", "swap_out",
+                           "swap_in", "swap_in"])
+        if kind == "add" or not live:
+            p = prompts[int(rng.integers(len(prompts)))] + rng.integers(0, 3, size=int(rng.integers(0, 3))).tolist()
+            rc, ro = _do(c, "add_seq_cached", next_id, p), _do(o, "add_seq_cached", next_id, p)
+            assert rc == ro
+            live.append(next_id)
+            next_id += 1
+            if rc[0] == "ok":
+                rest = p[rc[1]:]
+                rc, ro = _do(c, "append_tokens", next_id - 1, rest), _do(o, "append_tokens", next_id - 1, rest)
+                if rc[0] == "ok" and ro[0] == "ok":
+                    assert rc[1].tolist() == ro[1]
+            pair = (rc, ro)
+        elif kind == "append":
+            s = int(rng.choice(live))
+            t = rng.integers(0, 3, size=int(rng.integers(0, 2 * bs + 2))).tolist()
+            rc, ro = _do(c, "append_tokens", s, t), _do(o, "append_tokens", s, t)
+            if rc[0] == "ok" and ro[0] == "ok":
+                assert rc[1].tolist() == ro[1]
+            pair = (rc, ro)
+        elif kind == "share":
+            src = int(rng.choice(live))
+            n = int(rng.integers(0, o.num_tokens[src] + 1))
+            _do(c, "add_seq", next_id), _do(o, "add_seq", next_id)
+            pair = (_do(c, "share", next_id, src, n), _do(o, "share", next_id, src, n))
+            live.append(next_id)
+            next_id += 1
+        elif kind == "cow":
+            s = int(rng.choice(live))
+            lb = int(rng.integers(0, len(o.tables[s]) + 1))
+            rc, ro = _do(c, "cow", s, lb), _do(o, "cow", s, lb)
+            if rc[0] == "ok" and ro[0] == "ok":
+                assert tuple(rc[1]) == tuple(ro[1])
+            pair = (rc, ro)
+        elif kind in ("swap_out", "swap_in"):
+            s = int(rng.choice(live))
+            rc, ro = _do(c, kind, s), _do(o, kind, s)
+            if rc[0] == "ok" and ro[0] == "ok":
+                assert rc[1].tolist() == [list(p) for p in ro[1]]
+            pair = (rc, ro)
+        else:
+            s = int(rng.choice(live))
+            pair = (_do(c, "free_seq", s), _do(o, "free_seq", s))
+            live.remove(s)
+        assert pair[0][0] == pair[1][0], (step, kind, pair)
+        assert_same_swap(c, o)
+        if caching:
+            for b in range(nb):
+                assert c.block_hash(b) == o.pool.block_hash[b]
+
+
+def test_swap_needs_a_pool_and_a_large_enough_pairs_buffer():
+    c = BlockAllocator(8, 4)
+    c.add_seq(0)
+    c.append_slots(0, 9)
+    with pytest.raises(_lib.PAError):
+        c.swap_out(0)                                  # no swap pool yet
+    c.enable_swap(4)
+    with pytest.raises(_lib.PAError):
+        c.enable_swap(4)                               # set once
+    L = _lib.lib()
+    n = _lib.C.c_int(0)
+    out = np.empty((2, 2), dtype=np.int32)
+    st = L.pa_alloc_swap_out(c._h, 0, out.ctypes.data_as(_lib.C.POINTER(_lib.C.c_int32)), 2, _lib.C.byref(n))
+    assert st == _lib.PA_ERR_INVALID and n.value == 3   # three pairs needed, nothing changed
+    assert not c.is_swapped(0) and c.num_free() == 5 and c.num_free_cpu() == 4
+    pairs = c.swap_out(0)
+    assert pairs.shape == (3, 2) and c.is_swapped(0) and c.num_free() == 8 and c.num_free_cpu() == 1
