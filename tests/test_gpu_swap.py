@@ -81,7 +81,8 @@ def test_out_of_range_ids_are_recorded_and_skipped():
     from paged_kv_cache_76_gb300 import _lib
     a = torch.ones(6, 4, 1, 64, device="cuda", dtype=torch.float16)
     h = torch.zeros(3, 4, 1, 64, dtype=torch.float16).pin_memory()
-    ops().swap_blocks(a, a, h, h.clone(), torch.tensor([[0, 3], [6, 0], [1, 1]], dtype=torch.int32, device="cuda"))
+    pairs = torch.tensor([[0, 3], [6, 0], [1, 1]], dtype=torch.int32, device="cuda")
+    ops().swap_blocks(a, a, h, h.clone().pin_memory(), pairs)
     torch.cuda.synchronize()
     assert ops().get_device_error() == _lib.PA_DEVERR_BLOCK_ID
     assert torch.count_nonzero(h[0]) == 0 and torch.all(h[1] == 1)
