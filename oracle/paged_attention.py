@@ -33,6 +33,7 @@ __all__ = [
     "lse_merge",
     "decode_split",
     "chunked_prefill",
+    "verify_decode",
 ]
 
 
@@ -264,4 +265,36 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
             for h in range(Hq):
                 g = h // group
                 out[a + i, h] = _softmax_attend(q[a + i, h], K[:visible, g, :], V[:visible, g, :], scale)
+    return out
+
+
+def verify_decode(q, k_cache, v_cache, block_tables, context_lens, scale):
+    """Verify step of speculative decoding over the paged cache.
+
+    "Khám phá vLLM … phần 2", speculative decoding: the large model runs once
+    over the context plus the k draft tokens and yields a distribution for
+    each of the k+1 positions.  Here ``q`` is [B, k+1, q_heads, D]: the
+    queries of the last k+1 positions of each request, whose K/V are already
+    in the cache, so ``context_lens[r]`` = L counts them.  Query ``i`` sits at
+    position L-(k+1)+i and attends keys 0 .. L-(k+1)+i (causal), i.e. it is
+    plain decode with context L-k+i.  A query that sees no key (L < k+1-i)
+    gives a zero row.  Float64 output [B, k+1, q_heads, D].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Q, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    bs = k_cache.shape[1]
+    group = Hq // Hkv
+    out = np.zeros((B, Q, Hq, D), dtype=np.float64)
+    for r in range(B):
+        L = int(context_lens[r])
+        for i in range(Q):
+            visible = L - (Q - 1 - i)
+            if visible <= 0:
+                continue
+            K = gather_context(k_cache, block_tables[r], visible, bs)
+            V = gather_context(v_cache, block_tables[r], visible, bs)
+            for h in range(Hq):
+                g = h // group
+                out[r, i, h] = _softmax_attend(q[r, i, h], K[:, g, :], V[:, g, :], scale)
     return out

@@ -326,6 +326,49 @@ def test_prefill_chunk_of_one_is_decode_and_requests_are_independent():
     np.testing.assert_allclose(got[1], dec1b[0], rtol=1e-13, atol=1e-13)
 
 
+# ---------------------------------------------------------------- speculative verify
+@pytest.mark.parametrize("Q,Hq,Hkv,L", [(4, 8, 2, 37), (1, 4, 4, 9), (8, 6, 3, 8), (3, 4, 1, 100)])
+def test_verify_decode_is_the_last_rows_of_library_causal_attention(Q, Hq, Hkv, L):
+    """The k+1 queries of a request are the last k+1 rows of causal attention
+    over the whole context (torch's SDPA on contiguous K/V, GQA by torch)."""
+    rng = np.random.default_rng(40 + Q)
+    D, bs = 16, 4
+    table, K, V, kc, vc = _prefill_case(rng, Hq, Hkv, D, bs, L, 40)
+    qfull = _rand(rng, L, Hq, D)
+    full = _sdpa(qfull.transpose(1, 0, 2), K.transpose(1, 0, 2), V.transpose(1, 0, 2), 0.35, causal=True)
+    q = qfull[L - Q:][None]                                   # [1, Q, Hq, D]
+    got = pa.verify_decode(q, kc, vc, np.array([table]), [L], 0.35)
+    np.testing.assert_allclose(got[0], full.transpose(1, 0, 2)[L - Q:], rtol=1e-12, atol=1e-12)
+
+
+def test_verify_decode_batches_requests_and_its_last_query_is_decode():
+    rng = np.random.default_rng(44)
+    Hq, Hkv, D, bs, nb, Q = 4, 2, 16, 4, 40, 3
+    kc = _rand(rng, nb, bs, Hkv, D)
+    vc = _rand(rng, nb, bs, Hkv, D)
+    perm = rng.permutation(nb)
+    tables = np.array([perm[:8], perm[8:16]])
+    lens = [29, 13]
+    q = _rand(rng, 2, Q, Hq, D)
+    got = pa.verify_decode(q, kc, vc, tables, lens, 0.3)
+    for r in range(2):
+        for i in range(Q):
+            dec = pa.decode(q[r, i][None], kc, vc, tables[r:r + 1], [lens[r] - (Q - 1 - i)], 0.3)
+            np.testing.assert_allclose(got[r, i], dec[0], rtol=1e-13, atol=1e-13)
+
+
+def test_verify_decode_queries_before_the_first_key_give_zero_rows():
+    rng = np.random.default_rng(45)
+    Hq, Hkv, D, bs, Q = 2, 1, 8, 4, 5
+    kc = _rand(rng, 6, bs, Hkv, D)
+    vc = _rand(rng, 6, bs, Hkv, D)
+    q = _rand(rng, 1, Q, Hq, D)
+    got = pa.verify_decode(q, kc, vc, np.array([[3, 1]]), [3], 0.5)  # queries 0, 1 see nothing
+    assert not got[0, :2].any()
+    # query 2 sees exactly one key: its output is that key's value row, for every head
+    np.testing.assert_allclose(got[0, 2], np.repeat(vc[3, 0, 0][None], Hq, 0), atol=1e-15)
+
+
 # ---------------------------------------------------------------- sizing
 def test_kv_size_closed_form_matches_the_printed_numbers():
     g = json.load(open(os.path.join(GOLDEN, "kv_sizing.json")))
