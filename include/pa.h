@@ -205,6 +205,32 @@ int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* c
                  int split_tokens, void* out, pa_dtype dtype, pa_stream stream);
 
 /* ----------------------------------------------------------------------------
+ * pa_verify_decode - the attention of the verify step of speculative decoding.
+ *
+ * "Khám phá vLLM … phần 2", speculative decoding: a proposer drafts k tokens
+ * and the large model checks them in ONE forward pass over the context plus
+ * the drafts, which yields k+1 distributions.  Its attention is decode with
+ * q_len = k+1 queries per request: the drafts' K/V are written first (with
+ * pa_reshape_and_cache, into slots the allocator appended), so
+ * context_lens[r] = L counts them, and query i (0 <= i < q_len) of request r
+ * attends tokens [0, L - (q_len-1-i)) - causal inside the draft.  A query
+ * that sees no token gives a zero row.  All q_len*group query rows of a KV
+ * head share every K/V tile read, so the pass costs the KV bytes of one
+ * decode step.
+ *   q, out        [num_seqs][q_len][q_heads][head_dim]
+ *   q_len         >= 1, with (q_heads / kv_heads) * q_len <= 32
+ *   workspace     at least pa_verify_workspace_size(...) bytes
+ * Everything else as pa_decode (which is the q_len = 1 case).
+ * ------------------------------------------------------------------------- */
+size_t pa_verify_workspace_size(int num_seqs, int q_len, int q_heads, int head_dim, int max_blocks_per_seq,
+                                int block_size, int split_tokens);
+
+int pa_verify_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_len, int q_heads,
+                     int kv_heads, int head_dim, int block_size, int num_blocks, float scale, int split_tokens,
+                     void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
  * pa_decode_shared_prefix - decode for a batch whose requests all start with
  * the same physical blocks (a shared prompt prefix).
  *

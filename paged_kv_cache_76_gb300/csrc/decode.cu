@@ -24,6 +24,12 @@
 // in shared memory, so stale data in a partially filled block (NaN included)
 // never reaches the output.  All reduction orders depend only on logical
 // positions, so relabelling physical blocks gives bitwise-identical results.
+//
+// Speculative verify (q_len = k+1 queries per request): the n-tile columns are
+// the group's heads of each query, column n = i*group + head, up to 32
+// columns (NT = 4).  Column n stops at token ctx - (q_len-1-i) (causal within
+// the draft); a column with no visible token in a partition keeps m = -inf,
+// l = 0, o = 0, which the merge weighs by zero.
 #include <cuda_pipeline.h>
 #include <float.h>
 
@@ -96,6 +102,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int nsplit = (ctx - p.tok_begin + p.split_tokens - 1) / p.split_tokens;
   const bool active = c < (nsplit > 0 ? nsplit : (p.always_partial ? 0 : 1));
   const int G = p.group;
+  const int NC = G * p.q_len;  // columns: (query i, head) pairs, i-major
   const int qh0 = h * G;
   const int tok0 = p.tok_begin + c * p.split_tokens;
   const int tok1 = min(tok0 + p.split_tokens, ctx);
@@ -120,18 +127,20 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
       tab[i] = b;
     }
-    // Q^T as the B operand of S^T = K Q^T: lane holds head (lane/4) of each
-    // 8-head n-tile, elements d = 16ks + 2(lane%4) + {0,1} and +8.
-    const T* qb = reinterpret_cast<const T*>(p.q) + ((size_t)r * p.q_heads + qh0) * D;
+    // Q^T as the B operand of S^T = K Q^T: lane holds column (lane/4) of each
+    // 8-column n-tile, elements d = 16ks + 2(lane%4) + {0,1} and +8.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int hd = nt * 8 + (lane >> 2);
+      const int n = nt * 8 + (lane >> 2);
+      const int qi = n < NC ? n / G : 0;
+      const T* qb = reinterpret_cast<const T*>(p.q) +
+                    ((size_t)(r * p.q_len + qi) * p.q_heads + qh0 + (n - qi * G)) * D;
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
         const int d = ks * 16 + 2 * (lane & 3);
-        if (hd < G) {
-          qf[nt][ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + hd * D + d));
-          qf[nt][ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + hd * D + d + 8));
+        if (n < NC) {
+          qf[nt][ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qb + d));
+          qf[nt][ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qb + d + 8));
         } else {
           qf[nt][ks][0] = 0u;
           qf[nt][ks][1] = 0u;
@@ -151,9 +160,13 @@ __global__ void __launch_bounds__(WARPS * 32)
   if (!active) return;
 
   T* out = reinterpret_cast<T*>(p.out);
+  // row of column n in q / out / the partials
+  auto row_of = [&](int n) {
+    const int qi = n / G;
+    return (size_t)(r * p.q_len + qi) * p.q_heads + qh0 + (n - qi * G);
+  };
   if (ctx == 0) {
-    T* o = out + ((size_t)r * p.q_heads + qh0) * D;
-    for (int i = lane; i < G * D; i += 32) o[i] = Elem<T>::from(0.f);
+    for (int i = lane; i < NC * D; i += 32) out[row_of(i / D) * D + i % D] = Elem<T>::from(0.f);
     return;
   }
   __syncwarp();
@@ -199,6 +212,17 @@ __global__ void __launch_bounds__(WARPS * 32)
   const float sl2 = p.scale_log2;
   const int mi = lane >> 3, rr = lane & 7;
   const int r0 = lane >> 2;
+  // last visible token + 1 of this lane's two columns per n-tile (tok1 for
+  // decode, where every column sees the whole partition)
+  int lim[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = nt * 8 + 2 * (lane & 3) + e;
+      const int qi = n < NC ? n / G : p.q_len - 1;
+      lim[nt][e] = min(tok1, ctx - (p.q_len - 1 - qi));
+    }
   bool failed = false;
   int j = 0;
   for (; j < ntiles; ++j) {
@@ -237,10 +261,11 @@ __global__ void __launch_bounds__(WARPS * 32)
     uint32_t pb0[NT], pb1[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float s0 = r0 < nvalid ? sacc[nt][0] * sl2 : -INFINITY;
-      const float s1 = r0 < nvalid ? sacc[nt][1] * sl2 : -INFINITY;
-      const float s2 = r0 + 8 < nvalid ? sacc[nt][2] * sl2 : -INFINITY;
-      const float s3 = r0 + 8 < nvalid ? sacc[nt][3] * sl2 : -INFINITY;
+      const int t0 = ts + r0;
+      const float s0 = t0 < lim[nt][0] ? sacc[nt][0] * sl2 : -INFINITY;
+      const float s1 = t0 < lim[nt][1] ? sacc[nt][1] * sl2 : -INFINITY;
+      const float s2 = t0 + 8 < lim[nt][0] ? sacc[nt][2] * sl2 : -INFINITY;
+      const float s3 = t0 + 8 < lim[nt][1] ? sacc[nt][3] * sl2 : -INFINITY;
       float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -248,11 +273,14 @@ __global__ void __launch_bounds__(WARPS * 32)
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
       const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-      const float al0 = exp2f(m[nt][0] - mn0), al1 = exp2f(m[nt][1] - mn1);
+      // a column that has seen no token yet keeps m = -inf: exponents then
+      // use 0 as reference, so every p and the rescale are exactly 0
+      const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m[nt][0] - mb0), al1 = exp2f(m[nt][1] - mb1);
       m[nt][0] = mn0;
       m[nt][1] = mn1;
-      const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
-      const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+      const float p0 = exp2f(s0 - mb0), p1 = exp2f(s1 - mb1);
+      const float p2 = exp2f(s2 - mb0), p3 = exp2f(s3 - mb1);
       // P is rounded to the input type for the P.V MMA; the denominator sums
       // the same rounded values, so the output is an exact convex combination
       const uint32_t pk01 = Elem<T>::pack(p0, p1), pk23 = Elem<T>::pack(p2, p3);
@@ -304,10 +332,10 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int hd = nt * 8 + 2 * (lane & 3) + e;
-        if (hd < G) {
+        const int n = nt * 8 + 2 * (lane & 3) + e;
+        if (n < NC) {
           const float inv = lp[nt][e] > 0.f ? 1.f / lp[nt][e] : 0.f;
-          T* o = out + ((size_t)r * p.q_heads + qh0 + hd) * D;
+          T* o = out + row_of(n) * D;
 #pragma unroll
           for (int mt = 0; mt < KSTEPS; ++mt) {
             o[mt * 16 + r0] = Elem<T>::from(acc[nt][mt][e] * inv);
@@ -320,9 +348,9 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int hd = nt * 8 + 2 * (lane & 3) + e;
-        if (hd < G) {
-          const size_t row = (size_t)r * p.q_heads + qh0 + hd;
+        const int n = nt * 8 + 2 * (lane & 3) + e;
+        if (n < NC) {
+          const size_t row = row_of(n);
           const int slot = p.slot_base + c;
           float* po = p.part_o + (row * p.max_splits + slot) * D;
 #pragma unroll
@@ -355,8 +383,8 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
   griddep_launch_dependents();
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (row >= p.num_seqs * p.q_heads) return;
-  const int r = row / p.q_heads;
+  if (row >= p.num_seqs * p.q_len * p.q_heads) return;
+  const int r = row / (p.q_heads * p.q_len);
   int ctx = __ldg(p.lens + r);
   ctx = ctx < p.tok_begin ? p.tok_begin : (ctx > p.cap ? p.cap : ctx);
   const int nsplit = p.extra_slots + (ctx - p.tok_begin + p.split_tokens - 1) / p.split_tokens;
@@ -379,7 +407,7 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
   float den = 0.f;
 #pragma unroll 4
   for (int c = warp; c < nsplit; c += NW) {
-    const float w = exp2f(pm[c] - M);
+    const float w = pm[c] == -INFINITY ? 0.f : exp2f(pm[c] - M);  // a partition the row sees nothing of
     den += w * pl[c];
     if constexpr (V == 4) {
       const float4 x = *reinterpret_cast<const float4*>(po + (size_t)c * D);
@@ -416,8 +444,8 @@ __global__ void __launch_bounds__(256) lse_merge_warp_kernel(const MergeParams p
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row >= p.num_seqs * p.q_heads) return;
-  const int r = row / p.q_heads;
+  if (row >= p.num_seqs * p.q_len * p.q_heads) return;
+  const int r = row / (p.q_heads * p.q_len);
   int ctx = __ldg(p.lens + r);
   ctx = ctx < p.tok_begin ? p.tok_begin : (ctx > p.cap ? p.cap : ctx);
   const int nsplit = p.extra_slots + (ctx - p.tok_begin + p.split_tokens - 1) / p.split_tokens;
@@ -443,7 +471,7 @@ __global__ void __launch_bounds__(256) lse_merge_warp_kernel(const MergeParams p
   float M = mc;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float w = lane < nsplit ? exp2f(mc - M) : 0.f;
+  const float w = lane < nsplit && mc != -INFINITY ? exp2f(mc - M) : 0.f;
   float den = w * lc;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -505,8 +533,11 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
 template <int D, int BSUB, typename T>
 cudaError_t launch_decode_nt(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                              cudaStream_t stream) {
-  if (p.group <= 8) return launch_decode_t<D, BSUB, 1, T>(kmap, vmap, p, stream);
-  return launch_decode_t<D, BSUB, 2, T>(kmap, vmap, p, stream);
+  const int cols = p.group * p.q_len;
+  if (cols <= 8) return launch_decode_t<D, BSUB, 1, T>(kmap, vmap, p, stream);
+  if (cols <= 16) return launch_decode_t<D, BSUB, 2, T>(kmap, vmap, p, stream);
+  if (cols <= 32) return launch_decode_t<D, BSUB, 4, T>(kmap, vmap, p, stream);
+  return cudaErrorInvalidValue;
 }
 
 template <int D, typename T>
@@ -537,7 +568,7 @@ cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vm
 
 cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream) {
   if (p.max_splits <= 32) {  // one warp per row
-    const dim3 grid((p.num_seqs * p.q_heads + 7) / 8), block(256);
+    const dim3 grid((p.num_seqs * p.q_len * p.q_heads + 7) / 8), block(256);
     if (head_dim == 128)
       return dt == PA_BF16 ? launch_pdl(lse_merge_warp_kernel<128, __nv_bfloat16>, grid, block, 0, stream, p)
                            : launch_pdl(lse_merge_warp_kernel<128, __half>, grid, block, 0, stream, p);
@@ -546,7 +577,7 @@ cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cu
                            : launch_pdl(lse_merge_warp_kernel<64, __half>, grid, block, 0, stream, p);
     return cudaErrorInvalidValue;
   }
-  const dim3 grid(p.num_seqs * p.q_heads), block(128);
+  const dim3 grid(p.num_seqs * p.q_len * p.q_heads), block(128);
   if (head_dim == 128)
     return dt == PA_BF16 ? launch_pdl(lse_merge_kernel<128, __nv_bfloat16>, grid, block, 0, stream, p)
                          : launch_pdl(lse_merge_kernel<128, __half>, grid, block, 0, stream, p);

@@ -318,20 +318,25 @@ size_t pa_decode_workspace_size(int num_seqs, int q_heads, int head_dim, int max
   return s.ws.bytes;
 }
 
-int pa_decode_partial(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads,
-                      int head_dim, int block_size, int num_blocks, float scale, int split_tokens, void* workspace,
-                      size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
+namespace {
+
+// The partition pass of decode (q_len = 1) and of the speculative verify
+// (q_len = k+1 queries per request, rows r*q_len + i).
+int decode_partial_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_len, int q_heads,
+                        int kv_heads, int head_dim, int block_size, int num_blocks, float scale, int split_tokens,
+                        void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
   int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || num_seqs > 65535 || q_heads <= 0 || q_heads % kv_heads != 0 || q_heads / kv_heads > 16)
     return PA_ERR_INVALID;
+  if (q_len < 1 || (q_heads / kv_heads) * q_len > 32) return PA_ERR_INVALID;
   if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID;
   DecodeSetup s;
-  st = decode_setup(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s);
+  st = decode_setup(num_seqs * q_len, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s);
   if (st != PA_OK) return st;
   if (s.ws.bytes > 0 && (!workspace || workspace_bytes < s.ws.bytes || !aligned16(workspace)))
     return PA_ERR_WORKSPACE;
@@ -364,20 +369,21 @@ int pa_decode_partial(const void* q, const void* k_cache, const void* v_cache, c
   p.grid_splits = s.max_splits;
   p.tab_entries = s.split / block_size;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_len = q_len;
   const int bsub = block_size < 16 ? block_size : 16;
   return cuda_status(
       launch_decode_partial(km, vm, p, head_dim, bsub, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* context_lens, int num_seqs,
-                 int q_heads, int head_dim, int max_blocks_per_seq, int block_size, int split_tokens, void* out,
-                 pa_dtype dtype, pa_stream stream) {
+int lse_merge_impl(const void* workspace, size_t workspace_bytes, const int32_t* context_lens, int num_seqs,
+                   int q_len, int q_heads, int head_dim, int max_blocks_per_seq, int block_size, int split_tokens,
+                   void* out, pa_dtype dtype, pa_stream stream) {
   if (dtype != PA_FP16 && dtype != PA_BF16) return PA_ERR_DTYPE;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_INVALID;
-  if (num_seqs < 0 || q_heads <= 0) return PA_ERR_INVALID;
+  if (num_seqs < 0 || q_heads <= 0 || q_len < 1) return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
   DecodeSetup s;
-  int st = decode_setup(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s);
+  int st = decode_setup(num_seqs * q_len, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s);
   if (st != PA_OK) return st;
   if (s.ws.bytes == 0) return PA_OK;  // a single partition: pa_decode_partial wrote `out`
   if (!workspace || workspace_bytes < s.ws.bytes || !aligned16(workspace)) return PA_ERR_WORKSPACE;
@@ -394,7 +400,48 @@ int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* c
   p.max_splits = s.max_splits;
   p.split_tokens = s.split;
   p.cap = max_blocks_per_seq * block_size;
+  p.q_len = q_len;
   return cuda_status(launch_lse_merge(p, head_dim, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+int pa_decode_partial(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads,
+                      int head_dim, int block_size, int num_blocks, float scale, int split_tokens, void* workspace,
+                      size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
+  return decode_partial_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, 1,
+                             q_heads, kv_heads, head_dim, block_size, num_blocks, scale, split_tokens, workspace,
+                             workspace_bytes, out, dtype, stream);
+}
+
+int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* context_lens, int num_seqs,
+                 int q_heads, int head_dim, int max_blocks_per_seq, int block_size, int split_tokens, void* out,
+                 pa_dtype dtype, pa_stream stream) {
+  return lse_merge_impl(workspace, workspace_bytes, context_lens, num_seqs, 1, q_heads, head_dim,
+                        max_blocks_per_seq, block_size, split_tokens, out, dtype, stream);
+}
+
+size_t pa_verify_workspace_size(int num_seqs, int q_len, int q_heads, int head_dim, int max_blocks_per_seq,
+                                int block_size, int split_tokens) {
+  if (num_seqs < 0 || q_len < 1 || q_heads <= 0 || head_dim <= 0) return 0;
+  DecodeSetup s;
+  if (decode_setup(num_seqs * q_len, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s) != PA_OK)
+    return 0;
+  return s.ws.bytes;
+}
+
+int pa_verify_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_len, int q_heads,
+                     int kv_heads, int head_dim, int block_size, int num_blocks, float scale, int split_tokens,
+                     void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
+  if (q_len < 1 || (int64_t)num_seqs * q_len > INT32_MAX / 64) return PA_ERR_INVALID;
+  int st = decode_partial_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, q_len,
+                               q_heads, kv_heads, head_dim, block_size, num_blocks, scale, split_tokens, workspace,
+                               workspace_bytes, out, dtype, stream);
+  if (st != PA_OK) return st;
+  return lse_merge_impl(workspace, workspace_bytes, context_lens, num_seqs, q_len, q_heads, head_dim,
+                        max_blocks_per_seq, block_size, split_tokens, out, dtype, stream);
 }
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -564,6 +611,7 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   dp.always_partial = 1;
   dp.prefix_blocks = prefix_blocks;
   dp.prefix_nblk = prefix_len / block_size;
+  dp.q_len = 1;
   st = cuda_status(launch_decode_partial(km, vm, dp, head_dim, bsub, dtype, cs));
   if (st != PA_OK) return st;
 
@@ -582,6 +630,7 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   mp.tok_begin = prefix_len;
   mp.extra_slots = s.prefix_splits;
   mp.always = 1;
+  mp.q_len = 1;
   return cuda_status(launch_lse_merge(mp, head_dim, dtype, cs));
 }
 

@@ -56,6 +56,10 @@ struct DecodeParams {
   const int32_t* prefix_blocks;
   int prefix_nblk;
   int grid_splits;  // partitions the grid covers (normal mode: max_splits)
+  // Queries per request (1 = decode; k+1 = speculative verify).  Query i of
+  // request r is row r*q_len + i of q / out / the partials and sees tokens
+  // [0, context_len - (q_len-1-i)).
+  int q_len;
 };
 
 struct MergeParams {
@@ -68,6 +72,7 @@ struct MergeParams {
   // shared-prefix mode: extra_slots partials precede the suffix partitions of
   // [tok_begin, context_len); every row is merged (even a single slot)
   int tok_begin, extra_slots, always;
+  int q_len;  // queries per request: row / (q_heads * q_len) is the request
 };
 
 struct PrefillParams {

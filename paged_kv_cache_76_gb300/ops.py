@@ -27,6 +27,8 @@ __all__ = [
     "decode_shared_prefix",
     "decode_shared_prefix_workspace_size",
     "decode_shared_prefix_split_tokens",
+    "verify_decode",
+    "verify_workspace_size",
     "get_device_error",
     "launch_count",
     "dtype_code",
@@ -168,6 +170,36 @@ def lse_merge(workspace, context_lens, q, block_tables, block_size, out, split_t
     check(_lib.lib().pa_lse_merge(ws_ptr, ws_bytes, _i32(context_lens, "context_lens"), B, hq, d,
                                   int(block_tables.shape[1]), block_size, int(split_tokens), _dev(out, "out"),
                                   dtype_code(out.dtype), _stream(stream)), "pa_lse_merge")
+
+
+def verify_workspace_size(num_seqs, q_len, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens=0) -> int:
+    return int(_lib.lib().pa_verify_workspace_size(num_seqs, q_len, q_heads, head_dim, max_blocks_per_seq,
+                                                   block_size, split_tokens))
+
+
+def verify_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, split_tokens=0, workspace=None,
+                  stream=None):
+    """pa_verify_decode: ``q`` is [num_seqs, k+1, q_heads, head_dim]; query i of
+    request r sees its first ``context_lens[r] - k + i`` tokens."""
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    if q.dim() != 4:
+        raise ValueError("q is [num_seqs, q_len, q_heads, head_dim]")
+    B, ql, hq, dq = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if dq != d or out.shape != q.shape or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    maxblk = int(block_tables.shape[1])
+    if workspace is None:
+        n = verify_workspace_size(B, ql, hq, d, maxblk, bs, split_tokens)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (None, 0)
+    check(_lib.lib().pa_verify_decode(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(block_tables, "block_tables"), maxblk,
+        _i32(context_lens, "context_lens"), B, ql, hq, hkv, d, bs, nb, float(scale), int(split_tokens), ws_ptr,
+        ws_bytes, _dev(out, "out"), dtype_code(q.dtype), _stream(stream)), "pa_verify_decode")
+    return out
 
 
 def decode_shared_prefix_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq, block_size, prefix_len,

@@ -1,0 +1,120 @@
+"""Speculative verify attention on the GPU ("Khám phá vLLM … phần 2",
+speculative decoding): k+1 queries per request over the paged cache, against
+the float64 oracle, plus the bitwise identities the method fixes (query i is
+decode over the first L-k+i tokens; q_len = 1 is decode)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import paged_attention as opa
+from tests.paged_step import assert_close, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_76_gb300 import _lib
+    try:
+        _lib.lib()
+    except _lib.LibraryMissing:
+        from paged_kv_cache_76_gb300 import build
+        build.build()
+    torch.cuda.init()
+
+
+def ops():
+    from paged_kv_cache_76_gb300 import ops as o
+    return o
+
+
+def _case(seed, q_len, hq, hkv, d, bs, dt, lens, extra_blocks=3):
+    rng = np.random.default_rng(seed)
+    nblk = [max(-(-L // bs), 1) for L in lens]
+    maxblk = max(nblk) + extra_blocks
+    nb = sum(nblk) + 7
+    perm = rng.permutation(nb)
+    tables = np.full((len(lens), maxblk), -1, dtype=np.int32)
+    off = 0
+    for r, n in enumerate(nblk):
+        tables[r, :n] = perm[off:off + n]
+        off += n
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float16
+    kc = torch.randn(nb, bs, hkv, d, generator=g, device="cuda").to(dtype)
+    vc = torch.randn(nb, bs, hkv, d, generator=g, device="cuda").to(dtype)
+    q = torch.randn(len(lens), q_len, hq, d, generator=g, device="cuda").to(dtype)
+    return q, kc, vc, torch.from_numpy(tables).cuda(), torch.tensor(lens, dtype=torch.int32, device="cuda")
+
+
+VERIFY_CASES = [
+    # q_len, q_heads, kv_heads, head_dim, block_size, dtype, lens, split_tokens
+    (4, 32, 8, 128, 16, "bf16", [700, 4, 1025, 33, 16], 0),         # 16 columns
+    (8, 32, 8, 128, 16, "bf16", [2000, 9, 517, 8], 256),           # 32 columns; last partitions empty for early queries
+    (3, 8, 8, 64, 4, "fp16", [2, 3, 50, 1], 64),                   # contexts shorter than q_len: zero rows
+    (2, 16, 2, 128, 32, "bf16", [1000, 65, 64], 128),
+    (5, 12, 2, 64, 8, "fp16", [300, 77, 5], 0),                    # 30 columns
+    (6, 4, 1, 128, 16, "bf16", [4096, 3000], 512),                 # 24 columns, many partitions
+    (1, 28, 4, 128, 16, "bf16", [300, 1029], 256),                 # q_len 1
+]
+
+
+@pytest.mark.parametrize("case", VERIFY_CASES, ids=[f"q{c[0]}_h{c[1]}x{c[2]}_d{c[3]}_bs{c[4]}" for c in VERIFY_CASES])
+def test_verify_matches_the_oracle(case):
+    q_len, hq, hkv, d, bs, dt, lens, split = case
+    q, kc, vc, tables, lens_t = _case(1, q_len, hq, hkv, d, bs, dt, lens)
+    scale = 1 / np.sqrt(d)
+    out = ops().verify_decode(q, kc, vc, tables, lens_t, scale, split_tokens=split)
+    ref = opa.verify_decode(to_f64(q), to_f64(kc), to_f64(vc), tables.cpu().numpy(), lens, scale)
+    assert_close(out, ref, f"verify {case}")
+    for r, L in enumerate(lens):
+        for i in range(q_len):
+            if L - (q_len - 1 - i) <= 0:
+                assert torch.count_nonzero(out[r, i]) == 0
+    assert ops().get_device_error() == 0
+
+
+@pytest.mark.parametrize("split", [0, 128])
+def test_each_query_is_bitwise_decode_over_its_visible_prefix(split):
+    q_len, hq, hkv, d, bs = 7, 32, 8, 128, 16
+    lens = [900, 130, 129, 7, 2050]
+    q, kc, vc, tables, lens_t = _case(2, q_len, hq, hkv, d, bs, "bf16", lens)
+    scale = 1 / np.sqrt(d)
+    out = ops().verify_decode(q, kc, vc, tables, lens_t, scale, split_tokens=split)
+    for i in range(q_len):
+        li = torch.clamp(lens_t - (q_len - 1 - i), min=0).to(torch.int32)
+        dec = ops().decode(q[:, i].contiguous(), kc, vc, tables, li, scale, split_tokens=split)
+        assert torch.equal(out[:, i], dec), i
+    assert ops().get_device_error() == 0
+
+
+def test_q_len_one_is_decode_bitwise_and_relabelling_changes_no_bit():
+    hq, hkv, d, bs = 32, 8, 128, 16
+    lens = [1500, 17, 600]
+    q, kc, vc, tables, lens_t = _case(3, 1, hq, hkv, d, bs, "bf16", lens)
+    scale = 1 / np.sqrt(d)
+    out = ops().verify_decode(q, kc, vc, tables, lens_t, scale)
+    assert torch.equal(out[:, 0], ops().decode(q[:, 0].contiguous(), kc, vc, tables, lens_t, scale))
+    q4, kc4, vc4, t4, l4 = _case(4, 4, hq, hkv, d, bs, "bf16", lens)
+    a = ops().verify_decode(q4, kc4, vc4, t4, l4, scale)
+    pi = torch.randperm(kc4.shape[0], generator=torch.Generator().manual_seed(5)).cuda()
+    k2, v2 = torch.empty_like(kc4), torch.empty_like(vc4)
+    k2[pi] = kc4
+    v2[pi] = vc4
+    t2 = torch.where(t4 >= 0, pi[t4.clamp(min=0).long()].int(), t4)
+    b = ops().verify_decode(q4, k2, v2, t2, l4, scale)
+    assert torch.equal(a, b)
+    assert ops().get_device_error() == 0
+
+
+def test_verify_rejects_too_many_columns_and_bad_q_len():
+    from paged_kv_cache_76_gb300 import _lib
+    q, kc, vc, tables, lens_t = _case(6, 3, 48, 4, 128, 16, "bf16", [40])   # 12 heads x 3 queries = 36 columns
+    with pytest.raises(_lib.PAError):
+        ops().verify_decode(q, kc, vc, tables, lens_t, 0.1)
+    L = _lib.lib()
+    st = L.pa_verify_decode(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), tables.data_ptr(), tables.shape[1],
+                            lens_t.data_ptr(), 1, 0, 48, 4, 128, 16, kc.shape[0], 0.1, 0, None, 0, q.data_ptr(),
+                            _lib.PA_BF16, torch.cuda.current_stream().cuda_stream)
+    assert st == _lib.PA_ERR_INVALID
+    assert ops().get_device_error() == 0
