@@ -189,7 +189,10 @@ class Step:
             # a prefix every decode request shares (e.g. a common system prompt)
             # goes through pa_decode_shared_prefix: read once for all queries
             self.prefix_len = 0
-            if shared_prefix and wl.block_size >= 8 and len(wl.decode_seqs) >= 8:
+            if wl.q_len > 1:  # speculative verify: k+1 queries per request
+                n = ops.verify_workspace_size(len(wl.decode_seqs), wl.q_len, wl.q_heads, wl.head_dim, maxblk,
+                                              wl.block_size, self.split)
+            if shared_prefix and wl.q_len == 1 and wl.block_size >= 8 and len(wl.decode_seqs) >= 8:
                 nshared = a.common_prefix(wl.decode_seqs)
                 if nshared >= 8:
                     self.prefix_len = nshared * wl.block_size
@@ -290,6 +293,13 @@ class Step:
                                    workspace=self.workspace, stream=stream)
             if ev is not None:
                 ev[1].record(stream)
+        elif self.dec and wl.q_len > 1:
+            if ev is not None:
+                ev[0].record(stream)
+            o.verify_decode(d["q_decode"], self.k_cache, self.v_cache, d["dec_tables"], d["dec_lens"], wl.scale,
+                            out=self.out_dec, split_tokens=self.split, workspace=self.workspace, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
         elif self.dec:
             if ev is not None:
                 ev[0].record(stream)
@@ -353,13 +363,14 @@ class Step:
         out = {}
         if self.dec:
             L = self.dec_lens
-            out["decode"] = int(np.sum(2 * L * tok + 2 * qrow + 4 * np.ceil(L / bs) + 4))
+            out["decode"] = int(np.sum(2 * L * tok + 2 * qrow * wl.q_len + 4 * np.ceil(L / bs) + 4))
             used = {}
             for r, Lr in enumerate(L):
                 for j in range(int(math.ceil(Lr / bs))):
                     b = int(self.dec_tables_np[r, j])
                     used[b] = max(used.get(b, 0), min(bs, int(Lr) - j * bs))
-            out["decode_unique"] = int(sum(used.values()) * 2 * tok + np.sum(2 * qrow + 4 * np.ceil(L / bs) + 4))
+            out["decode_unique"] = int(sum(used.values()) * 2 * tok +
+                                       np.sum(2 * qrow * wl.q_len + 4 * np.ceil(L / bs) + 4))
         T = int(self.h["slots"].numel())
         out["reshape_and_cache"] = T * (4 * tok + 4)
         out["copy_blocks"] = self.n_pairs * (4 * bs * tok + 8)
@@ -392,7 +403,8 @@ def _unit_inputs(step: Step, unit, token_index):
     if kind == "decode":
         table = step.dec_tables_np[r]
         L = int(step.dec_lens[r])
-        q = step.h["q_decode"][r, g * G:(g + 1) * G][None]
+        q = step.h["q_decode"][r, ..., g * G:(g + 1) * G, :]
+        q = q[None] if wl.q_len == 1 else q  # [q_len, G, D]
     else:
         table = step.pre_tables_np[r]
         L = int(step.pre_lens[r])
@@ -422,7 +434,7 @@ def _unit_bytes(step: Step, unit):
     e, D, G, bs = 2, wl.head_dim, wl.q_heads // wl.kv_heads, wl.block_size
     if kind == "decode":
         L = int(step.dec_lens[r])
-        return 2 * L * D * e + 2 * G * D * e + (4 * math.ceil(L / bs) + 4) / wl.kv_heads
+        return 2 * L * D * e + 2 * G * D * e * wl.q_len + (4 * math.ceil(L / bs) + 4) / wl.kv_heads
     L = int(step.pre_lens[r])
     c = step.chunks[r]
     return 2 * L * D * e + 2 * c * G * D * e + (4 * math.ceil(L / bs) + 8) / wl.kv_heads
@@ -438,7 +450,9 @@ def run_oracle_units(step: Step, units, budget_s: float):
         x = _unit_inputs(step, u, 0)
         t0 = time.perf_counter()
         kc, vc = opa.reshape_and_cache(x["kn"], x["vn"], x["slots"], x["kc"], x["vc"])
-        if u[0] == "decode":
+        if u[0] == "decode" and wl.q_len > 1:
+            opa.verify_decode(x["q"][None], kc, vc, x["table"], [x["L"]], wl.scale)
+        elif u[0] == "decode":
             opa.decode(x["q"], kc, vc, x["table"], [x["L"]], wl.scale)
         else:
             opa.chunked_prefill(x["q"], [0, x["chunk"]], [x["L"]], kc, vc, x["table"], wl.scale)
@@ -639,6 +653,7 @@ def main():
             "context_lens": [int(min(step.dec_lens)), int(max(step.dec_lens))] if n_dec else None,
             "mean_context": float(np.mean(step.dec_lens)) if n_dec else None,
             "split_tokens": step.split if n_dec else None,
+            "queries_per_request": wl.q_len,
             "prefill_chunks": step.chunks if step.pre else None,
             "copy_pairs": step.n_pairs,
             "bytes_per_step": nb,
@@ -678,8 +693,10 @@ def main():
         dec_bytes = nb["decode"]
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
         traffic = kernel_traffic(f"decode_partial_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/decode.cu")
+        verify = wl.q_len > 1
         res["roofline"] = {
-            "kernel": "decode_partial_kernel",
+            "kernel": ("decode_partial_kernel with q_len=k+1 + lse_merge (pa_verify_decode)" if verify
+                       else "decode_partial_kernel"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -689,9 +706,13 @@ def main():
             "traffic": traffic,
             "algorithmic_bytes_per_launch": dec_bytes,
             "avg_launch_ms": round(dec_ms, 5),
-            "timing": "CUDA events around each of K decode_partial launches on the bench stream, "
-                      "in a second pass of the same K steps",
+            "timing": (f"CUDA events around each of K pa_verify_decode calls (partial + merge kernels) on the "
+                       f"bench stream, in a second pass of the same K steps" if verify else
+                       "CUDA events around each of K decode_partial launches on the bench stream, "
+                       "in a second pass of the same K steps"),
         }
+        if verify:
+            res["roofline"]["q_len"] = wl.q_len
         if "decode_unique" in nb and nb["decode_unique"] < dec_bytes:
             res["roofline"]["unique_bytes_per_launch"] = nb["decode_unique"]
             res["roofline"]["achieved_unique"] = round(nb["decode_unique"] / (dec_ms * 1e-3) / 1e9, 1)

@@ -77,7 +77,8 @@ def oracle_step(wl: W.Workload, vals: dict, decode_rows=None, prefill_rows=None,
         tabs = [tab(s) for s in dec_seqs]
         lens = [m.num_tokens[s] for s in dec_seqs]
         q = to_f64(vals["q_decode"])[dec_idx]
-        res["decode"] = opa.decode(q, kc, vc, padded(tabs, max(map(len, tabs))), lens, wl.scale)
+        attend = opa.decode if wl.q_len == 1 else opa.verify_decode
+        res["decode"] = attend(q, kc, vc, padded(tabs, max(map(len, tabs))), lens, wl.scale)
         res["decode_lens"] = lens
     if wl.prefill:
         tabs = [tab(s) for s in pre_seqs]
@@ -121,7 +122,12 @@ class DeviceStep:
             self.q_decode = vals["q_decode"].to(d).contiguous()
             self.out_decode = torch.empty_like(self.q_decode)
             from paged_kv_cache_76_gb300 import ops
-            self.workspace = ops.make_workspace(self.q_decode, self.dec_tables, wl.block_size, self.split_tokens)
+            if wl.q_len == 1:
+                self.workspace = ops.make_workspace(self.q_decode, self.dec_tables, wl.block_size, self.split_tokens)
+            else:
+                n = ops.verify_workspace_size(len(wl.decode_seqs), wl.q_len, wl.q_heads, wl.head_dim, maxblk,
+                                              wl.block_size, self.split_tokens)
+                self.workspace = torch.empty(n, dtype=torch.uint8, device=d) if n else None
         if wl.prefill:
             seqs = [s for s, _, _ in wl.prefill]
             maxblk = max(len(a.block_table(s)) for s in seqs)
@@ -146,9 +152,9 @@ class DeviceStep:
             ops.chunked_prefill(self.q_prefill, self.q_start, self.pre_lens, self.k_cache, self.v_cache,
                                 self.pre_tables, wl.scale, self.max_q_len, out=self.out_prefill, stream=stream)
         if wl.decode_seqs:
-            ops.decode(self.q_decode, self.k_cache, self.v_cache, self.dec_tables, self.dec_lens, wl.scale,
-                       out=self.out_decode, split_tokens=self.split_tokens, workspace=self.workspace,
-                       stream=stream)
+            attend = ops.decode if wl.q_len == 1 else ops.verify_decode
+            attend(self.q_decode, self.k_cache, self.v_cache, self.dec_tables, self.dec_lens, wl.scale,
+                   out=self.out_decode, split_tokens=self.split_tokens, workspace=self.workspace, stream=stream)
 
 
 def assert_close(got: torch.Tensor, ref: np.ndarray, what=""):

@@ -43,6 +43,19 @@ def test_llama8b_gqa_decode_full_size():
     _no_err()
 
 
+def test_spec_verify_decode_full_size():
+    """The verify workload as bench.py times it: reshape_and_cache of the k=3
+    drafts, then pa_verify_decode; sampled requests against the oracle."""
+    wl = W.spec_verify_decode()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    dev.run()
+    rows = list(range(0, 64, 8))
+    ref = oracle_step(wl, vals, decode_rows=rows, compact=True)
+    assert_close(dev.out_decode[rows], ref["decode"], "verify sampled")
+    _no_err()
+
+
 def test_long_context_splitk_decode_full_size():
     wl = W.long_context_splitk_decode()
     vals = W.make_values(wl, device="cuda")

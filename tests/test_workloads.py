@@ -34,6 +34,16 @@ def test_decode_workloads_shape(name):
     assert lo <= min(wl.decode_lens) and max(wl.decode_lens) <= hi
 
 
+def test_spec_verify_workload_writes_k_plus_one_tokens_per_request():
+    wl = W.spec_verify_decode()
+    m, slots, pairs = _replay(wl)
+    assert wl.q_len == 4 and len(slots) == wl.new_tokens == 4 * len(wl.decode_seqs) and pairs == []
+    for s, L in zip(wl.decode_seqs, wl.decode_lens):
+        assert m.num_tokens[s] == L and 512 <= L <= 4096
+    vals = W.make_values(wl)
+    assert vals["q_decode"].shape == (64, 4, 32, 128)
+
+
 def test_prefix_shared_workload_refcounts_and_cow():
     wl = W.prefix_shared_cow_decode()
     m = SequenceManager(wl.num_blocks, wl.block_size, wl.free_order)

@@ -65,6 +65,7 @@ class Workload:
     decode_lens: list = field(default_factory=list)     # context length incl. the new token
     prefill: list = field(default_factory=list)         # (seq id, chunk tokens, context len incl. chunk)
     split_tokens: int = 0           # 0 = let the library choose
+    q_len: int = 1                  # queries per decode request (k+1 for a speculative verify)
     value_dist: str = "normal"      # "normal" N(0,1) | "uniform" U[-1,1]
     seed: int = 0
     note: str = ""
@@ -98,14 +99,14 @@ def _pool(rng, needed_blocks: int, factor: float = 1.5):
     return nb, rng.permutation(nb).astype(np.int32)
 
 
-def _decode_scripts(seqs, lens):
-    """History of len-1 tokens per sequence, then one new token this step."""
+def _decode_scripts(seqs, lens, new: int = 1):
+    """History of len-new tokens per sequence, then `new` tokens this step."""
     setup, step = [], []
     for s, L in zip(seqs, lens):
         setup.append(("add", s))
-        if L - 1 > 0:
-            setup.append(("append", s, L - 1))
-        step.append(("append", s, 1))
+        if L - new > 0:
+            setup.append(("append", s, L - new))
+        step.append(("append", s, min(new, L)))
     return setup, step
 
 
@@ -162,6 +163,22 @@ def llama8b_gqa_decode(seed: int = 0, batch: int = 64, len_lo: int = 512, len_hi
     """Batch 64, 32 q heads / 8 KV heads, D=128, bs=16, bf16 N(0,1), lens U{512..4096}."""
     wl = custom_decode(batch, len_lo, len_hi, 32, 8, 128, 16, "bf16", seed, name="llama8b_gqa_decode")
     wl.note = "one query token per request; pool 1.5x needed, shuffled free list"
+    return wl
+
+
+def spec_verify_decode(seed: int = 0, batch: int = 64, len_lo: int = 512, len_hi: int = 4096,
+                       k: int = 3) -> Workload:
+    """Verify step of speculative decoding on the llama8b_gqa_decode shape.
+
+    Batch 64, 32 q heads / 8 KV heads, D=128, bs=16, bf16 N(0,1); each
+    request's context is U{512..4096} tokens including its k=3 draft tokens,
+    whose K/V this step writes; k+1 = 4 queries per request (the last
+    accepted token and the drafts), 16 query rows per KV head.
+    """
+    wl = custom_decode(batch, len_lo, len_hi, 32, 8, 128, 16, "bf16", seed, name="spec_verify_decode")
+    wl.q_len = k + 1
+    wl.setup_ops, wl.step_ops = _decode_scripts(wl.decode_seqs, wl.decode_lens, k + 1)
+    wl.note = f"k={k} draft tokens per request written this step; k+1 causal queries per request"
     return wl
 
 
@@ -278,6 +295,7 @@ WORKLOADS = {
     "tiny_paged_decode": tiny_paged_decode,
     "llama8b_gqa_decode": llama8b_gqa_decode,
     "long_context_splitk_decode": long_context_splitk_decode,
+    "spec_verify_decode": spec_verify_decode,
     "prefix_shared_cow_decode": prefix_shared_cow_decode,
     "mixed_prefill_decode": mixed_prefill_decode,
     "mixed_prefill_part": mixed_prefill_part,
@@ -292,7 +310,8 @@ def make_values(wl: Workload, device="cpu", seed: int | None = None, poison_pool
 
     * ``k_cache``, ``v_cache``: [num_blocks, block_size, kv_heads, head_dim],
       the pool's contents before the step (history and stale data alike);
-    * ``q_decode``: [len(decode_seqs), q_heads, head_dim];
+    * ``q_decode``: [len(decode_seqs), q_heads, head_dim], or
+      [len(decode_seqs), q_len, q_heads, head_dim] when q_len > 1;
     * ``q_prefill``: [sum of chunks, q_heads, head_dim];
     * ``k_new``, ``v_new``: [new_tokens, kv_heads, head_dim], ordered as the
       step's ``append`` ops list their tokens.
@@ -309,7 +328,8 @@ def make_values(wl: Workload, device="cpu", seed: int | None = None, poison_pool
     shapes = {
         "k_cache": pool_shape,
         "v_cache": pool_shape,
-        "q_decode": (len(wl.decode_seqs), wl.q_heads, wl.head_dim),
+        "q_decode": ((len(wl.decode_seqs), wl.q_heads, wl.head_dim) if wl.q_len == 1 else
+                     (len(wl.decode_seqs), wl.q_len, wl.q_heads, wl.head_dim)),
         "q_prefill": (nq_pref, wl.q_heads, wl.head_dim),
         "k_new": (wl.new_tokens, wl.kv_heads, wl.head_dim),
         "v_new": (wl.new_tokens, wl.kv_heads, wl.head_dim),
