@@ -21,6 +21,11 @@ Reported (one JSON line from rank 0):
   -> device copies of the step's inputs and a device -> host read of its
   outputs inside the timed region.
 ``--impl reference`` times the CPU oracle itself as the reference arm.
+``--kv-layout contiguous|vmm`` (decode-only workloads) runs the same step on
+the competing design of "vAttention 完全拆解": one contiguous
+[slots][max_len][kv_heads][head_dim] K and V per layer (plain device memory,
+or a virtual range whose 2 MiB pages are mapped on demand), no Block Table;
+the contexts are the paged step's, copied in before timing.
 Multi-GPU: independent replicas (the path needs no collective); N>1 runs under
 torch.distributed.run with one rank per GPU.
 """
@@ -152,7 +157,7 @@ class Step:
     """Device buffers and host copies of one workload step; runs it through the C ABI."""
 
     def __init__(self, wl: W.Workload, device: torch.device, value_seed: int, overlap_streams: bool = True,
-                 shared_prefix: bool = True):
+                 shared_prefix: bool = True, kv_layout: str = "paged"):
         from paged_kv_cache_76_gb300 import ops
         from paged_kv_cache_76_gb300.allocator import BlockAllocator
         self.ops = ops
@@ -175,6 +180,9 @@ class Step:
         self.n_pairs = len(pairs)
         self.dec = bool(wl.decode_seqs)
         self.pre = bool(wl.prefill)
+        self.layout = kv_layout
+        if kv_layout != "paged" and (self.pre or self.n_pairs or wl.q_len != 1 or not self.dec):
+            raise ValueError("--kv-layout contiguous|vmm takes a decode-only workload")
         if self.dec:
             maxblk = max(len(a.block_table(s)) for s in wl.decode_seqs)
             t, l = a.build_tables(wl.decode_seqs, maxblk)
@@ -202,6 +210,10 @@ class Step:
                                                                        wl.split_tokens)
                     n = ops.decode_shared_prefix_workspace_size(len(wl.decode_seqs), wl.q_heads, wl.head_dim, maxblk,
                                                                 wl.block_size, self.prefix_len, self.split)
+            if kv_layout != "paged":
+                shared_prefix = False
+                self.prefix_len = 0
+                n = self._contiguous_setup(a, device)
             self.workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=device) if n else None
         if self.pre:
             seqs = [s for s, _, _ in wl.prefill]
@@ -262,9 +274,72 @@ class Step:
         self.h_out_dec = hv.get("dec")
         self.h_out_pre = hv.get("pre")
 
+    def _contiguous_setup(self, a, device):
+        """Contiguous per-slot K/V holding the paged step's contexts (request r in slot r)."""
+        from paged_kv_cache_76_gb300 import vattention as va
+        wl = self.wl
+        S = len(wl.decode_seqs)
+        row = wl.kv_heads * wl.head_dim * 2
+        lens = self.dec_lens.astype(np.int64)
+        self.vkv = None
+        if self.layout == "vmm":
+            G = va.VirtualKV.granularity()
+            unit = int(np.lcm(16, G // math.gcd(G, row)))
+            L = int(-(-int(lens.max()) // unit) * unit)
+            t0 = time.perf_counter()
+            self.vkv = va.VirtualKV(S, L, 1, wl.kv_heads, wl.head_dim, wl.torch_dtype, page_bytes=G)
+            for _ in range(S):
+                self.vkv.alloc_slot()
+            self.vkv.step(lens.astype(np.int32))
+            torch.cuda.synchronize()
+            self.vmm_setup_s = time.perf_counter() - t0
+            self.ck, self.cv = self.vkv.tensor(0, False), self.vkv.tensor(0, True)
+        else:
+            L = int(-(-int(lens.max()) // 16) * 16)
+            self.ck = torch.empty(S, L, wl.kv_heads, wl.head_dim, dtype=wl.torch_dtype, device=device)
+            self.cv = torch.empty_like(self.ck)
+        self.max_len = L
+        # history: every token but this step's new one, copied block by block
+        # (rows inside each slot's mapped range only)
+        bs = wl.block_size
+        for r, s in enumerate(wl.decode_seqs):
+            hist = int(lens[r]) - 1
+            t = self.dec_tables_np[r]
+            for j in range(-(-hist // bs)):
+                n = min(bs, hist - j * bs)
+                self.ck[r, j * bs:j * bs + n] = self.k_cache[int(t[j]), :n]
+                self.cv[r, j * bs:j * bs + n] = self.v_cache[int(t[j]), :n]
+        torch.cuda.synchronize()
+        del self.h["dec_tables"]  # no Block Table on this layout
+        self.h["slot_ids"] = torch.arange(S, dtype=torch.int32).pin_memory()
+        self.h["positions"] = torch.from_numpy((lens - 1).astype(np.int32)).pin_memory()
+        return self.ops.decode_workspace_size(S, wl.q_heads, wl.head_dim, L // 16, 16, wl.split_tokens)
+
+    def _run_contiguous(self, stream, ev):
+        from paged_kv_cache_76_gb300 import vattention as va
+        o, d, wl = self.ops, self.d, self.wl
+        if self.vkv is not None:
+            self.vkv.reshape_and_cache(0, d["k_new"], d["v_new"], d["slot_ids"], d["positions"], stream=stream)
+        else:
+            va.reshape_and_cache_slots(d["k_new"], d["v_new"], d["slot_ids"], d["positions"], self.ck, self.cv,
+                                       stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        if self.vkv is not None:
+            self.vkv.decode(0, d["q_decode"], d["slot_ids"], d["dec_lens"], wl.scale, out=self.out_dec,
+                            split_tokens=wl.split_tokens, workspace=self.workspace, stream=stream)
+        else:
+            va.decode_contiguous(d["q_decode"], self.ck, self.cv, d["slot_ids"], d["dec_lens"], wl.scale,
+                                 out=self.out_dec, split_tokens=wl.split_tokens, workspace=self.workspace,
+                                 stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
     # -- one step through the C ABI; ev = (start, end) events around the decode partial kernel
     def run(self, stream, ev=None):
         o, d, wl = self.ops, self.d, self.wl
+        if self.layout != "paged":
+            return self._run_contiguous(stream, ev)
         if self.n_pairs:
             o.copy_blocks(self.k_cache, self.v_cache, d["pairs"], stream=stream)
         o.reshape_and_cache(d["k_new"], d["v_new"], d["slots"], self.k_cache, self.v_cache, stream=stream)
@@ -363,7 +438,8 @@ class Step:
         out = {}
         if self.dec:
             L = self.dec_lens
-            out["decode"] = int(np.sum(2 * L * tok + 2 * qrow * wl.q_len + 4 * np.ceil(L / bs) + 4))
+            table = 4 * np.ceil(L / bs) if self.layout == "paged" else 4  # contiguous: a slot id instead
+            out["decode"] = int(np.sum(2 * L * tok + 2 * qrow * wl.q_len + table + 4))
             used = {}
             for r, Lr in enumerate(L):
                 for j in range(int(math.ceil(Lr / bs))):
@@ -478,6 +554,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--serial", action="store_true", help="run prefill and decode on one stream, one after the other")
+    ap.add_argument("--kv-layout", default="paged", choices=["paged", "contiguous", "vmm"],
+                    help="decode-only workloads: paged blocks (default), or one contiguous K/V per request slot in "
+                         "plain memory or in on-demand-mapped virtual memory (the vAttention comparison)")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="decode a shared prefix per request instead of once for the batch")
     ap.add_argument("--prefill-ctas", type=int, default=None,
@@ -504,7 +583,7 @@ def main():
     if args.split is not None:
         wl.split_tokens = args.split
     step = Step(wl, device, value_seed=1000 * rank, overlap_streams=not args.serial,
-                shared_prefix=not args.no_shared_prefix)
+                shared_prefix=not args.no_shared_prefix, kv_layout=args.kv_layout)
     peak, peak_kind = measured_peaks()
 
     if args.impl == "reference":
@@ -654,6 +733,7 @@ def main():
             "mean_context": float(np.mean(step.dec_lens)) if n_dec else None,
             "split_tokens": step.split if n_dec else None,
             "queries_per_request": wl.q_len,
+            "kv_layout": step.layout,
             "prefill_chunks": step.chunks if step.pre else None,
             "copy_pairs": step.n_pairs,
             "bytes_per_step": nb,
@@ -668,6 +748,15 @@ def main():
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    if step.layout != "paged":
+        res["config"]["max_len"] = step.max_len
+        if step.vkv is not None:
+            vs = step.vkv.stats()
+            res["config"]["vmm"] = {"page_bytes": vs["page_bytes"], "pages_mapped": vs["pages_mapped"],
+                                    "bytes_committed": vs["bytes_committed"], "bytes_reserved": vs["bytes_reserved"],
+                                    "map_calls": vs["map_calls"],
+                                    "map_us_per_page": round(vs["total_map_ns"] / max(1, vs["map_calls"]) / 1e3, 2),
+                                    "setup_s": round(step.vmm_setup_s, 3)}
     if step.dec and step.prefix_len:
         ub = nb["decode_unique"]
         flops = 4 * len(wl.decode_seqs) * wl.q_heads * wl.head_dim * step.prefix_len
@@ -692,11 +781,14 @@ def main():
     elif step.dec:
         dec_bytes = nb["decode"]
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-        traffic = kernel_traffic(f"decode_partial_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/decode.cu")
+        prof = (f"decode_partial_{wl.name}.md" if step.layout == "paged" else
+                f"decode_contiguous_{step.layout}_{wl.name}.md")
+        traffic = kernel_traffic(prof, "paged_kv_cache_76_gb300/csrc/decode.cu")
         verify = wl.q_len > 1
         res["roofline"] = {
             "kernel": ("decode_partial_kernel with q_len=k+1 + lse_merge (pa_verify_decode)" if verify
-                       else "decode_partial_kernel"),
+                       else "decode_partial_kernel" if step.layout == "paged" else
+                       f"decode_partial_kernel, contiguous mode + lse_merge ({step.layout} memory)"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -708,6 +800,8 @@ def main():
             "avg_launch_ms": round(dec_ms, 5),
             "timing": (f"CUDA events around each of K pa_verify_decode calls (partial + merge kernels) on the "
                        f"bench stream, in a second pass of the same K steps" if verify else
+                       "CUDA events around each of K contiguous decode calls (partial + merge kernels) on the "
+                       "bench stream, in a second pass of the same K steps" if step.layout != "paged" else
                        "CUDA events around each of K decode_partial launches on the bench stream, "
                        "in a second pass of the same K steps"),
         }

@@ -231,6 +231,99 @@ int pa_verify_decode(const void* q, const void* k_cache, const void* v_cache, co
                      void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream);
 
 /* ----------------------------------------------------------------------------
+ * Contiguous virtual KV, vAttention style ("vAttention 完全拆解") - the
+ * competing design, built as a comparison baseline for the paged kernels.
+ *
+ * Each K and V tensor of each layer is ONE contiguous virtual range
+ * [num_slots][max_len][kv_heads][head_dim]; request slot s starts at
+ * s*max_len*kv_heads*head_dim*2 bytes, token t of the slot is row
+ * s*max_len + t, and no Block Table exists.  Physical pages (CUDA virtual
+ * memory: cuMemCreate / cuMemMap / cuMemSetAccess) are mapped into a slot
+ * only when pa_vkv_step sees its length reach them:
+ *  - pages for n tokens: ceil(roundup(n, 16) * kv_heads*head_dim*2 /
+ *    page_bytes) in every one of the 2*num_layers sub-tensors (the attention
+ *    kernel reads whole 16-token tiles, so the rounded length is mapped);
+ *  - pa_vkv_free_slot keeps the slot's pages mapped; pa_vkv_alloc_slot hands
+ *    out the free slot holding the most pages (lowest id on ties), whose
+ *    pages the new request reuses;
+ *  - a step that needs more than max_pages mapped pages in total unmaps whole
+ *    inactive slots (lowest id first, after cudaDeviceSynchronize) and fails
+ *    with PA_ERR_NO_FREE_BLOCKS, changing nothing, if even that is not enough.
+ * page_bytes = 0 takes the driver's minimum granularity (2 MiB on current
+ * GPUs); max_len * kv_heads*head_dim*2 must be a multiple of page_bytes and
+ * max_len a multiple of 16.  PA_VKV_DRY_RUN keeps only the bookkeeping (no
+ * memory, no GPU needed; page_bytes must then be given).
+ * Kernels only ever touch rows below a slot's mapped bound: pa_vkv_decode and
+ * pa_vkv_reshape_and_cache check every access against the device copy of the
+ * per-slot mapped token counts, which pa_vkv_step updates in stream order.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_vkv pa_vkv;
+#define PA_VKV_DRY_RUN 1
+
+typedef struct {
+  int64_t page_bytes;
+  int64_t slot_pages;        /* virtual pages per slot per sub-tensor          */
+  int64_t pages_mapped;      /* over all sub-tensors                           */
+  int64_t pages_pooled;      /* created, currently unmapped                    */
+  int64_t pages_created;     /* cuMemCreate calls                              */
+  int64_t map_calls;         /* page mappings made (one per page per tensor)   */
+  int64_t unmap_calls;
+  int64_t bytes_reserved;    /* virtual address space                          */
+  int64_t bytes_committed;   /* pages_mapped * page_bytes                      */
+  int64_t last_step_map_ns;  /* host time the last pa_vkv_step spent mapping   */
+  int64_t total_map_ns;
+  int64_t active_slots;
+} pa_vkv_stats;
+
+int pa_vkv_granularity(size_t* out);
+int pa_vkv_create(int num_slots, int max_len, int num_layers, int kv_heads, int head_dim, pa_dtype dtype,
+                  size_t page_bytes, int64_t max_pages, int flags, pa_vkv** out);
+/* Synchronises the device, unmaps and releases every page, frees the range. */
+void pa_vkv_destroy(pa_vkv* v);
+int pa_vkv_alloc_slot(pa_vkv* v, int* slot_out);
+int pa_vkv_free_slot(pa_vkv* v, int slot);
+/* lens: HOST int32 [num_slots], the length every slot reaches this iteration
+ * (0 for inactive slots).  Maps what is missing, then copies the per-slot
+ * mapped token counts to the device on `stream`. */
+int pa_vkv_step(pa_vkv* v, const int32_t* lens, pa_stream stream);
+/* Base of layer `layer`'s K (is_v = 0) or V tensor; NULL in dry-run mode. */
+int pa_vkv_tensor(const pa_vkv* v, int layer, int is_v, void** out);
+/* Tokens of each slot backed by mapped pages: into host_out [num_slots] (may
+ * be NULL); *device_out (may be NULL) = the device copy the kernels read. */
+int pa_vkv_slot_tokens(const pa_vkv* v, int32_t* host_out, const int32_t** device_out);
+int pa_vkv_slot_pages(const pa_vkv* v, int slot);
+int pa_vkv_get_stats(const pa_vkv* v, pa_vkv_stats* out);
+
+/* Decode over a contiguous [num_slots][max_len][kv_heads][head_dim] cache:
+ * request r reads slot slot_ids[r] (device int32 [num_seqs]; NULL: slot r),
+ * tokens [0, context_lens[r]).  slot_tokens (device int32 [num_slots], may be
+ * NULL = all max_len rows exist) bounds the rows each slot has backed by
+ * memory: a context past it records PA_DEVERR_CONTEXT_LEN and its tokens past
+ * the bound count as absent; a bad slot id records PA_DEVERR_BLOCK_ID and
+ * gives a zero row.  Same math, partitions (pa_decode_split_tokens(max_len/16,
+ * 16, split_tokens)) and workspace (pa_decode_workspace_size(num_seqs,
+ * q_heads, head_dim, max_len/16, 16, split_tokens)) as pa_decode with 16-token
+ * blocks, whose result it equals bit for bit on the same K/V. */
+int pa_decode_contiguous(const void* q, const void* k_cache, const void* v_cache, int num_slots, int max_len,
+                         const int32_t* slot_ids, const int32_t* slot_tokens, const int32_t* context_lens,
+                         int num_seqs, int q_heads, int kv_heads, int head_dim, float scale, int split_tokens,
+                         void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream);
+/* reshape_and_cache into a contiguous cache: token i to row
+ * slot_ids[i]*max_len + positions[i] (slot < 0: padding, skipped); a
+ * position outside [0, bound) - bound = slot_tokens[slot] or max_len - records
+ * PA_DEVERR_SLOT and is skipped. */
+int pa_reshape_and_cache_slots(const void* k, const void* v, const int32_t* slot_ids, const int32_t* positions,
+                               int num_tokens, void* k_cache, void* v_cache, int num_slots, int max_len,
+                               const int32_t* slot_tokens, int kv_heads, int head_dim, pa_dtype dtype,
+                               pa_stream stream);
+/* The two calls above on layer `layer` of a manager, with its mapped bounds. */
+int pa_vkv_decode(const pa_vkv* v, int layer, const void* q, const int32_t* slot_ids, const int32_t* context_lens,
+                  int num_seqs, int q_heads, float scale, int split_tokens, void* workspace, size_t workspace_bytes,
+                  void* out, pa_stream stream);
+int pa_vkv_reshape_and_cache(const pa_vkv* v, int layer, const void* k, const void* vv, const int32_t* slot_ids,
+                             const int32_t* positions, int num_tokens, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
  * pa_decode_shared_prefix - decode for a batch whose requests all start with
  * the same physical blocks (a shared prompt prefix).
  *

@@ -53,6 +53,14 @@ class PrefixCacheStats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("lookup_blocks", "hit_blocks", "evictions", "cached_blocks")]
 
 
+class VkvStats(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in (
+        "page_bytes", "slot_pages", "pages_mapped", "pages_pooled", "pages_created", "map_calls", "unmap_calls",
+        "bytes_reserved", "bytes_committed", "last_step_map_ns", "total_map_ns", "active_slots")]
+
+
+PA_VKV_DRY_RUN = 1
+
 _P = C.c_void_p
 _I = C.c_int
 _I32P = C.POINTER(C.c_int32)
@@ -101,6 +109,20 @@ PROTOTYPES = {
     "pa_alloc_append_tokens": (_I, [_P, _I, _I32P, _I, _I32P]),
     "pa_alloc_block_hash": (_I, [_P, _I, C.POINTER(C.c_uint64), C.POINTER(_I)]),
     "pa_alloc_get_prefix_cache_stats": (_I, [_P, C.POINTER(PrefixCacheStats)]),
+    "pa_vkv_granularity": (_I, [C.POINTER(_SZ)]),
+    "pa_vkv_create": (_I, [_I, _I, _I, _I, _I, _I, _SZ, C.c_int64, _I, C.POINTER(_P)]),
+    "pa_vkv_destroy": (None, [_P]),
+    "pa_vkv_alloc_slot": (_I, [_P, C.POINTER(_I)]),
+    "pa_vkv_free_slot": (_I, [_P, _I]),
+    "pa_vkv_step": (_I, [_P, _I32P, _P]),
+    "pa_vkv_tensor": (_I, [_P, _I, _I, C.POINTER(_P)]),
+    "pa_vkv_slot_tokens": (_I, [_P, _I32P, C.POINTER(_P)]),
+    "pa_vkv_slot_pages": (_I, [_P, _I]),
+    "pa_vkv_get_stats": (_I, [_P, C.POINTER(VkvStats)]),
+    "pa_decode_contiguous": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I, _P]),
+    "pa_reshape_and_cache_slots": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _P, _I, _I, _I, _P]),
+    "pa_vkv_decode": (_I, [_P, _I, _P, _P, _P, _I, _I, _F, _I, _P, _SZ, _P, _P]),
+    "pa_vkv_reshape_and_cache": (_I, [_P, _I, _P, _P, _P, _P, _I, _P]),
     "pa_alloc_enable_swap": (_I, [_P, _I]),
     "pa_alloc_num_free_cpu": (_I, [_P]),
     "pa_alloc_is_swapped": (_I, [_P, _I]),

@@ -47,6 +47,39 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// reshape_and_cache into a contiguous [num_slots][contig_len] cache: token i
+// goes to row slot_ids[i]*contig_len + positions[i].  A negative slot marks
+// padding; a position outside [0, bound) - bound = slot_tokens[slot], the rows
+// of the slot backed by memory, or contig_len - records PA_DEVERR_SLOT and the
+// token is skipped, so no write ever reaches an unmapped page.
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_slots_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                   const int32_t* __restrict__ slot_ids, const int32_t* __restrict__ positions,
+                                   uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int num_tokens,
+                                   int row_vecs, int num_slots, int contig_len,
+                                   const int32_t* __restrict__ slot_tokens, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t total = (int64_t)num_tokens * row_vecs;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tok = i / row_vecs;
+    const int64_t j = i - tok * row_vecs;
+    const int32_t s = __ldg(slot_ids + tok);
+    if (s < 0) continue;  // padding token
+    const int32_t pos = __ldg(positions + tok);
+    const int bound = s < num_slots ? (slot_tokens ? min(__ldg(slot_tokens + s), contig_len) : contig_len) : 0;
+    if (s >= num_slots || pos < 0 || pos >= bound) {
+      if (j == 0) record_error(err, PA_DEVERR_SLOT);
+      continue;
+    }
+    const int64_t row = (int64_t)s * contig_len + pos;
+    const uint4 kv = ld_stream(k + i);
+    const uint4 vv = ld_stream(v + i);
+    k_cache[row * row_vecs + j] = kv;
+    v_cache[row * row_vecs + j] = vv;
+  }
+}
+
 // blockIdx.y strides over pairs; x threads over the block's 16-byte vectors.
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ pairs,
@@ -144,6 +177,21 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
   return launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
                     static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, static_cast<uint4*>(k_cache),
                     static_cast<uint4*>(v_cache), num_tokens, row_vecs, num_slots, err);
+}
+
+cudaError_t launch_reshape_and_cache_slots(const void* k, const void* v, const int32_t* slot_ids,
+                                           const int32_t* positions, int num_tokens, void* k_cache, void* v_cache,
+                                           int num_slots, int contig_len, const int32_t* slot_tokens, int row_bytes,
+                                           int* err, cudaStream_t stream) {
+  const int row_vecs = row_bytes / 16;
+  const int64_t total = (int64_t)num_tokens * row_vecs;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  return launch_pdl(reshape_and_cache_slots_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                    static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_ids, positions,
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, row_vecs, num_slots,
+                    contig_len, slot_tokens, err);
 }
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,

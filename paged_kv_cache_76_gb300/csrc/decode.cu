@@ -30,6 +30,13 @@
 // columns (NT = 4).  Column n stops at token ctx - (q_len-1-i) (causal within
 // the draft); a column with no visible token in a partition keeps m = -inf,
 // l = 0, o = 0, which the merge weighs by zero.
+//
+// Contiguous mode (CONTIG): the cache is one [slots][max_len][Hkv][D] tensor
+// (a vAttention-style virtual tensor, or plain memory) and request r reads
+// slot slot_ids[r]: token t is row slot*max_len + t, one 16-row TMA box per
+// tile, no Block Table.  Only tokens below the slot's mapped bound
+// (slot_tokens[slot], a multiple of 16) are ever loaded; a context past it
+// records PA_DEVERR_CONTEXT_LEN and the rest counts as empty.
 #include <cuda_pipeline.h>
 #include <float.h>
 
@@ -60,7 +67,7 @@ struct DecodeSmem {
   static constexpr int MAX_BYTES = TAB_OFF + WARPS * kMaxTableEntries * 4 + 1024;
 };
 
-template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES>
+template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES, bool CONTIG>
 __global__ void __launch_bounds__(WARPS * 32)
     decode_partial_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const DecodeParams p) {
@@ -97,8 +104,21 @@ __global__ void __launch_bounds__(WARPS * 32)
   int ctx = __ldg(p.lens + r);
   // tokens [tok_begin, ctx) are this kernel's (tok_begin > 0: the suffix
   // after a shared prefix attended elsewhere)
-  const bool bad_len = ctx < p.tok_begin || ctx > cap;
+  bool bad_len = ctx < p.tok_begin || ctx > cap;
   ctx = ctx < p.tok_begin ? p.tok_begin : (ctx > cap ? cap : ctx);
+  // contiguous mode: the slot and the tokens it has backed by memory
+  int slot = 0, mapped = cap;
+  bool bad_slot = false;
+  if constexpr (CONTIG) {
+    slot = p.slot_ids ? __ldg(p.slot_ids + r) : r;
+    if (slot < 0 || slot >= p.num_slots) {
+      bad_slot = true;
+      mapped = 0;
+    } else if (p.slot_tokens) {
+      mapped = min(cap, __ldg(p.slot_tokens + slot) & ~15);
+    }
+    if (ctx > mapped && !bad_slot) bad_len = true;
+  }
   const int nsplit = (ctx - p.tok_begin + p.split_tokens - 1) / p.split_tokens;
   const bool active = c < (nsplit > 0 ? nsplit : (p.always_partial ? 0 : 1));
   const int G = p.group;
@@ -106,26 +126,29 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int qh0 = h * G;
   const int tok0 = p.tok_begin + c * p.split_tokens;
   const int tok1 = min(tok0 + p.split_tokens, ctx);
-  const int ntiles = active && ctx > tok0 ? (tok1 - tok0 + 15) >> 4 : 0;
+  const int load_end = min(tok1, mapped);  // == tok1 unless a contiguous slot is short of memory
+  const int ntiles = active && load_end > tok0 ? (load_end - tok0 + 15) >> 4 : 0;
   const int blk0 = tok0 / p.block_size;
 
   // Set-up that reads only this call's immutable inputs (block table slice,
   // q) overlaps the previous kernel's tail; the cache is read after
   // griddep_wait().
-  bool bad_id = false;
+  bool bad_id = bad_slot;
   uint32_t qf[NT][KSTEPS][2];
   if (ntiles > 0) {
     // Block Table slice of this partition; an out-of-range id is replaced by
     // num_blocks, whose rows lie past the tensor map: TMA then zero-fills.
-    const int nblk = (tok1 - 1) / p.block_size - blk0 + 1;
-    const int32_t* trow = p.tables + (size_t)r * p.maxblk + blk0;
-    for (int i = lane; i < nblk; i += 32) {
-      int b = __ldg(trow + i);
-      if (b < 0 || b >= p.num_blocks) {
-        bad_id = true;
-        b = p.num_blocks;
+    if constexpr (!CONTIG) {
+      const int nblk = (tok1 - 1) / p.block_size - blk0 + 1;
+      const int32_t* trow = p.tables + (size_t)r * p.maxblk + blk0;
+      for (int i = lane; i < nblk; i += 32) {
+        int b = __ldg(trow + i);
+        if (b < 0 || b >= p.num_blocks) {
+          bad_id = true;
+          b = p.num_blocks;
+        }
+        tab[i] = b;
       }
-      tab[i] = b;
     }
     // Q^T as the B operand of S^T = K Q^T: lane holds column (lane/4) of each
     // 8-column n-tile, elements d = 16ks + 2(lane%4) + {0,1} and +8.
@@ -149,7 +172,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   }
   // shared-prefix mode: each table must start with the prefix blocks
-  if (p.prefix_blocks && c == 0 && h == 0) {
+  if (!CONTIG && p.prefix_blocks && c == 0 && h == 0) {
     const int32_t* trow0 = p.tables + (size_t)r * p.maxblk;
     for (int i = lane; i < p.prefix_nblk; i += 32)
       if (__ldg(trow0 + i) != __ldg(p.prefix_blocks + i)) bad_id = true;
@@ -175,7 +198,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   auto issue = [&](int j) {
     const int s = j % STAGES;
     const int ts = tok0 + 16 * j;
-    const int nvalid = min(16, tok1 - ts);
+    const int nvalid = min(16, load_end - ts);
     const int nsub = (nvalid + BSUB - 1) / BSUB;
     const uint32_t bar = smem_u32(&bars[s]);
     const uint32_t kdst = smem_u32(wbase + s * L::STAGE_BYTES);
@@ -189,8 +212,13 @@ __global__ void __launch_bounds__(WARPS * 32)
       const int isv = rem / Tile::NH;
       const int hf = rem % Tile::NH;
       const int tok = ts + sub * BSUB;
-      const int b = tab[tok / p.block_size - blk0];
-      const int row = b * p.block_size + tok % p.block_size;
+      int row;
+      if constexpr (CONTIG) {
+        row = slot * p.contig_len + tok;
+      } else {
+        const int b = tab[tok / p.block_size - blk0];
+        row = b * p.block_size + tok % p.block_size;
+      }
       tma_load_4d_hint(kdst + isv * Tile::BYTES + Tile::box(hf, sub), isv ? &vmap : &kmap, bar, 0, hf, h, row,
                        pol);
     }
@@ -221,7 +249,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int e = 0; e < 2; ++e) {
       const int n = nt * 8 + 2 * (lane & 3) + e;
       const int qi = n < NC ? n / G : p.q_len - 1;
-      lim[nt][e] = min(tok1, ctx - (p.q_len - 1 - qi));
+      lim[nt][e] = min(load_end, ctx - (p.q_len - 1 - qi));
     }
   bool failed = false;
   int j = 0;
@@ -232,7 +260,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       break;
     }
     const int ts = tok0 + 16 * j;
-    const int nvalid = min(16, tok1 - ts);
+    const int nvalid = min(16, load_end - ts);
     uint8_t* kt = wbase + s * L::STAGE_BYTES;
     uint8_t* vt = kt + Tile::BYTES;
     if (nvalid < 16) {
@@ -511,12 +539,12 @@ __global__ void __launch_bounds__(256) lse_merge_warp_kernel(const MergeParams p
   }
 }
 
-template <int D, int BSUB, int NT, typename T>
+template <int D, int BSUB, int NT, typename T, bool CONTIG = false>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                             cudaStream_t stream) {
   constexpr int W = kDecodeWarps, S = kDecodeStages;
   using L = DecodeSmem<D, BSUB, NT, T, W, S>;
-  auto kern = decode_partial_kernel<D, BSUB, NT, T, W, S>;
+  auto kern = decode_partial_kernel<D, BSUB, NT, T, W, S, CONTIG>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -527,7 +555,15 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
   }
   const int units = p.grid_splits * p.kv_heads;
   dim3 grid((units + W - 1) / W, p.num_seqs);
-  return launch_pdl(kern, grid, dim3(W * 32), L::bytes(p.tab_entries), stream, kmap, vmap, p);
+  return launch_pdl(kern, grid, dim3(W * 32), L::bytes(CONTIG ? 0 : p.tab_entries), stream, kmap, vmap, p);
+}
+
+template <int D, typename T>
+cudaError_t launch_decode_contig_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                                   cudaStream_t stream) {
+  if (p.group * p.q_len <= 8) return launch_decode_t<D, 16, 1, T, true>(kmap, vmap, p, stream);
+  if (p.group * p.q_len <= 16) return launch_decode_t<D, 16, 2, T, true>(kmap, vmap, p, stream);
+  return cudaErrorInvalidValue;
 }
 
 template <int D, int BSUB, typename T>
@@ -563,6 +599,17 @@ cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vm
     return dt == PA_BF16 ? launch_decode_bs<64, __nv_bfloat16>(kmap, vmap, p, bsub, stream)
                          : launch_decode_bs<64, __half>(kmap, vmap, p, bsub, stream);
   }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_contig(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                                 int head_dim, pa_dtype dt, cudaStream_t stream) {
+  if (head_dim == 128)
+    return dt == PA_BF16 ? launch_decode_contig_t<128, __nv_bfloat16>(kmap, vmap, p, stream)
+                         : launch_decode_contig_t<128, __half>(kmap, vmap, p, stream);
+  if (head_dim == 64)
+    return dt == PA_BF16 ? launch_decode_contig_t<64, __nv_bfloat16>(kmap, vmap, p, stream)
+                         : launch_decode_contig_t<64, __half>(kmap, vmap, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -422,6 +422,84 @@ int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* c
                         max_blocks_per_seq, block_size, split_tokens, out, dtype, stream);
 }
 
+int pa_decode_contiguous(const void* q, const void* k_cache, const void* v_cache, int num_slots, int max_len,
+                         const int32_t* slot_ids, const int32_t* slot_tokens, const int32_t* context_lens,
+                         int num_seqs, int q_heads, int kv_heads, int head_dim, float scale, int split_tokens,
+                         void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream) {
+  if (num_slots <= 0 || max_len <= 0 || max_len % 16 != 0 || (int64_t)num_slots * max_len > INT32_MAX - 16)
+    return PA_ERR_INVALID;
+  const int maxblk = max_len / 16;
+  int st = check_kv_shape(num_slots * maxblk, 16, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || q_heads <= 0 || q_heads % kv_heads != 0 || q_heads / kv_heads > 16)
+    return PA_ERR_INVALID;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID;
+  DecodeSetup s;
+  st = decode_setup(num_seqs, q_heads, head_dim, maxblk, 16, split_tokens, &s);
+  if (st != PA_OK) return st;
+  if (s.ws.bytes > 0 && (!workspace || workspace_bytes < s.ws.bytes || !aligned16(workspace)))
+    return PA_ERR_WORKSPACE;
+  CUtensorMap km, vm;
+  if (!kv_map(k_cache, num_slots * maxblk, 16, kv_heads, head_dim, dtype, &km) ||
+      !kv_map(v_cache, num_slots * maxblk, 16, kv_heads, head_dim, dtype, &vm))
+    return PA_ERR_CUDA;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  DecodeParams p{};
+  p.q = q;
+  p.lens = context_lens;
+  p.out = out;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.part_o = s.ws.bytes ? reinterpret_cast<float*>(ws + s.ws.o_off) : nullptr;
+  p.part_m = s.ws.bytes ? reinterpret_cast<float*>(ws + s.ws.m_off) : nullptr;
+  p.part_l = s.ws.bytes ? reinterpret_cast<float*>(ws + s.ws.l_off) : nullptr;
+  p.err = err;
+  p.maxblk = maxblk;
+  p.num_seqs = num_seqs;
+  p.q_heads = q_heads;
+  p.kv_heads = kv_heads;
+  p.group = q_heads / kv_heads;
+  p.num_blocks = num_slots * maxblk;
+  p.block_size = 16;
+  p.split_tokens = s.split;
+  p.max_splits = s.max_splits;
+  p.grid_splits = s.max_splits;
+  p.tab_entries = 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_len = 1;
+  p.slot_ids = slot_ids;
+  p.slot_tokens = slot_tokens;
+  p.num_slots = num_slots;
+  p.contig_len = max_len;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  st = cuda_status(launch_decode_contig(km, vm, p, head_dim, dtype, cs));
+  if (st != PA_OK) return st;
+  return lse_merge_impl(workspace, workspace_bytes, context_lens, num_seqs, 1, q_heads, head_dim, maxblk, 16,
+                        split_tokens, out, dtype, stream);
+}
+
+int pa_reshape_and_cache_slots(const void* k, const void* v, const int32_t* slot_ids, const int32_t* positions,
+                               int num_tokens, void* k_cache, void* v_cache, int num_slots, int max_len,
+                               const int32_t* slot_tokens, int kv_heads, int head_dim, pa_dtype dtype,
+                               pa_stream stream) {
+  if (num_slots <= 0 || max_len <= 0 || max_len % 16 != 0 || (int64_t)num_slots * max_len > INT32_MAX - 16)
+    return PA_ERR_INVALID;
+  int st = check_kv_shape(num_slots * (max_len / 16), 16, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_ids || !positions || !k_cache || !v_cache) return PA_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  return cuda_status(launch_reshape_and_cache_slots(k, v, slot_ids, positions, num_tokens, k_cache, v_cache,
+                                                    num_slots, max_len, slot_tokens, kv_heads * head_dim * 2, err,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t pa_verify_workspace_size(int num_seqs, int q_len, int q_heads, int head_dim, int max_blocks_per_seq,
                                 int block_size, int split_tokens) {
   if (num_seqs < 0 || q_len < 1 || q_heads <= 0 || head_dim <= 0) return 0;

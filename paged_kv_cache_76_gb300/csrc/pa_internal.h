@@ -60,6 +60,12 @@ struct DecodeParams {
   // request r is row r*q_len + i of q / out / the partials and sees tokens
   // [0, context_len - (q_len-1-i)).
   int q_len;
+  // Contiguous mode (launch_decode_contig): the cache is [num_slots][contig_len]
+  // rows; request r reads slot slot_ids[r] (r if null); slot_tokens (may be
+  // null) bounds the rows of each slot that are backed by memory.
+  const int32_t* slot_ids;
+  const int32_t* slot_tokens;
+  int num_slots, contig_len;
 };
 
 struct MergeParams {
@@ -112,6 +118,8 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int q_heads, int head_dim,
 cudaError_t launch_decode_partial(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                                   int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_lse_merge(const MergeParams& p, int head_dim, pa_dtype dt, cudaStream_t stream);
+cudaError_t launch_decode_contig(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                                 int head_dim, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_chunked_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
                                    int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
 // tcgen05/TMEM kernel for blocks of >= 8 tokens (bsub >= 8): chunked prefill
@@ -124,6 +132,10 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
                                      cudaStream_t stream);
 // pointers as the kernel dereferences them (host pools through their mapped
 // device addresses); block_bytes = one block of K (or V)
+cudaError_t launch_reshape_and_cache_slots(const void* k, const void* v, const int32_t* slot_ids,
+                                           const int32_t* positions, int num_tokens, void* k_cache, void* v_cache,
+                                           int num_slots, int contig_len, const int32_t* slot_tokens, int row_bytes,
+                                           int* err, cudaStream_t stream);
 cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* pairs,
                                int num_pairs, int num_src, int num_dst, int64_t block_bytes, int* err,
                                cudaStream_t stream);
