@@ -269,6 +269,13 @@ class Step:
             # so that its CTAs take their SMs first; decode (HBM-bound) fills the rest
             self.side = torch.cuda.Stream(device, priority=torch.cuda.Stream.priority_range()[1])
             self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
+        self.prefix_side = None
+        if self.dec and self.prefix_len and overlap_streams:
+            # the shared prefix's tensor-core pass on a second stream, forked at
+            # the start of the step: it reads only q and blocks this step does
+            # not write, and runs beside the HBM-bound suffix decode
+            self.prefix_side = torch.cuda.Stream(device, priority=torch.cuda.Stream.priority_range()[1])
+            self.ev_pfork = torch.cuda.Event()
         self.out_dec = dv.get("dec")
         self.out_pre = dv.get("pre")
         self.h_out_dec = hv.get("dec")
@@ -340,6 +347,9 @@ class Step:
         o, d, wl = self.ops, self.d, self.wl
         if self.layout != "paged":
             return self._run_contiguous(stream, ev)
+        if self.prefix_side is not None:
+            self.ev_pfork.record(stream)
+            self.prefix_side.wait_event(self.ev_pfork)
         if self.n_pairs:
             o.copy_blocks(self.k_cache, self.v_cache, d["pairs"], stream=stream)
         o.reshape_and_cache(d["k_new"], d["v_new"], d["slots"], self.k_cache, self.v_cache, stream=stream)
@@ -365,7 +375,7 @@ class Step:
                 ev[0].record(stream)
             o.decode_shared_prefix(d["q_decode"], self.k_cache, self.v_cache, d["prefix_blocks"], self.prefix_len,
                                    d["dec_tables"], d["dec_lens"], wl.scale, out=self.out_dec, split_tokens=self.split,
-                                   workspace=self.workspace, stream=stream)
+                                   workspace=self.workspace, stream=stream, prefix_stream=self.prefix_side)
             if ev is not None:
                 ev[1].record(stream)
         elif self.dec and wl.q_len > 1:
@@ -743,7 +753,9 @@ def main():
                    f"{total_bytes / 1e6:.1f} MB moved per step)"),
             "parallelism": f"replicas x{ws}",
             "streams": (f"prefill on a second, highest-priority stream over {step.prefill_ctas or 'all'} CTAs, "
-                        f"concurrent with decode" if step.side is not None else "one"),
+                        f"concurrent with decode" if step.side is not None else
+                        "shared-prefix pass on a second, highest-priority stream, concurrent with the suffix decode"
+                        if step.prefix_side is not None else "one"),
         },
         "gpu_launches": int(launches),
         "clocks": clk,

@@ -331,7 +331,7 @@ int pa_vkv_reshape_and_cache(const pa_vkv* v, int layer, const void* k, const vo
  * physical blocks of a common prefix.  Instead of reading those blocks once per
  * request, this call attends the prefix once for every request's queries:
  * rows (request, query head of the group) x prefix keys are dense tiles for the
- * 5th-generation tensor cores, split into key ranges of 512 tokens, each
+ * 5th-generation tensor cores, split into key ranges (512 tokens), each
  * producing a log-sum-exp partial; each request's own suffix (tokens
  * prefix_len .. context_lens[r]-1) runs through the paged decode kernel into
  * further partials; the merge combines them.  The result equals pa_decode
@@ -345,7 +345,18 @@ int pa_vkv_reshape_and_cache(const pa_vkv* v, int layer, const void* k, const vo
  *                  PA_DEVERR_CONTEXT_LEN).  pa_alloc_common_prefix gives the
  *                  number of shared full blocks of a set of sequences.
  *   workspace      at least pa_decode_shared_prefix_workspace_size(...) bytes.
- * Other arguments as pa_decode.  With 4-token blocks this is pa_decode.
+ *   prefix_stream  NULL (or == stream): all three passes run on `stream`.
+ *                  Otherwise the prefix pass runs on prefix_stream, with NO
+ *                  dependency on `stream`, concurrently with the suffix pass
+ *                  (the prefix pass is tensor-core work on a few SMs, the
+ *                  suffix pass HBM-bound on the rest); the merge on `stream`
+ *                  waits for it.  The caller orders prefix_stream after every
+ *                  write of q, prefix_blocks and the prefix's K/V, and after
+ *                  every earlier use of the workspace.  In this mode the
+ *                  prefix key ranges grow (512 x 2^k tokens) until the prefix
+ *                  pass needs at most half of the SMs.
+ * Other arguments as pa_decode.  With 4-token blocks this is pa_decode (on
+ * `stream`).
  * ------------------------------------------------------------------------- */
 size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq,
                                               int block_size, int prefix_len, int split_tokens);
@@ -361,7 +372,8 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
                             int prefix_len, const int32_t* block_tables, int max_blocks_per_seq,
                             const int32_t* context_lens, int num_seqs, int q_heads, int kv_heads, int head_dim,
                             int block_size, int num_blocks, float scale, int split_tokens, void* workspace,
-                            size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream);
+                            size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream,
+                            pa_stream prefix_stream);
 
 /* ----------------------------------------------------------------------------
  * pa_chunked_prefill - a chunk of prompt tokens per request attends its paged

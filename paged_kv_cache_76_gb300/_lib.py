@@ -86,7 +86,7 @@ PROTOTYPES = {
     "pa_decode_shared_prefix_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "pa_decode_shared_prefix_split_tokens": (_I, [_I, _I, _I, _I]),
     "pa_decode_shared_prefix": (_I, [_P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I,
-                                     _P]),
+                                     _P, _P]),
     "pa_get_device_error": (_I, [_I32P, _P]),
     "pa_alloc_create": (_I, [_I, _I, _I32P, C.POINTER(_P)]),
     "pa_alloc_destroy": (None, [_P]),

@@ -216,8 +216,12 @@ def decode_shared_prefix_split_tokens(max_blocks_per_seq, block_size, prefix_len
 
 
 def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_tables, context_lens, scale, out=None,
-                         split_tokens=0, workspace=None, stream=None):
-    """pa_decode_shared_prefix: decode whose requests share ``prefix_blocks`` (int32, device)."""
+                         split_tokens=0, workspace=None, stream=None, prefix_stream=None):
+    """pa_decode_shared_prefix: decode whose requests share ``prefix_blocks`` (int32, device).
+
+    ``prefix_stream`` (a torch.cuda.Stream): run the prefix pass there,
+    concurrently with the suffix pass; the caller orders it after the writes
+    of ``q``, the prefix's K/V and the previous use of ``workspace``."""
     nb, bs, hkv, d = _cache_dims(k_cache)
     B, hq, dq = q.shape
     if dq != d or block_tables.shape[0] != B or context_lens.shape[0] != B:
@@ -232,7 +236,8 @@ def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_t
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(prefix_blocks, "prefix_blocks"),
         int(prefix_len), _i32(block_tables, "block_tables"), maxblk, _i32(context_lens, "context_lens"), B, hq, hkv,
         d, bs, nb, float(scale), int(split_tokens), workspace.data_ptr(), workspace.numel(), _dev(out, "out"),
-        dtype_code(q.dtype), _stream(stream)), "pa_decode_shared_prefix")
+        dtype_code(q.dtype), _stream(stream), prefix_stream.cuda_stream if prefix_stream is not None else None),
+        "pa_decode_shared_prefix")
     return out
 
 

@@ -99,3 +99,42 @@ def test_four_token_blocks_fall_back_to_decode():
     dev = DeviceStep(wl, W.make_values(wl))
     out, _ = _run(dev)
     assert torch.equal(out, dev.out_decode)
+
+
+def _concurrent(dev, pb, plen):
+    """The prefix pass on a second stream forked from the current one (the
+    caller's ordering duty: q and the prefix K/V are written before the fork)."""
+    from paged_kv_cache_76_gb300 import ops
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream(priority=torch.cuda.Stream.priority_range()[1])
+    side.wait_stream(main)
+    out = ops.decode_shared_prefix(dev.q_decode, dev.k_cache, dev.v_cache, pb, plen, dev.dec_tables, dev.dec_lens,
+                                   dev.wl.scale, prefix_stream=side)
+    torch.cuda.synchronize()
+    assert ops.get_device_error() == 0
+    return out
+
+
+def test_concurrent_prefix_pass_with_the_same_key_ranges_is_bitwise_the_same():
+    # 24 requests x 4 heads: one pair of row tiles per KV head, so 512-token
+    # ranges already fit in half of the SMs and the partials are the same
+    wl = W.prefix_shared_cow_decode(batch=24, prefix_tokens=16 * 64, suffix_lo=1, suffix_hi=300, cow_frac=0.25)
+    vals = W.make_values(wl)
+    dev = DeviceStep(wl, vals)
+    out, plen = _run(dev)
+    pb, _ = _shared(dev)
+    assert torch.equal(_concurrent(dev, pb, plen), out)
+
+
+def test_concurrent_prefix_pass_at_full_size_matches_the_oracle():
+    wl = W.prefix_shared_cow_decode()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    dev.run()
+    pb, plen = _shared(dev)
+    out = _concurrent(dev, pb, plen)
+    rows = list(range(0, 256, 16))
+    ref = oracle_step(wl, vals, decode_rows=rows, compact=True)["decode"]
+    assert_close(out[rows], ref, "concurrent shared prefix")
+    # every row against pa_decode on the full tables (two bf16 roundings apart)
+    assert float(np.abs(to_f64(out) - to_f64(dev.out_decode)).mean()) < 1e-3
