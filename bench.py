@@ -63,6 +63,20 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(x: float, ws: int, device) -> float:
+    """The largest x over all ranks (x itself on one rank): the slowest replica sets the time."""
+    if ws == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: float, steps: int, seconds: float, ws: int) -> float:
+    """Weak scaling: every rank moves the same bytes per step; all ranks' bytes over the max time."""
+    return ws * bytes_per_rank_step * steps / seconds / 1e9
+
+
 def measured_tensor_peak():
     """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed alone)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -653,10 +667,7 @@ def main():
     ms = t_start.elapsed_time(t_end) if flush is None else sum(a.elapsed_time(b) for a, b in pairs)
     if ops.get_device_error(stream) != 0:
         raise RuntimeError("device error recorded during the timed region")
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = reduce_max(ms, ws, device)
     ms_per_step = ms / args.steps
 
     # Dominant kernel: the same K steps again, each decode-partial launch
@@ -712,13 +723,10 @@ def main():
                 step.run_e2e(stream)
             stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=device)
-    if ws > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_s = float(te.item())
-    e2e_val = ws * total_bytes * args.e2e_steps / e2e_s / 1e9
+    e2e_s = reduce_max(e2e_s, ws, device)
+    e2e_val = whole_job_gbs(total_bytes, args.e2e_steps, e2e_s, ws)
 
-    value = ws * total_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(total_bytes, args.steps, ms * 1e-3, ws)
     n_dec = len(wl.decode_seqs)
     res = {
         "metric": METRIC,
