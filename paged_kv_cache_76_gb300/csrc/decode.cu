@@ -27,9 +27,15 @@
 //
 // Speculative verify (q_len = k+1 queries per request): the n-tile columns are
 // the group's heads of each query, column n = i*group + head, up to 32
-// columns (NT = 4).  Column n stops at token ctx - (q_len-1-i) (causal within
-// the draft); a column with no visible token in a partition keeps m = -inf,
-// l = 0, o = 0, which the merge weighs by zero.
+// columns.  Up to 16 columns one warp holds them (NT = 1 or 2); 17..32
+// columns are split over two warps that share the unit's TMA ring (the first
+// issues the loads, an "empty" barrier per stage counts both warps out before
+// the stage is refilled), which keeps every warp at NT = 2 and 168 registers.
+// Column n stops at token ctx - (q_len-1-i) (causal within the draft); a
+// column with no visible token in a partition keeps m = -inf, l = 0, o = 0,
+// which the merge weighs by zero.  Per column the arithmetic is the same
+// whatever the split, so each query's result equals decode over its visible
+// prefix bit for bit.
 //
 // Contiguous mode (CONTIG): the cache is one [slots][max_len][Hkv][D] tensor
 // (a vAttention-style virtual tensor, or plain memory) and request r reads
@@ -55,24 +61,29 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES>
+// One ring of STAGES K+V tiles per unit; a unit is one warp, or CW > 1 warps
+// that split the unit's query columns (NT*8 each) and share its tiles.
+template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES, int CW>
 struct DecodeSmem {
   using Tile = KvTile<D, BSUB, 16>;
+  static constexpr int UNITS = WARPS / CW;
+  static constexpr int NBARS = CW > 1 ? 2 * STAGES : STAGES;  // full (+ empty) per stage
   static constexpr int STAGE_BYTES = 2 * Tile::BYTES;  // K tile then V tile
   static constexpr int WARP_BYTES = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = WARPS * WARP_BYTES;
-  static constexpr int TAB_OFF = BAR_OFF + WARPS * STAGES * 8;
-  // dynamic bytes for `entries` table entries per warp, + alignment slack
-  static constexpr int bytes(int entries) { return TAB_OFF + WARPS * entries * 4 + 1024; }
-  static constexpr int MAX_BYTES = TAB_OFF + WARPS * kMaxTableEntries * 4 + 1024;
+  static constexpr int BAR_OFF = UNITS * WARP_BYTES;
+  static constexpr int TAB_OFF = BAR_OFF + UNITS * NBARS * 8;
+  // dynamic bytes for `entries` table entries per unit, + alignment slack
+  static constexpr int bytes(int entries) { return TAB_OFF + UNITS * entries * 4 + 1024; }
+  static constexpr int MAX_BYTES = TAB_OFF + UNITS * kMaxTableEntries * 4 + 1024;
 };
 
-template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES, bool CONTIG>
+template <int D, int BSUB, int NT, typename T, int WARPS, int STAGES, bool CONTIG, int CW>
 __global__ void __launch_bounds__(WARPS * 32)
     decode_partial_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const DecodeParams p) {
-  using L = DecodeSmem<D, BSUB, NT, T, WARPS, STAGES>;
+  using L = DecodeSmem<D, BSUB, NT, T, WARPS, STAGES, CW>;
   using Tile = typename L::Tile;
+  constexpr bool PAIR = CW > 1;  // several warps per unit
   constexpr int KSTEPS = D / 16;
   constexpr int LOADS = Tile::NH * 2;  // TMA boxes per sub-block: halves x {K, V}
 
@@ -80,13 +91,23 @@ __global__ void __launch_bounds__(WARPS * 32)
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  uint8_t* wbase = smem + warp * L::WARP_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + warp * STAGES;
-  int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF) + warp * p.tab_entries;
+  // CW > 1: warps CW*k .. CW*k+CW-1 share unit k's ring; the first issues the
+  // loads, warp CW*k+i takes query columns [i*NT*8, (i+1)*NT*8)
+  const int uw = warp / CW;
+  const int half = warp % CW;
+  const bool issuer = half == 0;
+  const int col0 = half * NT * 8;
+  uint8_t* wbase = smem + uw * L::WARP_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF) + uw * L::NBARS;
+  uint64_t* empty = bars + STAGES;  // CW > 1 only: every warp of the unit has consumed the stage
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF) + uw * p.tab_entries;
 
-  if (lane == 0) {
+  if (lane == 0 && issuer) {
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);
+      if constexpr (PAIR) mbar_init(smem_u32(&empty[s]), CW);
+    }
     fence_mbar_init();
   }
   if (threadIdx.x == 0) {
@@ -97,7 +118,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   griddep_launch_dependents();
 
   const int r = blockIdx.y;
-  const int u = blockIdx.x * WARPS + warp;
+  const int u = blockIdx.x * L::UNITS + uw;
   const int h = u % p.kv_heads;
   const int c = u / p.kv_heads;
   const int cap = p.maxblk * p.block_size;
@@ -138,7 +159,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   if (ntiles > 0) {
     // Block Table slice of this partition; an out-of-range id is replaced by
     // num_blocks, whose rows lie past the tensor map: TMA then zero-fills.
-    if constexpr (!CONTIG) {
+    if (!CONTIG && issuer) {
       const int nblk = (tok1 - 1) / p.block_size - blk0 + 1;
       const int32_t* trow = p.tables + (size_t)r * p.maxblk + blk0;
       for (int i = lane; i < nblk; i += 32) {
@@ -154,7 +175,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     // 8-column n-tile, elements d = 16ks + 2(lane%4) + {0,1} and +8.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int n = nt * 8 + (lane >> 2);
+      const int n = col0 + nt * 8 + (lane >> 2);
       const int qi = n < NC ? n / G : 0;
       const T* qb = reinterpret_cast<const T*>(p.q) +
                     ((size_t)(r * p.q_len + qi) * p.q_heads + qh0 + (n - qi * G)) * D;
@@ -172,7 +193,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
   }
   // shared-prefix mode: each table must start with the prefix blocks
-  if (!CONTIG && p.prefix_blocks && c == 0 && h == 0) {
+  if (!CONTIG && issuer && p.prefix_blocks && c == 0 && h == 0) {
     const int32_t* trow0 = p.tables + (size_t)r * p.maxblk;
     for (int i = lane; i < p.prefix_nblk; i += 32)
       if (__ldg(trow0 + i) != __ldg(p.prefix_blocks + i)) bad_id = true;
@@ -188,8 +209,9 @@ __global__ void __launch_bounds__(WARPS * 32)
     const int qi = n / G;
     return (size_t)(r * p.q_len + qi) * p.q_heads + qh0 + (n - qi * G);
   };
-  if (ctx == 0) {
-    for (int i = lane; i < NC * D; i += 32) out[row_of(i / D) * D + i % D] = Elem<T>::from(0.f);
+  if (ctx == 0) {  // this warp's columns get zero rows
+    const int ncw = max(0, min(NC - col0, NT * 8));
+    for (int i = lane; i < ncw * D; i += 32) out[row_of(col0 + i / D) * D + i % D] = Elem<T>::from(0.f);
     return;
   }
   __syncwarp();
@@ -235,7 +257,8 @@ __global__ void __launch_bounds__(WARPS * 32)
   }
 
   const int npro = ntiles < STAGES ? ntiles : STAGES;
-  for (int j = 0; j < npro; ++j) issue(j);
+  if (issuer)
+    for (int j = 0; j < npro; ++j) issue(j);
 
   const float sl2 = p.scale_log2;
   const int mi = lane >> 3, rr = lane & 7;
@@ -247,7 +270,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int n = nt * 8 + 2 * (lane & 3) + e;
+      const int n = col0 + nt * 8 + 2 * (lane & 3) + e;
       const int qi = n < NC ? n / G : p.q_len - 1;
       lim[nt][e] = min(load_end, ctx - (p.q_len - 1 - qi));
     }
@@ -333,13 +356,27 @@ __global__ void __launch_bounds__(WARPS * 32)
       for (int nt = 0; nt < NT; ++nt) mma_16816<T>(acc[nt][mt], a, pb0[nt], pb1[nt]);
     }
     __syncwarp();
-    if (j + STAGES < ntiles) issue(j + STAGES);
+    if constexpr (PAIR) {
+      // the stage is refilled once both warps of the pair are done with it
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      if (issuer && j + STAGES < ntiles) {
+        if (!mbar_wait(smem_u32(&empty[s]), (j / STAGES) & 1)) {
+          failed = true;
+          break;
+        }
+        issue(j + STAGES);
+      }
+    } else {
+      if (j + STAGES < ntiles) issue(j + STAGES);
+    }
   }
 
   if (failed) {
     if (lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
-    // drain this warp's loads still in flight (bounded) before leaving
-    for (int k = j + 1; k < ntiles && k < j + STAGES; ++k) mbar_wait(smem_u32(&bars[k % STAGES]), (k / STAGES) & 1);
+    // the issuing warp drains its loads still in flight (bounded) before leaving
+    if (issuer)
+      for (int k = j + 1; k < ntiles && k < j + STAGES; ++k)
+        mbar_wait(smem_u32(&bars[k % STAGES]), (k / STAGES) & 1);
     return;
   }
 
@@ -360,7 +397,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int n = nt * 8 + 2 * (lane & 3) + e;
+        const int n = col0 + nt * 8 + 2 * (lane & 3) + e;
         if (n < NC) {
           const float inv = lp[nt][e] > 0.f ? 1.f / lp[nt][e] : 0.f;
           T* o = out + row_of(n) * D;
@@ -376,7 +413,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int n = nt * 8 + 2 * (lane & 3) + e;
+        const int n = col0 + nt * 8 + 2 * (lane & 3) + e;
         if (n < NC) {
           const size_t row = row_of(n);
           const int slot = p.slot_base + c;
@@ -539,12 +576,12 @@ __global__ void __launch_bounds__(256) lse_merge_warp_kernel(const MergeParams p
   }
 }
 
-template <int D, int BSUB, int NT, typename T, bool CONTIG = false>
+template <int D, int BSUB, int NT, typename T, bool CONTIG = false, int CW = 1>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                             cudaStream_t stream) {
   constexpr int W = kDecodeWarps, S = kDecodeStages;
-  using L = DecodeSmem<D, BSUB, NT, T, W, S>;
-  auto kern = decode_partial_kernel<D, BSUB, NT, T, W, S, CONTIG>;
+  using L = DecodeSmem<D, BSUB, NT, T, W, S, CW>;
+  auto kern = decode_partial_kernel<D, BSUB, NT, T, W, S, CONTIG, CW>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -554,7 +591,7 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
     attr_set[dev] = true;
   }
   const int units = p.grid_splits * p.kv_heads;
-  dim3 grid((units + W - 1) / W, p.num_seqs);
+  dim3 grid((units + L::UNITS - 1) / L::UNITS, p.num_seqs);
   return launch_pdl(kern, grid, dim3(W * 32), L::bytes(CONTIG ? 0 : p.tab_entries), stream, kmap, vmap, p);
 }
 
@@ -572,7 +609,13 @@ cudaError_t launch_decode_nt(const CUtensorMap& kmap, const CUtensorMap& vmap, c
   const int cols = p.group * p.q_len;
   if (cols <= 8) return launch_decode_t<D, BSUB, 1, T>(kmap, vmap, p, stream);
   if (cols <= 16) return launch_decode_t<D, BSUB, 2, T>(kmap, vmap, p, stream);
-  if (cols <= 32) return launch_decode_t<D, BSUB, 4, T>(kmap, vmap, p, stream);
+  // 17..32 columns: two warps per unit, 16 columns each, sharing its tiles.
+  // Measured on GB300 (k = 7 drafts, 32 columns, spec_verify_decode shape):
+  // one warp with 32 columns (255 registers, spills) 152.6 us per step; two
+  // warps x 16 columns 140.5 us (4 stages: 141.4); four warps x 8 columns
+  // (4 stages, 93 registers, 5 CTAs per SM) 148.7 us - each warp re-reads
+  // the K/V tile from shared memory for its own columns.
+  if (cols <= 32) return launch_decode_t<D, BSUB, 2, T, false, 2>(kmap, vmap, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -182,6 +182,11 @@ def spec_verify_decode(seed: int = 0, batch: int = 64, len_lo: int = 512, len_hi
     return wl
 
 
+def _renamed(wl: Workload, name: str) -> Workload:
+    wl.name = name
+    return wl
+
+
 def long_context_splitk_decode(seed: int = 0, batch: int = 8, len_lo: int = 32768,
                                len_hi: int = 131072) -> Workload:
     """Batch 8, 64 q heads / 8 KV heads, D=128, bs=16, lens U{32768..131072}, 512-token splits."""
@@ -296,6 +301,7 @@ WORKLOADS = {
     "llama8b_gqa_decode": llama8b_gqa_decode,
     "long_context_splitk_decode": long_context_splitk_decode,
     "spec_verify_decode": spec_verify_decode,
+    "spec_verify_decode_k7": lambda seed=0: _renamed(spec_verify_decode(seed, k=7), "spec_verify_decode_k7"),
     "prefix_shared_cow_decode": prefix_shared_cow_decode,
     "mixed_prefill_decode": mixed_prefill_decode,
     "mixed_prefill_part": mixed_prefill_part,
