@@ -290,6 +290,19 @@ class Step:
             # not write, and runs beside the HBM-bound suffix decode
             self.prefix_side = torch.cuda.Stream(device, priority=torch.cuda.Stream.priority_range()[1])
             self.ev_pfork = torch.cuda.Event()
+        # a second set of staging buffers: the end-to-end loop keeps two steps
+        # in flight (the host launches step i+1 before it reads step i's result)
+        self._sets = [dict(h_stage=self.h_stage, d_stage=self.d_stage, d=self.d, d_out=self.d_out,
+                           h_outbuf=self.h_outbuf, out_dec=dv.get("dec"), out_pre=dv.get("pre"))]
+        h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        h2.copy_(self.h_stage)
+        d2 = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        d2.copy_(h2)
+        o2 = torch.empty(obytes, dtype=torch.uint8, device=device)
+        dv2 = views(o2, ooffs, outs)
+        self._sets.append(dict(h_stage=h2, d_stage=d2, d=views(d2, offs, self.h), d_out=o2,
+                               h_outbuf=torch.empty(obytes, dtype=torch.uint8).pin_memory(), out_dec=dv2.get("dec"),
+                               out_pre=dv2.get("pre")))
         self.out_dec = dv.get("dec")
         self.out_pre = dv.get("pre")
         self.h_out_dec = hv.get("dec")
@@ -442,6 +455,11 @@ class Step:
         cap = int(round(1.25 * sms * t_pre / max(t_dec, 1e-6)))
         self.prefill_ctas = max(max(1, sms // 8), min(sms // 2, cap))
         return self.prefill_ctas
+
+    def select(self, k: int):
+        """Use staging buffer set k (0 or 1) for the following steps."""
+        for name, val in self._sets[k].items():
+            setattr(self, name, val)
 
     def run_e2e(self, stream):
         """Host buffers in, host buffers out: one copy each way inside the step."""
@@ -685,44 +703,82 @@ def main():
         stream.synchronize()
         dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
 
-    # e2e: host buffers through the public API.  One step = H2D copy of the
-    # step's inputs (one pinned buffer) -> kernels -> D2H copy of its outputs,
-    # captured once as a CUDA graph and replayed with a host sync per step.
+    # e2e: host buffers through the public API.  Every step copies its inputs
+    # from pinned host memory (one buffer), runs the kernels (a CUDA graph per
+    # staging-buffer set) and copies its outputs back, and the host reads
+    # them.  The copies run on two copy streams, so step i+1's inputs go up
+    # and step i-1's outputs come down while step i computes; two buffer sets
+    # alternate, each reused only after the host has read its outputs.
     e2e_val = None
     h2d, d2h = step.e2e_bytes()
-    e2e_mode = "cuda graph (H2D + step + D2H), host sync per step"
-    graph = None
+    e2e_mode = ("H2D copy stream -> kernels (CUDA graph) -> D2H copy stream per step; copies overlap the "
+                "neighbouring steps' kernels; the host reads every step's outputs")
+    graphs = None
     with torch.cuda.stream(stream):
-        for _ in range(3):
+        for k in (0, 1, 0):
+            step.select(k)
             step.run_e2e(stream)
     stream.synchronize()
     eager_out = step.h_outbuf.clone()  # the eager step's outputs, for checking a replay
     try:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step.run_e2e(stream)
-        step.h_outbuf.zero_()
-        with torch.cuda.stream(stream):
-            graph.replay()  # replays on the current stream
-        stream.synchronize()
-        if ops.get_device_error(stream) != 0:
-            raise RuntimeError("device error in graph replay")
-        if not torch.equal(step.h_outbuf[:step.out_used], eager_out[:step.out_used]):
-            raise RuntimeError("graph replay output differs from the eager step")
+        graphs = []
+        for k in (0, 1):
+            step.select(k)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step.run(stream)
+            graphs.append(g)
+        for k in (0, 1):
+            step.select(k)
+            step.d_out.zero_()
+            with torch.cuda.stream(stream):
+                graphs[k].replay()  # replays on the current stream
+            stream.synchronize()
+            step.h_outbuf.copy_(step.d_out)
+            if ops.get_device_error(stream) != 0:
+                raise RuntimeError("device error in graph replay")
+            if not torch.equal(step.h_outbuf[:step.out_used], eager_out[:step.out_used]):
+                raise RuntimeError("graph replay output differs from the eager step")
     except Exception as exc:  # capture not possible here: eager launches instead
-        graph = None
-        e2e_mode = f"eager launches, host sync per step (graph capture not used: {exc})"
+        graphs = None
+        e2e_mode = f"eager kernel launches, copies on two copy streams (graph capture not used: {exc})"
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("up", "kern", "down")}
+    checksum = 0.0
+    sets = step._sets
     if ws > 1:
         torch.distributed.barrier()
+    torch.cuda.synchronize()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(args.e2e_steps):
-            if graph is not None:
-                graph.replay()
+    for i in range(args.e2e_steps):
+        k = i & 1
+        b = sets[k]
+        if i >= 2:
+            up.wait_event(ev["kern"][k])  # step i-2's kernels are done with this input buffer
+        with torch.cuda.stream(up):
+            b["d_stage"].copy_(b["h_stage"], non_blocking=True)
+        ev["up"][k].record(up)
+        stream.wait_event(ev["up"][k])
+        if i >= 2:
+            stream.wait_event(ev["down"][k])  # step i-2's outputs have left this output buffer
+        step.select(k)
+        with torch.cuda.stream(stream):
+            if graphs is not None:
+                graphs[k].replay()
             else:
-                step.run_e2e(stream)
-            stream.synchronize()
+                step.run(stream)
+        ev["kern"][k].record(stream)
+        down.wait_event(ev["kern"][k])
+        with torch.cuda.stream(down):
+            b["h_outbuf"].copy_(b["d_out"], non_blocking=True)
+        ev["down"][k].record(down)
+        if i >= 1:  # the previous step's outputs, now in pinned host memory
+            ev["down"][k ^ 1].synchronize()
+            checksum += float(sets[k ^ 1]["h_outbuf"][:16].float().sum())
+    ev["down"][(args.e2e_steps - 1) & 1].synchronize()
+    checksum += float(sets[(args.e2e_steps - 1) & 1]["h_outbuf"][:16].float().sum())
     e2e_s = time.perf_counter() - t0
+    step.select(0)
     e2e_s = reduce_max(e2e_s, ws, device)
     e2e_val = whole_job_gbs(total_bytes, args.e2e_steps, e2e_s, ws)
 
