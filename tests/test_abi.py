@@ -76,3 +76,31 @@ def test_device_calls_reject_bad_arguments_before_launching(lib):
     # misaligned device pointer
     assert lib.pa_decode(17, 16, 16, 16, 4, 16, 1, 8, 2, 128, 16, 4, 0.1, 0, None, 0, 16, 1,
                          None) == _lib.PA_ERR_INVALID
+
+
+def test_newer_calls_reject_bad_arguments_before_touching_the_gpu(lib):
+    inv = _lib.PA_ERR_INVALID
+    # swap: bad head_dim / dtype, negative pair count; zero pairs is a no-op
+    assert lib.pa_swap_blocks(None, None, None, None, None, 1, 4, 4, 16, 1, 96, 1, None) == inv
+    assert lib.pa_swap_blocks(None, None, None, None, None, 1, 4, 4, 16, 1, 64, 9, None) == _lib.PA_ERR_DTYPE
+    assert lib.pa_swap_blocks(None, None, None, None, None, -1, 4, 4, 16, 1, 64, 1, None) == inv
+    assert lib.pa_swap_blocks(None, None, None, None, None, 0, 4, 4, 16, 1, 64, 1, None) == _lib.PA_OK
+    # verify: q_len < 1, or more than 32 (query, group head) columns per KV head
+    args = (16, 16, 16, 16, 8, 16, 1)
+    assert lib.pa_verify_decode(*args, 0, 8, 2, 128, 16, 4, 0.1, 0, None, 0, 16, 1, None) == inv
+    assert lib.pa_verify_decode(*args, 9, 8, 2, 128, 16, 4, 0.1, 0, None, 0, 16, 1, None) == inv   # 4 x 9 = 36
+    assert lib.pa_verify_workspace_size(4, 0, 8, 128, 8, 16, 0) == 0
+    n1 = lib.pa_verify_workspace_size(4, 1, 8, 128, 64, 16, 128)
+    assert n1 > 0 and lib.pa_verify_workspace_size(4, 3, 8, 128, 64, 16, 128) >= 3 * n1 - 2048
+    # contiguous decode / slot writes: max_len not a multiple of 16, no slots
+    assert lib.pa_decode_contiguous(16, 16, 16, 4, 100, None, None, 16, 1, 8, 2, 128, 0.1, 0, None, 0, 16, 1,
+                                    None) == inv
+    assert lib.pa_decode_contiguous(16, 16, 16, 0, 128, None, None, 16, 1, 8, 2, 128, 0.1, 0, None, 0, 16, 1,
+                                    None) == inv
+    assert lib.pa_reshape_and_cache_slots(None, None, None, None, 1, None, None, 4, 100, None, 2, 128, 1,
+                                          None) == inv
+    assert lib.pa_reshape_and_cache_slots(None, None, None, None, 0, None, None, 4, 128, None, 2, 128, 1,
+                                          None) == _lib.PA_OK
+    # shared prefix: prefix not a multiple of the block size
+    assert lib.pa_decode_shared_prefix(16, 16, 16, 16, 20, 16, 8, 16, 2, 8, 2, 128, 16, 64, 0.1, 0, 16, 1 << 20,
+                                       16, 1, None, None) == inv
