@@ -107,3 +107,25 @@ def test_mixed_prefill_decode_full_size():
     assert_close(dev.out_decode[dec_rows], ref["decode"], "mixed decode sampled")
     assert_close(dev.out_prefill[pre_rows], ref["prefill"][pre_rows], "mixed prefill sampled")
     _no_err()
+
+
+def test_mixed_step_as_the_bench_launches_it_equals_the_single_stream_step():
+    """bench.py's mixed step: the prefill on a second, highest-priority stream
+    over a capped set of persistent CTAs, beside the decode.  Every unit
+    computes exactly as with one CTA per unit on one stream, so the outputs
+    are the same bits."""
+    import bench
+    wl = W.mixed_prefill_decode()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    dev.run()
+    step = bench.Step(wl, torch.device("cuda", 0), value_seed=wl.seed)
+    assert step.side is not None
+    step.prefill_ctas = 57
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step.run(s)
+    s.synchronize()
+    assert torch.equal(step.out_pre, dev.out_prefill)
+    assert torch.equal(step.out_dec, dev.out_decode)
+    _no_err()
