@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_QFULL), 4);
     mbar_init(bar(B_QFULL + 1), 4);
-    mbar_init(bar(B_MMADONE), 2);
+    mbar_init(bar(B_MMADONE), 4);  // two S issuers + two softmax groups (P.V)
     fence_mbar_init();
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
@@ -258,9 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int x = warp;
       bool ok = true;
-      const uint32_t kbase = smem_u32(smem + L::K_OFF), vbase = smem_u32(smem + L::V_OFF);
+      const uint32_t kbase = smem_u32(smem + L::K_OFF);
       const uint32_t qa = smem_u32(smem + L::Q_OFF + x * L::QTILE);
-      const uint32_t sd = tmem + S_COL + x * kKeys, od = tmem + O_COL + x * D;
+      const uint32_t sd = tmem + S_COL + x * kKeys;
       int gt = 0, nu = 0;  // key tiles and units processed by this CTA
       for (int u = cta0; ok && u < nunits; u += nctas) {
         TcUnit w;
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (x == 1 && nu == 0 && !mbar_wait(bar(B_PLO), 0)) { ok = false; break; }
         ++nu;
         for (int j = 0; ok && j < w.ntiles; ++j, ++gt) {
-          const int sk = gt % kKStages, sv = gt % kVStages;
+          const int sk = gt % kKStages;
           // S_x(j) = Q_x K_j^T.  It overwrites P_x(j-1): wait for P.V_x(j-1).
           if (!mbar_wait(bar(B_KFULL + sk), (gt / kKStages) & 1)) { ok = false; break; }
           if (j > 0 && !mbar_wait(bar(B_OFULL + x), (gt - 1) & 1)) { ok = false; break; }
@@ -294,24 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(bar(B_SFULL + x));
           tc_commit(bar(B_KEMPTY + sk));  // this issuer is done with K_j
-          // O_x += P_x(j) V_j in two halves of 64 keys, each as soon as its P
-          // half is in TMEM
-          if (!mbar_wait(bar(B_VFULL + sv), (gt / kVStages) & 1)) { ok = false; break; }
-          const uint32_t vb = vbase + sv * Tile::BYTES;
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            if (!mbar_wait(bar((hh ? B_PHI : B_PLO) + x), gt & 1)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int k4 = 0; k4 < PSTEPS / 2; ++k4) {
-              // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
-              const int kk = hh * (PSTEPS / 2) + k4;
-              const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
-              tc_mma_f16_ts(od, sd + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          if (!ok) break;
-          tc_commit(bar(B_OFULL + x));
-          tc_commit(bar(B_VEMPTY + sv));  // this issuer is done with V_j
+          // O_x += P_x(j) V_j is issued by tile x's softmax group itself
         }
       }
       if (!ok) record_error(p.err, PA_DEVERR_TIMEOUT);
@@ -328,6 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t scol = tmem + lane_addr + S_COL + x * kKeys;
     const uint32_t ocol = tmem + lane_addr + O_COL + x * D;
     uint8_t* qt = smem + L::Q_OFF + x * L::QTILE;
+    // The group's first thread issues the group's P.V MMAs: the named barrier
+    // 1 + x (the group's 128 threads, with an AND vote that keeps every exit
+    // uniform) replaces a hand-off to another warp.
+    const bool leader = quarter == 0 && lane == 0;
+    const uint32_t sd0 = tmem + S_COL + x * kKeys, od0 = tmem + O_COL + x * D;
+    const uint32_t vbase = smem_u32(smem + L::V_OFF);
+    bool lok = true;  // leader: every V wait succeeded
     bool ok = true;
     int gt = 0;  // key tiles processed by this CTA
     for (int u = cta0; ok && u < nunits; u += nctas) {
@@ -355,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float m = -INFINITY, l = 0.f;  // running (possibly stale) max in log2 units, row sum
       for (int j = 0; j < w.ntiles; ++j, ++gt) {
-        if (!mbar_wait(bar(B_SFULL + x), gt & 1)) { ok = false; break; }
+        const bool sfull = mbar_wait(bar(B_SFULL + x), gt & 1);
+        if (!bar_red_and(1 + x, 128, sfull)) { ok = false; break; }  // the group stops together
         tc_fence_after();
         const int ts = w.k0 + j * kKeys;
         const int nvis = lim - ts + 1;  // keys of this tile the row may see (<= 0: none)
@@ -396,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // runs in four packed-pair chains.
         float sx[4] = {0.f, 0.f, 0.f, 0.f}, sy[4] = {0.f, 0.f, 0.f, 0.f};
         const int nvalid = min(kKeys, w.kend - ts);
+        bool vok = true;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -435,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // group's.
               const int s = gt % kVStages;
               if (!mbar_wait(bar(B_VFULL + s), (gt / kVStages) & 1)) {
-                ok = false;
+                vok = false;
               } else if (row >= nvalid) {
                 uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
 #pragma unroll
@@ -451,11 +443,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar((hh ? B_PHI : B_PLO) + x));
+          // all 128 rows of P_x(j) half hh are in TMEM (and any V rows past the
+          // keys zeroed): the leader issues O_x += P_x(j)[half hh] V_j
+          if (!bar_red_and(1 + x, 128, vok)) {
+            ok = false;
+            break;
+          }
+          if (leader) {
+            tc_fence_after();
+            const int vst = gt % kVStages;
+            if (hh == 0 && lok) lok = mbar_wait(bar(B_VFULL + vst), (gt / kVStages) & 1);
+            if (lok) {  // else S_x(j+1) never comes and the group stops at its next vote
+              const uint32_t vb = vbase + vst * Tile::BYTES;
+#pragma unroll
+              for (int k4 = 0; k4 < PSTEPS / 2; ++k4) {
+                // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
+                const int kk = hh * (PSTEPS / 2) + k4;
+                const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
+                tc_mma_f16_ts(od0, sd0 + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+              }
+              if (hh == 1) {
+                tc_commit(bar(B_OFULL + x));
+                tc_commit(bar(B_VEMPTY + vst));  // this group is done with V_j
+              }
+            }
+          }
         }
         l += ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
         if (!ok) break;
       }
-      if (ok) ok = mbar_wait(bar(B_OFULL + x), (gt - 1) & 1);  // the unit's last P.V_x
+      const bool ofull = ok && mbar_wait(bar(B_OFULL + x), (gt - 1) & 1);  // the unit's last P.V_x
+      ok = bar_red_and(1 + x, 128, ofull);
       if (!ok) break;
       tc_fence_after();
       if (p.causal) {
@@ -498,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();  // O_x read out before the next unit's P.V overwrites it
     }
-    if (!ok && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
+    if ((!ok && lane == 0) || (leader && !lok)) record_error(p.err, PA_DEVERR_TIMEOUT);
+    if (leader) tc_commit(bar(B_MMADONE));  // this group's P.V MMAs have completed
   }
 
   // ------------------------------------------------------------------ teardown
