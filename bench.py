@@ -212,6 +212,7 @@ class Step:
             # goes through pa_decode_shared_prefix: read once for all queries
             self.prefix_len = 0
             if wl.q_len > 1:  # speculative verify: k+1 queries per request
+                self.split = ops.verify_split_tokens(maxblk, wl.block_size, wl.q_len, wl.split_tokens)
                 n = ops.verify_workspace_size(len(wl.decode_seqs), wl.q_len, wl.q_heads, wl.head_dim, maxblk,
                                               wl.block_size, self.split)
             if shared_prefix and wl.q_len == 1 and wl.block_size >= 8 and len(wl.decode_seqs) >= 8:

@@ -162,9 +162,10 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
  * call with these arguments uses, or PA_ERR_INVALID if split_tokens is not
  * allowed.  A request with one
  * partition is written straight to `out`; a request with more keeps per
- * partition the unnormalised output and its running max and sum, and
- * pa_lse_merge combines them:  M = max_c m_c,  out = sum_c e^(m_c-M) o_c /
- * sum_c e^(m_c-M) l_c.
+ * partition the unnormalised output o_c, the reference maximum m_c its
+ * exponents were taken against (the running maximum, or up to 8 below it in
+ * log2 units) and the sum l_c, and pa_lse_merge combines them:
+ * M = max_c m_c,  out = sum_c e^(m_c-M) o_c / sum_c e^(m_c-M) l_c.
  *
  *   q             [num_seqs][q_heads][head_dim]
  *   out           [num_seqs][q_heads][head_dim]
@@ -219,9 +220,16 @@ int pa_lse_merge(const void* workspace, size_t workspace_bytes, const int32_t* c
  * decode step.
  *   q, out        [num_seqs][q_len][q_heads][head_dim]
  *   q_len         >= 1, with (q_heads / kv_heads) * q_len <= 32
+ *   split_tokens  as pa_decode; 0 = the library's choice, which for q_len > 1
+ *                 and contexts up to 8192 tokens is 768 (longer than decode's:
+ *                 each partition's partials and merge rows grow with q_len)
  *   workspace     at least pa_verify_workspace_size(...) bytes
  * Everything else as pa_decode (which is the q_len = 1 case).
+ * pa_verify_split_tokens returns the partition size such a call uses, or
+ * PA_ERR_INVALID.
  * ------------------------------------------------------------------------- */
+int pa_verify_split_tokens(int max_blocks_per_seq, int block_size, int q_len, int split_tokens);
+
 size_t pa_verify_workspace_size(int num_seqs, int q_len, int q_heads, int head_dim, int max_blocks_per_seq,
                                 int block_size, int split_tokens);
 

@@ -17,7 +17,8 @@
 //
 // Math per tile (GQA: the whole query-head group shares every K/V tile):
 //   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]       mma.m16n8k16, D/16 k-steps
-//   online softmax per head column (running max in log2 units, running sum)
+//   online softmax per head column (reference max in log2 units, raised only
+//   when a score passes it by more than 8, and the running sum)
 //   P^T -> bf16/fp16, transposed in registers with movmatrix into the B
 //   fragment of   O^T[D x 8] += V^T[D x 16 tok] . P^T[16 x 8]   (D/16 m-tiles)
 // Tokens past the context are masked to -inf in S and their V rows are zeroed
@@ -323,27 +324,40 @@ __global__ void __launch_bounds__(WARPS * 32)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
-      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-      // a column that has seen no token yet keeps m = -inf: exponents then
-      // use 0 as reference, so every p and the rescale are exactly 0
-      const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m[nt][0] - mb0), al1 = exp2f(m[nt][1] - mb1);
-      m[nt][0] = mn0;
-      m[nt][1] = mn1;
+      // m is the reference the column's exponents are taken against.  It is
+      // raised (to the tile's maximum) only when a score exceeds it by more
+      // than 8 (log2 units), so p stays below 2^8 and most tiles skip the
+      // rescale of o and l; o, l and m stay consistent, so out and the merge
+      // are unchanged up to rounding.  Each column decides from its own
+      // scores alone (the vote only skips work when no column moves), so a
+      // column's bits do not depend on its neighbours.  A column that has
+      // seen no token yet keeps m = -inf: exponents then use 0 as reference,
+      // so every p is exactly 0.
+      const bool up0 = mx0 > m[nt][0] + 8.f, up1 = mx1 > m[nt][1] + 8.f;
+      if (__any_sync(0xffffffffu, up0 || up1)) {
+        const float al0 = up0 ? exp2f(m[nt][0] - mx0) : 1.f;
+        const float al1 = up1 ? exp2f(m[nt][1] - mx1) : 1.f;
+        m[nt][0] = up0 ? mx0 : m[nt][0];
+        m[nt][1] = up1 ? mx1 : m[nt][1];
+        lp[nt][0] *= al0;
+        lp[nt][1] *= al1;
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          acc[nt][mt][0] *= al0;
+          acc[nt][mt][1] *= al1;
+          acc[nt][mt][2] *= al0;
+          acc[nt][mt][3] *= al1;
+        }
+      }
+      const float mb0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0];
+      const float mb1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
       const float p0 = exp2f(s0 - mb0), p1 = exp2f(s1 - mb1);
       const float p2 = exp2f(s2 - mb0), p3 = exp2f(s3 - mb1);
       // P is rounded to the input type for the P.V MMA; the denominator sums
       // the same rounded values, so the output is an exact convex combination
       const uint32_t pk01 = Elem<T>::pack(p0, p1), pk23 = Elem<T>::pack(p2, p3);
-      lp[nt][0] = lp[nt][0] * al0 + (Elem<T>::lo(pk01) + Elem<T>::lo(pk23));
-      lp[nt][1] = lp[nt][1] * al1 + (Elem<T>::hi(pk01) + Elem<T>::hi(pk23));
-#pragma unroll
-      for (int mt = 0; mt < KSTEPS; ++mt) {
-        acc[nt][mt][0] *= al0;
-        acc[nt][mt][1] *= al1;
-        acc[nt][mt][2] *= al0;
-        acc[nt][mt][3] *= al1;
-      }
+      lp[nt][0] += Elem<T>::lo(pk01) + Elem<T>::lo(pk23);
+      lp[nt][1] += Elem<T>::hi(pk01) + Elem<T>::hi(pk23);
       pb0[nt] = movmatrix_trans(pk01);
       pb1[nt] = movmatrix_trans(pk23);
     }

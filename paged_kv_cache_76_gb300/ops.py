@@ -28,6 +28,7 @@ __all__ = [
     "decode_shared_prefix_workspace_size",
     "decode_shared_prefix_split_tokens",
     "verify_decode",
+    "verify_split_tokens",
     "verify_workspace_size",
     "get_device_error",
     "launch_count",
@@ -170,6 +171,11 @@ def lse_merge(workspace, context_lens, q, block_tables, block_size, out, split_t
     check(_lib.lib().pa_lse_merge(ws_ptr, ws_bytes, _i32(context_lens, "context_lens"), B, hq, d,
                                   int(block_tables.shape[1]), block_size, int(split_tokens), _dev(out, "out"),
                                   dtype_code(out.dtype), _stream(stream)), "pa_lse_merge")
+
+
+def verify_split_tokens(max_blocks_per_seq: int, block_size: int, q_len: int, split_tokens: int = 0) -> int:
+    return check(_lib.lib().pa_verify_split_tokens(max_blocks_per_seq, block_size, q_len, split_tokens),
+                 "pa_verify_split_tokens")
 
 
 def verify_workspace_size(num_seqs, q_len, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens=0) -> int:

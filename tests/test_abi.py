@@ -45,6 +45,13 @@ def test_host_only_calls(lib):
     assert lib.pa_decode_split_tokens(256, 16, 24) == _lib.PA_ERR_INVALID      # not a multiple of 16
     assert lib.pa_decode_split_tokens(256, 32, 48) == _lib.PA_ERR_INVALID      # not a multiple of bs=32
     assert lib.pa_decode_split_tokens(256, 4, 2048) == _lib.PA_ERR_INVALID     # > 256 * bs
+    assert lib.pa_verify_split_tokens(256, 16, 4, 0) == 768           # verify auto, contexts up to 8K
+    assert lib.pa_verify_split_tokens(256, 32, 8, 0) == 768
+    assert lib.pa_verify_split_tokens(256, 16, 1, 0) == 384           # q_len 1 is decode
+    assert lib.pa_verify_split_tokens(1024, 16, 4, 0) == 512          # longer contexts: decode's choice
+    assert lib.pa_verify_split_tokens(256, 16, 4, 128) == 128         # explicit
+    assert lib.pa_verify_split_tokens(256, 16, 0, 0) == _lib.PA_ERR_INVALID
+    assert lib.pa_verify_split_tokens(256, 16, 4, 24) == _lib.PA_ERR_INVALID
     # shared-prefix suffixes: a quarter of the suffix bound, >= 128, <= the decode default
     assert lib.pa_decode_shared_prefix_split_tokens(160, 16, 2048, 0) == 128    # suffix bound 512
     assert lib.pa_decode_shared_prefix_split_tokens(256, 16, 1024, 0) == 384    # bound 3072 -> 768, capped

@@ -81,9 +81,11 @@ def test_each_query_is_bitwise_decode_over_its_visible_prefix(split):
     q, kc, vc, tables, lens_t = _case(2, q_len, hq, hkv, d, bs, "bf16", lens)
     scale = 1 / np.sqrt(d)
     out = ops().verify_decode(q, kc, vc, tables, lens_t, scale, split_tokens=split)
+    # the same partitions as the verify call (its automatic choice differs from decode's)
+    dsplit = ops().verify_split_tokens(tables.shape[1], bs, q_len, split)
     for i in range(q_len):
         li = torch.clamp(lens_t - (q_len - 1 - i), min=0).to(torch.int32)
-        dec = ops().decode(q[:, i].contiguous(), kc, vc, tables, li, scale, split_tokens=split)
+        dec = ops().decode(q[:, i].contiguous(), kc, vc, tables, li, scale, split_tokens=dsplit)
         assert torch.equal(out[:, i], dec), i
     assert ops().get_device_error() == 0
 
@@ -117,4 +119,32 @@ def test_verify_rejects_too_many_columns_and_bad_q_len():
                             lens_t.data_ptr(), 1, 0, 48, 4, 128, 16, kc.shape[0], 0.1, 0, None, 0, q.data_ptr(),
                             _lib.PA_BF16, torch.cuda.current_stream().cuda_stream)
     assert st == _lib.PA_ERR_INVALID
+    assert ops().get_device_error() == 0
+
+
+@pytest.mark.parametrize("q_len,split", [(1, 256), (4, 0), (8, 128)])
+def test_rising_scores_move_the_reference_per_column(q_len, split):
+    # K grows along each request's context, so every column's maximum keeps
+    # rising past its exponent reference, at different tiles for different
+    # columns: the output still matches the oracle, and each query still
+    # equals decode over its visible prefix bit for bit (a column's
+    # reference never depends on its neighbours).
+    hq, hkv, d, bs = 32, 8, 128, 16
+    lens = [1500, 37, 700]
+    q, kc, vc, tables, lens_t = _case(11, q_len, hq, hkv, d, bs, "bf16", lens)
+    tab = tables.cpu().numpy()
+    grow = torch.ones(kc.shape[0], device="cuda")
+    for r, L in enumerate(lens):
+        for j in range(-(-L // bs)):
+            grow[int(tab[r, j])] = 1.0 + 0.35 * j
+    kc = (kc.float() * grow[:, None, None, None]).to(kc.dtype)
+    scale = 1 / np.sqrt(d)
+    out = ops().verify_decode(q, kc, vc, tables, lens_t, scale, split_tokens=split)
+    ref = opa.verify_decode(to_f64(q), to_f64(kc), to_f64(vc), tab, lens, scale)
+    assert_close(out, ref, f"rising scores q_len {q_len}")
+    dsplit = ops().verify_split_tokens(tables.shape[1], bs, q_len, split)
+    for i in range(q_len):
+        li = torch.clamp(lens_t - (q_len - 1 - i), min=0).to(torch.int32)
+        dec = ops().decode(q[:, i].contiguous(), kc, vc, tables, li, scale, split_tokens=dsplit)
+        assert torch.equal(out[:, i], dec), i
     assert ops().get_device_error() == 0
