@@ -20,8 +20,8 @@
 //
 // Warp roles (384 threads = 12 warps, so that each thread may hold 168
 // registers; one CTA per SM):
-//   warps 0,1   MMA issuers, one thread per Q tile x: per key tile j,
-//                 S_x(j) = Q_x K_j^T, then O_x += P_x(j) V_j
+//   warps 0,1   S issuers, one thread per Q tile x: per key tile j,
+//                 S_x(j) = Q_x K_j^T
 //               S_x(j) overwrites P_x(j-1), so it is issued once P.V_x(j-1)
 //               has completed.  The two issuers wait only on their own tile;
 //               the tensor pipe interleaves their MMAs.
@@ -30,7 +30,9 @@
 //               read it.
 //   warps 4..7  softmax of tile A, warps 8..11 of tile B: thread = TMEM lane
 //               = row.  It loads its S row, takes the row maximum, writes
-//               P = 2^(s*scale*log2e - m) into TMEM and sums it.  The running
+//               P = 2^(s*scale*log2e - m) into TMEM and sums it; after each
+//               half of P the group meets at a named barrier and its first
+//               thread issues O_x += P_x(j) V_j for that half.  The running
 //               maximum m is raised only when a row maximum exceeds it by
 //               more than 2^8 (O is then rescaled in TMEM); the final O / sum
 //               uses the same m, so this is exact.
