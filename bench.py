@@ -52,6 +52,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention: achieved KV GB/s vs GB300 HBM peak; decode tokens/s"
 DEFAULT_WORKLOAD = "llama8b_gqa_decode"
+E2E_SETS = 3  # staging buffer sets, i.e. end-to-end steps in flight
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -291,19 +292,21 @@ class Step:
             # not write, and runs beside the HBM-bound suffix decode
             self.prefix_side = torch.cuda.Stream(device, priority=torch.cuda.Stream.priority_range()[1])
             self.ev_pfork = torch.cuda.Event()
-        # a second set of staging buffers: the end-to-end loop keeps two steps
-        # in flight (the host launches step i+1 before it reads step i's result)
+        # more sets of staging buffers: the end-to-end loop keeps E2E_SETS steps
+        # in flight (the host launches step i+E2E_SETS-1 before it reads step
+        # i's result), so host-side jitter does not starve the GPU
         self._sets = [dict(h_stage=self.h_stage, d_stage=self.d_stage, d=self.d, d_out=self.d_out,
                            h_outbuf=self.h_outbuf, out_dec=dv.get("dec"), out_pre=dv.get("pre"))]
-        h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-        h2.copy_(self.h_stage)
-        d2 = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        d2.copy_(h2)
-        o2 = torch.empty(obytes, dtype=torch.uint8, device=device)
-        dv2 = views(o2, ooffs, outs)
-        self._sets.append(dict(h_stage=h2, d_stage=d2, d=views(d2, offs, self.h), d_out=o2,
-                               h_outbuf=torch.empty(obytes, dtype=torch.uint8).pin_memory(), out_dec=dv2.get("dec"),
-                               out_pre=dv2.get("pre")))
+        for _ in range(E2E_SETS - 1):
+            h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+            h2.copy_(self.h_stage)
+            d2 = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            d2.copy_(h2)
+            o2 = torch.empty(obytes, dtype=torch.uint8, device=device)
+            dv2 = views(o2, ooffs, outs)
+            self._sets.append(dict(h_stage=h2, d_stage=d2, d=views(d2, offs, self.h), d_out=o2,
+                                   h_outbuf=torch.empty(obytes, dtype=torch.uint8).pin_memory(),
+                                   out_dec=dv2.get("dec"), out_pre=dv2.get("pre")))
         self.out_dec = dv.get("dec")
         self.out_pre = dv.get("pre")
         self.h_out_dec = hv.get("dec")
@@ -460,7 +463,7 @@ class Step:
         return self.prefill_ctas
 
     def select(self, k: int):
-        """Use staging buffer set k (0 or 1) for the following steps."""
+        """Use staging buffer set k (0 .. E2E_SETS-1) for the following steps."""
         for name, val in self._sets[k].items():
             setattr(self, name, val)
 
@@ -596,6 +599,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split", type=int, default=None, help="decode partition size (default: the workload's)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-launch", default="graph", choices=["graph", "eager"],
+                    help="kernels of each end-to-end step: a CUDA graph per buffer set, or eager launches")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--serial", action="store_true", help="run prefill and decode on one stream, one after the other")
@@ -710,28 +715,33 @@ def main():
     # from pinned host memory (one buffer), runs the kernels (a CUDA graph per
     # staging-buffer set) and copies its outputs back, and the host reads
     # them.  The copies run on two copy streams, so step i+1's inputs go up
-    # and step i-1's outputs come down while step i computes; two buffer sets
-    # alternate, each reused only after the host has read its outputs.
+    # and step i-1's outputs come down while step i computes; E2E_SETS buffer
+    # sets rotate, each reused only after the host has read its outputs.
     e2e_val = None
     h2d, d2h = step.e2e_bytes()
     e2e_mode = ("H2D copy stream -> kernels (CUDA graph) -> D2H copy stream per step; copies overlap the "
                 "neighbouring steps' kernels; the host reads every step's outputs")
     graphs = None
+    if args.e2e_launch == "eager":
+        e2e_mode = e2e_mode.replace("kernels (CUDA graph)", "kernels (eager launches)")
+    nsets = len(step._sets)
     with torch.cuda.stream(stream):
-        for k in (0, 1, 0):
+        for k in list(range(nsets)) + [0]:
             step.select(k)
             step.run_e2e(stream)
     stream.synchronize()
     eager_out = step.h_outbuf.clone()  # the eager step's outputs, for checking a replay
     try:
+        if args.e2e_launch == "eager":
+            raise StopIteration
         graphs = []
-        for k in (0, 1):
+        for k in range(nsets):
             step.select(k)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 step.run(stream)
             graphs.append(g)
-        for k in (0, 1):
+        for k in range(nsets):
             step.select(k)
             step.d_out.zero_()
             with torch.cuda.stream(stream):
@@ -742,28 +752,31 @@ def main():
                 raise RuntimeError("device error in graph replay")
             if not torch.equal(step.h_outbuf[:step.out_used], eager_out[:step.out_used]):
                 raise RuntimeError("graph replay output differs from the eager step")
+    except StopIteration:
+        graphs = None
     except Exception as exc:  # capture not possible here: eager launches instead
         graphs = None
         e2e_mode = f"eager kernel launches, copies on two copy streams (graph capture not used: {exc})"
     up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("up", "kern", "down")}
-    checksum = 0.0
+    ev = {n: [torch.cuda.Event() for _ in range(nsets)] for n in ("up", "kern", "down")}
+    checksum = 0
     sets = step._sets
+    host_out = [b["h_outbuf"].numpy() for b in sets]  # the pinned output buffers, read by the host
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(args.e2e_steps):
-        k = i & 1
+        k = i % nsets
         b = sets[k]
-        if i >= 2:
-            up.wait_event(ev["kern"][k])  # step i-2's kernels are done with this input buffer
+        if i >= nsets:
+            up.wait_event(ev["kern"][k])  # step i-nsets's kernels are done with this input buffer
         with torch.cuda.stream(up):
             b["d_stage"].copy_(b["h_stage"], non_blocking=True)
         ev["up"][k].record(up)
         stream.wait_event(ev["up"][k])
-        if i >= 2:
-            stream.wait_event(ev["down"][k])  # step i-2's outputs have left this output buffer
+        if i >= nsets:
+            stream.wait_event(ev["down"][k])  # step i-nsets's outputs have left this output buffer
         step.select(k)
         with torch.cuda.stream(stream):
             if graphs is not None:
@@ -775,11 +788,14 @@ def main():
         with torch.cuda.stream(down):
             b["h_outbuf"].copy_(b["d_out"], non_blocking=True)
         ev["down"][k].record(down)
-        if i >= 1:  # the previous step's outputs, now in pinned host memory
-            ev["down"][k ^ 1].synchronize()
-            checksum += float(sets[k ^ 1]["h_outbuf"][:16].float().sum())
-    ev["down"][(args.e2e_steps - 1) & 1].synchronize()
-    checksum += float(sets[(args.e2e_steps - 1) & 1]["h_outbuf"][:16].float().sum())
+        if i >= nsets - 1:  # step i-nsets+1's outputs, in pinned host memory; its set is reused next
+            kk = (i + 1) % nsets
+            ev["down"][kk].synchronize()
+            checksum += int(host_out[kk][:64].sum())
+    for i in range(max(0, args.e2e_steps - nsets + 1), args.e2e_steps):  # the last steps' outputs
+        kk = i % nsets
+        ev["down"][kk].synchronize()
+        checksum += int(host_out[kk][:64].sum())
     e2e_s = time.perf_counter() - t0
     step.select(0)
     e2e_s = reduce_max(e2e_s, ws, device)
