@@ -97,6 +97,9 @@ DECODE_CASES = [
     (8, 4, 64, 32, "bf16", [31, 32, 1000], 0),
     (4, 4, 128, 4, "bf16", [3, 400, 1025], 256),
     (12, 3, 64, 16, "fp16", [2050, 16, 15], 1024),
+    # the largest partitions (256 table entries per warp) on both block sizes
+    (8, 2, 128, 16, "bf16", [4096, 4097, 9000, 1], 4096),
+    (4, 1, 64, 4, "fp16", [1024, 1025, 2100], 1024),
 ]
 
 
