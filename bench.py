@@ -19,7 +19,9 @@ Reported (one JSON line from rank 0):
   workload on this host (rank 0 only);
 * e2e: the same metric through the public API with host buffers: pinned host
   -> device copies of the step's inputs and a device -> host read of its
-  outputs inside the timed region.
+  outputs inside the timed region, three steps in flight; the kernels of a
+  one-stream step are the library calls marshalled once (ops.recording) and
+  issued again each step, those of a two-stream step one CUDA graph.
 ``--impl reference`` times the CPU oracle itself as the reference arm.
 ``--kv-layout contiguous|vmm`` (decode-only workloads) runs the same step on
 the competing design of "vAttention 完全拆解": one contiguous
@@ -176,6 +178,7 @@ class Step:
         from paged_kv_cache_76_gb300 import ops
         from paged_kv_cache_76_gb300.allocator import BlockAllocator
         self.ops = ops
+        self._rec = None  # a plan being recorded (record_plan)
         self.wl = wl
         self.dev = device
         a = BlockAllocator(wl.num_blocks, wl.block_size, wl.free_order)
@@ -373,14 +376,31 @@ class Step:
         if ev is not None:
             ev[1].record(stream)
 
+    def _do(self, fn):
+        """A stream/event operation of the step: run it, or add it to the plan being recorded."""
+        if self._rec is not None:
+            self._rec.add(fn)
+        else:
+            fn()
+
+    def record_plan(self, stream):
+        """The step's launches and stream/event operations, marshalled once (ops.recording)."""
+        with self.ops.recording() as rec:
+            self._rec = rec
+            try:
+                self.run(stream)
+            finally:
+                self._rec = None
+        return rec
+
     # -- one step through the C ABI; ev = (start, end) events around the decode partial kernel
     def run(self, stream, ev=None):
         o, d, wl = self.ops, self.d, self.wl
         if self.layout != "paged":
             return self._run_contiguous(stream, ev)
         if self.prefix_side is not None:
-            self.ev_pfork.record(stream)
-            self.prefix_side.wait_event(self.ev_pfork)
+            self._do(lambda: self.ev_pfork.record(stream))
+            self._do(lambda: self.prefix_side.wait_event(self.ev_pfork))
         if self.n_pairs:
             o.copy_blocks(self.k_cache, self.v_cache, d["pairs"], stream=stream)
         o.reshape_and_cache(d["k_new"], d["v_new"], d["slots"], self.k_cache, self.v_cache, stream=stream)
@@ -388,12 +408,12 @@ class Step:
         if overlap:
             # prefill (tensor-bound) on a second stream, concurrent with decode (HBM-bound);
             # both only read the cache this step's reshape_and_cache wrote
-            self.ev_fork.record(stream)
-            self.side.wait_event(self.ev_fork)
+            self._do(lambda: self.ev_fork.record(stream))
+            self._do(lambda: self.side.wait_event(self.ev_fork))
             o.chunked_prefill(d["q_prefill"], d["q_start"], d["pre_lens"], self.k_cache, self.v_cache,
                               d["pre_tables"], wl.scale, self.max_q_len, out=self.out_pre, stream=self.side,
                               max_ctas=self.prefill_ctas)
-            self.ev_join.record(self.side)
+            self._do(lambda: self.ev_join.record(self.side))
         elif self.pre:
             if ev is not None and not self.dec:
                 ev[0].record(stream)
@@ -426,7 +446,7 @@ class Step:
             o.lse_merge(self.workspace, d["dec_lens"], d["q_decode"], d["dec_tables"], wl.block_size, self.out_dec,
                         split_tokens=self.split, stream=stream)
         if overlap:
-            stream.wait_event(self.ev_join)
+            self._do(lambda: stream.wait_event(self.ev_join))
 
     def calibrate_prefill_ctas(self, stream, sms: int, reps: int = 3) -> int:
         """SMs to leave to the prefill when it runs beside decode.
@@ -599,8 +619,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split", type=int, default=None, help="decode partition size (default: the workload's)")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--e2e-launch", default="graph", choices=["graph", "eager"],
-                    help="kernels of each end-to-end step: a CUDA graph per buffer set, or eager launches")
+    ap.add_argument("--e2e-launch", default="auto", choices=["auto", "graph", "eager"],
+                    help="kernels of each end-to-end step: eager launches marshalled once (ops.recording), or a "
+                         "CUDA graph per buffer set; auto = eager for one-stream steps, graph for steps that fork "
+                         "a second stream")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--serial", action="store_true", help="run prefill and decode on one stream, one after the other")
@@ -722,8 +744,16 @@ def main():
     e2e_mode = ("H2D copy stream -> kernels (CUDA graph) -> D2H copy stream per step; copies overlap the "
                 "neighbouring steps' kernels; the host reads every step's outputs")
     graphs = None
-    if args.e2e_launch == "eager":
-        e2e_mode = e2e_mode.replace("kernels (CUDA graph)", "kernels (eager launches)")
+    plans = None
+    e2e_launch = args.e2e_launch
+    if e2e_launch == "auto":
+        # measured on GB300: recorded eager launches beat a graph replay by 2-5 us per step when the
+        # step runs on one stream (the 8B-style step: 95.2 against 100.5 us); a step that forks a
+        # second stream issues more host calls than the GPU takes to run it (shared prefix: 86-90 us
+        # eager against 71.4 us as a graph)
+        e2e_launch = "graph" if (step.side is not None or step.prefix_side is not None) else "eager"
+    if e2e_launch == "eager":
+        e2e_mode = e2e_mode.replace("kernels (CUDA graph)", "kernels (eager launches, marshalled once)")
     nsets = len(step._sets)
     with torch.cuda.stream(stream):
         for k in list(range(nsets)) + [0]:
@@ -732,7 +762,7 @@ def main():
     stream.synchronize()
     eager_out = step.h_outbuf.clone()  # the eager step's outputs, for checking a replay
     try:
-        if args.e2e_launch == "eager":
+        if e2e_launch == "eager":
             raise StopIteration
         graphs = []
         for k in range(nsets):
@@ -757,6 +787,12 @@ def main():
     except Exception as exc:  # capture not possible here: eager launches instead
         graphs = None
         e2e_mode = f"eager kernel launches, copies on two copy streams (graph capture not used: {exc})"
+    if graphs is None:
+        # eager: each set's launches marshalled once (ops.recording), issued as they are every step
+        plans = []
+        for k in range(nsets):
+            step.select(k)
+            plans.append(step.record_plan(stream))
     up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev = {n: [torch.cuda.Event() for _ in range(nsets)] for n in ("up", "kern", "down")}
     checksum = 0
@@ -782,7 +818,7 @@ def main():
             if graphs is not None:
                 graphs[k].replay()
             else:
-                step.run(stream)
+                plans[k]()
         ev["kern"][k].record(stream)
         down.wait_event(ev["kern"][k])
         with torch.cuda.stream(down):

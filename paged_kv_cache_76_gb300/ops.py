@@ -33,6 +33,8 @@ __all__ = [
     "get_device_error",
     "launch_count",
     "dtype_code",
+    "recording",
+    "Recording",
 ]
 
 
@@ -42,6 +44,64 @@ def dtype_code(dt: torch.dtype) -> int:
     if dt == torch.float16:
         return PA_FP16
     raise TypeError(f"unsupported dtype {dt}: use torch.bfloat16 or torch.float16")
+
+
+class Recording:
+    """Library launches marshalled once, to be issued again as they are.
+
+    Inside ``with recording() as rec:`` the launching functions of this module
+    check and marshal their arguments but launch nothing: each appends a
+    callable to ``rec.steps`` that issues the same C call with the same
+    pointers, sizes and streams.  ``rec.add(fn)`` appends any other step (an
+    event record or wait) in order.  ``rec()`` runs the steps in order: the
+    same launches for a fraction of the host time of the marshalling (the
+    tensors must stay alive and in place).
+    """
+
+    def __init__(self):
+        self.steps = []
+        self.keep = []  # tensors a recorded launch writes or reads that the caller did not pass in
+
+    def add(self, fn):
+        self.steps.append(fn)
+
+    def __call__(self):
+        for fn in self.steps:
+            fn()
+
+
+_recording = None
+
+
+class recording:
+    """Context manager: see :class:`Recording`."""
+
+    def __enter__(self) -> Recording:
+        global _recording
+        if _recording is not None:
+            raise RuntimeError("recordings do not nest")
+        _recording = Recording()
+        return _recording
+
+    def __exit__(self, *exc):
+        global _recording
+        _recording = None
+        return False
+
+
+def _keep(*tensors) -> None:
+    """Inside a recording, keep tensors allocated by the call alive with the recording."""
+    if _recording is not None:
+        _recording.keep.extend(t for t in tensors if t is not None)
+
+
+def _launch(name: str, *args) -> None:
+    """Issue (or, inside a recording, record) the C call `name`(*args)."""
+    fn = getattr(_lib.lib(), name)
+    if _recording is not None:
+        _recording.add(lambda: check(fn(*args), name))
+        return
+    check(fn(*args), name)
 
 
 def _stream(stream=None):
@@ -77,18 +137,20 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None):
     nb, bs, hkv, d = _cache_dims(k_cache)
     if v_cache.shape != k_cache.shape or k.shape != v.shape or k.shape[1:] != (hkv, d):
         raise ValueError("shape mismatch")
-    check(_lib.lib().pa_reshape_and_cache(
+    _launch(
+        "pa_reshape_and_cache",
         _dev(k, "k"), _dev(v, "v"), _i32(slot_mapping, "slot_mapping"), int(k.shape[0]),
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), nb, bs, hkv, d, dtype_code(k_cache.dtype),
-        _stream(stream)), "pa_reshape_and_cache")
+        _stream(stream))
 
 
 def copy_blocks(k_cache, v_cache, pairs, stream=None):
     """``pairs``: int32 [n, 2] (src, dst) on the cache's device."""
     nb, bs, hkv, d = _cache_dims(k_cache)
-    check(_lib.lib().pa_copy_blocks(
+    _launch(
+        "pa_copy_blocks",
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(pairs, "pairs"), int(pairs.shape[0]),
-        nb, bs, hkv, d, dtype_code(k_cache.dtype), _stream(stream)), "pa_copy_blocks")
+        nb, bs, hkv, d, dtype_code(k_cache.dtype), _stream(stream))
 
 
 def _dev_or_pinned(t: torch.Tensor, name: str):
@@ -110,10 +172,11 @@ def swap_blocks(src_k, src_v, dst_k, dst_v, pairs, stream=None):
         raise TypeError("pairs must be int32")
     ns, bs, hkv, d = _cache_dims(src_k)
     nd = dst_k.shape[0]
-    check(_lib.lib().pa_swap_blocks(
+    _launch(
+        "pa_swap_blocks",
         _dev_or_pinned(src_k, "src_k"), _dev_or_pinned(src_v, "src_v"), _dev_or_pinned(dst_k, "dst_k"),
         _dev_or_pinned(dst_v, "dst_v"), _dev_or_pinned(pairs, "pairs"), int(pairs.shape[0]), ns, nd, bs, hkv, d,
-        dtype_code(src_k.dtype), _stream(stream)), "pa_swap_blocks")
+        dtype_code(src_k.dtype), _stream(stream))
 
 
 def decode_split_tokens(max_blocks_per_seq: int, block_size: int, split_tokens: int = 0) -> int:
@@ -155,22 +218,23 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, spl
     if workspace is None:
         workspace = make_workspace(q, block_tables, k_cache.shape[1], split_tokens)
     args = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, workspace)
-    check(_lib.lib().pa_decode(*args, _stream(stream)), "pa_decode")
+    _keep(out, workspace)
+    _launch("pa_decode", *args, _stream(stream))
     return out
 
 
 def decode_partial(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens=0, workspace=None,
                    stream=None):
     args = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, workspace)
-    check(_lib.lib().pa_decode_partial(*args, _stream(stream)), "pa_decode_partial")
+    _launch("pa_decode_partial", *args, _stream(stream))
 
 
 def lse_merge(workspace, context_lens, q, block_tables, block_size, out, split_tokens=0, stream=None):
     B, hq, d = q.shape
     ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
-    check(_lib.lib().pa_lse_merge(ws_ptr, ws_bytes, _i32(context_lens, "context_lens"), B, hq, d,
-                                  int(block_tables.shape[1]), block_size, int(split_tokens), _dev(out, "out"),
-                                  dtype_code(out.dtype), _stream(stream)), "pa_lse_merge")
+    _launch("pa_lse_merge", ws_ptr, ws_bytes, _i32(context_lens, "context_lens"), B, hq, d,
+            int(block_tables.shape[1]), block_size, int(split_tokens), _dev(out, "out"), dtype_code(out.dtype),
+            _stream(stream))
 
 
 def verify_split_tokens(max_blocks_per_seq: int, block_size: int, q_len: int, split_tokens: int = 0) -> int:
@@ -201,10 +265,12 @@ def verify_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=No
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
     ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
         if workspace is not None else (None, 0)
-    check(_lib.lib().pa_verify_decode(
+    _keep(out, workspace)
+    _launch(
+        "pa_verify_decode",
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(block_tables, "block_tables"), maxblk,
         _i32(context_lens, "context_lens"), B, ql, hq, hkv, d, bs, nb, float(scale), int(split_tokens), ws_ptr,
-        ws_bytes, _dev(out, "out"), dtype_code(q.dtype), _stream(stream)), "pa_verify_decode")
+        ws_bytes, _dev(out, "out"), dtype_code(q.dtype), _stream(stream))
     return out
 
 
@@ -238,12 +304,13 @@ def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_t
     if workspace is None:
         n = decode_shared_prefix_workspace_size(B, hq, d, maxblk, bs, int(prefix_len), split_tokens)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
-    check(_lib.lib().pa_decode_shared_prefix(
+    _keep(out, workspace)
+    _launch(
+        "pa_decode_shared_prefix",
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(prefix_blocks, "prefix_blocks"),
         int(prefix_len), _i32(block_tables, "block_tables"), maxblk, _i32(context_lens, "context_lens"), B, hq, hkv,
         d, bs, nb, float(scale), int(split_tokens), workspace.data_ptr(), workspace.numel(), _dev(out, "out"),
-        dtype_code(q.dtype), _stream(stream), prefix_stream.cuda_stream if prefix_stream is not None else None),
-        "pa_decode_shared_prefix")
+        dtype_code(q.dtype), _stream(stream), prefix_stream.cuda_stream if prefix_stream is not None else None)
     return out
 
 
@@ -259,11 +326,13 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
         raise ValueError("q_start must have num_reqs+1 entries")
     if out is None:
         out = torch.empty_like(q)
-    check(_lib.lib().pa_chunked_prefill(
+    _keep(out)
+    _launch(
+        "pa_chunked_prefill",
         _dev(q, "q"), _i32(q_start, "q_start"), _i32(context_lens, "context_lens"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _i32(block_tables, "block_tables"), int(block_tables.shape[1]), R, T,
         int(max_q_len), int(max_ctas), hq, hkv, d, bs, nb, float(scale), _dev(out, "out"), dtype_code(q.dtype),
-        _stream(stream)), "pa_chunked_prefill")
+        _stream(stream))
     return out
 
 

@@ -11,6 +11,7 @@ import torch
 
 from . import _lib
 from ._lib import PA_ERR_NO_FREE_BLOCKS, PAError, check
+from .ops import _keep, _launch
 
 __all__ = ["VirtualKV", "NoPages", "decode_contiguous", "reshape_and_cache_slots"]
 
@@ -140,15 +141,15 @@ class VirtualKV:
             n = int(self._L.pa_decode_workspace_size(B, hq, d, self.max_len // 16, 16, int(split_tokens)))
             workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
         ws, wb = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
-        check(self._L.pa_vkv_decode(self._h, int(layer), _dev(q, "q"), _i32(slot_ids, "slot_ids"),
-                                    _i32(context_lens, "context_lens"), B, hq, float(scale), int(split_tokens), ws,
-                                    wb, _dev(out, "out"), _stream(stream)), "pa_vkv_decode")
+        _keep(out, workspace)
+        _launch("pa_vkv_decode", self._h, int(layer), _dev(q, "q"), _i32(slot_ids, "slot_ids"),
+                _i32(context_lens, "context_lens"), B, hq, float(scale), int(split_tokens), ws, wb, _dev(out, "out"),
+                _stream(stream))
         return out
 
     def reshape_and_cache(self, layer, k, v, slot_ids, positions, stream=None):
-        check(self._L.pa_vkv_reshape_and_cache(self._h, int(layer), _dev(k, "k"), _dev(v, "v"),
-                                               _i32(slot_ids, "slot_ids"), _i32(positions, "positions"),
-                                               int(k.shape[0]), _stream(stream)), "pa_vkv_reshape_and_cache")
+        _launch("pa_vkv_reshape_and_cache", self._h, int(layer), _dev(k, "k"), _dev(v, "v"),
+                _i32(slot_ids, "slot_ids"), _i32(positions, "positions"), int(k.shape[0]), _stream(stream))
 
 
 def decode_contiguous(q, k_cache, v_cache, slot_ids, context_lens, scale, slot_tokens=None, out=None,
@@ -163,19 +164,21 @@ def decode_contiguous(q, k_cache, v_cache, slot_ids, context_lens, scale, slot_t
         n = int(lib.pa_decode_workspace_size(B, hq, d, L // 16, 16, int(split_tokens)))
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
     ws, wb = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
-    check(lib.pa_decode_contiguous(
+    _keep(out, workspace)
+    _launch(
+        "pa_decode_contiguous",
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ns, L,
         _i32(slot_ids, "slot_ids") if slot_ids is not None else None,
         _i32(slot_tokens, "slot_tokens") if slot_tokens is not None else None, _i32(context_lens, "context_lens"),
-        B, hq, hkv, d, float(scale), int(split_tokens), ws, wb, _dev(out, "out"), _code(q.dtype), _stream(stream)),
-        "pa_decode_contiguous")
+        B, hq, hkv, d, float(scale), int(split_tokens), ws, wb, _dev(out, "out"), _code(q.dtype), _stream(stream))
     return out
 
 
 def reshape_and_cache_slots(k, v, slot_ids, positions, k_cache, v_cache, slot_tokens=None, stream=None):
     ns, L, hkv, d = k_cache.shape
-    check(_lib.lib().pa_reshape_and_cache_slots(
+    _launch(
+        "pa_reshape_and_cache_slots",
         _dev(k, "k"), _dev(v, "v"), _i32(slot_ids, "slot_ids"), _i32(positions, "positions"), int(k.shape[0]),
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ns, L,
         _i32(slot_tokens, "slot_tokens") if slot_tokens is not None else None, hkv, d, _code(k.dtype),
-        _stream(stream)), "pa_reshape_and_cache_slots")
+        _stream(stream))
