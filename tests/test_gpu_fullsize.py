@@ -129,3 +129,31 @@ def test_mixed_step_as_the_bench_launches_it_equals_the_single_stream_step():
     assert torch.equal(step.out_pre, dev.out_prefill)
     assert torch.equal(step.out_dec, dev.out_decode)
     _no_err()
+
+
+@pytest.mark.parametrize("name", ["prefix_shared_cow_decode", "mixed_prefill_decode"])
+def test_bench_step_recorded_once_replays_to_the_same_bits(name):
+    """bench.py's end-to-end loop can issue a step from launches marshalled
+    once (ops.recording), including the event fork and join of a second
+    stream: replaying the plan gives the bits of the step run directly."""
+    import bench
+    wl = W.WORKLOADS[name]()
+    step = bench.Step(wl, torch.device("cuda", 0), value_seed=wl.seed)
+    assert step.side is not None or step.prefix_side is not None
+    if step.side is not None:
+        step.prefill_ctas = 57
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step.run(s)
+    s.synchronize()
+    outs = [t.clone() for t in (step.out_dec, step.out_pre) if t is not None]
+    plan = step.record_plan(s)
+    for t in (step.out_dec, step.out_pre):
+        if t is not None:
+            t.zero_()
+    with torch.cuda.stream(s):
+        plan()
+    s.synchronize()
+    got = [t for t in (step.out_dec, step.out_pre) if t is not None]
+    assert all(torch.equal(a, b) for a, b in zip(got, outs))
+    _no_err()
