@@ -8,6 +8,7 @@ documented shapes; int32 index tensors live on the same device.
 from __future__ import annotations
 
 import math
+import threading
 
 import torch
 
@@ -55,7 +56,8 @@ class Recording:
     pointers, sizes and streams.  ``rec.add(fn)`` appends any other step (an
     event record or wait) in order.  ``rec()`` runs the steps in order: the
     same launches for a fraction of the host time of the marshalling (the
-    tensors must stay alive and in place).
+    tensors must stay alive and in place).  A recording belongs to the thread
+    that opened it; other threads launch as usual meanwhile.
     """
 
     def __init__(self):
@@ -70,36 +72,36 @@ class Recording:
             fn()
 
 
-_recording = None
+_tls = threading.local()  # .rec: the open recording of this thread, if any
 
 
 class recording:
     """Context manager: see :class:`Recording`."""
 
     def __enter__(self) -> Recording:
-        global _recording
-        if _recording is not None:
+        if getattr(_tls, "rec", None) is not None:
             raise RuntimeError("recordings do not nest")
-        _recording = Recording()
-        return _recording
+        _tls.rec = Recording()
+        return _tls.rec
 
     def __exit__(self, *exc):
-        global _recording
-        _recording = None
+        _tls.rec = None
         return False
 
 
 def _keep(*tensors) -> None:
     """Inside a recording, keep tensors allocated by the call alive with the recording."""
-    if _recording is not None:
-        _recording.keep.extend(t for t in tensors if t is not None)
+    rec = getattr(_tls, "rec", None)
+    if rec is not None:
+        rec.keep.extend(t for t in tensors if t is not None)
 
 
 def _launch(name: str, *args) -> None:
     """Issue (or, inside a recording, record) the C call `name`(*args)."""
     fn = getattr(_lib.lib(), name)
-    if _recording is not None:
-        _recording.add(lambda: check(fn(*args), name))
+    rec = getattr(_tls, "rec", None)
+    if rec is not None:
+        rec.add(lambda: check(fn(*args), name))
         return
     check(fn(*args), name)
 
