@@ -947,6 +947,8 @@ def main():
         # flops of the visible (query, key) pairs against the measured bf16 peak
         tpeak, tkind = measured_tensor_peak()
         fl = nb["prefill_flops"]
+        ptraffic = kernel_traffic(f"attn_tc_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/attn_tc.cu") \
+            if wl.block_size >= 8 else None
         res["roofline"] = {
             "kernel": "attn_tc_kernel" if wl.block_size >= 8 else "chunked_prefill_kernel",
             "bound": "tensor",
@@ -955,7 +957,7 @@ def main():
             "peak_kind": tkind,
             "unit": "TFLOP/s",
             "frac": round(fl / (dec_ms * 1e-3) / 1e12 / tpeak, 4),
-            "traffic": None,
+            "traffic": ptraffic,
             "algorithmic_flops_per_launch": fl,
             "avg_launch_ms": round(dec_ms, 5),
             "timing": "CUDA events around each of K chunked-prefill launches on the bench stream, in a second "
