@@ -890,6 +890,8 @@ def main():
                                     "setup_s": round(step.vmm_setup_s, 3)}
     if step.dec and step.prefix_len:
         ub = nb["decode_unique"]
+        # DRAM traffic of the call's dominant kernel, the suffix decode pass
+        straffic = kernel_traffic(f"decode_partial_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/decode.cu")
         flops = 4 * len(wl.decode_seqs) * wl.q_heads * wl.head_dim * step.prefix_len
         res["roofline"] = {
             "kernel": "pa_decode_shared_prefix (tcgen05 prefix pass + suffix decode + merge)",
@@ -899,7 +901,8 @@ def main():
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(ub / (dec_ms * 1e-3) / 1e9 / peak, 4),
-            "traffic": None,
+            "traffic": straffic,
+            "traffic_kernel": "decode_partial_kernel (suffix pass)",
             "algorithmic_bytes_per_launch": ub,
             "logical_bytes_per_launch": nb["decode"],
             "achieved_logical": round(nb["decode"] / (dec_ms * 1e-3) / 1e9, 1),
