@@ -303,6 +303,9 @@ PREFILL_CASES = [
     (4, 1, 64, 4, "fp16", [7, 33], [9, 40]),
     (16, 2, 128, 32, "bf16", [64, 65], [63, 70]),
     (32, 2, 64, 8, "fp16", [130, 0], [31, 256]),
+    # a request with an empty chunk between two others, on both prefill kernels
+    (8, 2, 128, 16, "bf16", [100, 40, 0], [33, 0, 20]),
+    (4, 1, 64, 4, "fp16", [7, 0, 12], [0, 9, 5]),
 ]
 
 
