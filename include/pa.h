@@ -451,6 +451,15 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, c
  * PA_ERR_DEVICE_CHECK if a code was recorded, PA_OK otherwise. */
 int pa_get_device_error(int32_t* host_code, pa_stream stream);
 
+/* Self-test of the bounded waits: launches one thread that waits on a
+ * shared-memory barrier phase nothing completes, with a limit of wait_ms
+ * (1..2000) instead of the kernels' 2 s.  The wait gives up, records
+ * PA_DEVERR_TIMEOUT in the error word and the kernel finishes normally, as
+ * any kernel of the library does when one of its waits expires; the context
+ * stays usable.  Asynchronous on `stream`; PA_ERR_INVALID for wait_ms out of
+ * range. */
+int pa_selftest_wait_timeout(int wait_ms, pa_stream stream);
+
 /* ============================================================================
  * Host block allocator ("2.1 PagedAttention" §9.1-§9.3, §3, §6).
  *

@@ -80,6 +80,7 @@ PROTOTYPES = {
     "pa_decode_partial": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I, _P]),
     "pa_lse_merge": (_I, [_P, _SZ, _P, _I, _I, _I, _I, _I, _I, _P, _I, _P]),
     "pa_verify_split_tokens": (_I, [_I, _I, _I, _I]),
+    "pa_selftest_wait_timeout": (_I, [_I, _P]),
     "pa_verify_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "pa_verify_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I, _P]),
     "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P]),

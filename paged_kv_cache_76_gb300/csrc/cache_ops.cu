@@ -151,7 +151,23 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Self-test of the bounded wait every kernel of the library uses: one
+// thread waits on an mbarrier phase that no arrival completes.  The wait
+// gives up after limit_ns, records PA_DEVERR_TIMEOUT and the kernel returns
+// normally, so the context stays usable.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  if (!mbar_wait_for(smem_u32(&bar), 0, limit_ns)) record_error(err, PA_DEVERR_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t stream) {
+  return launch_pdl(wait_timeout_kernel, dim3(1), dim3(32), 0, stream, err, limit_ns);
+}
 
 cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* pairs,
                                int num_pairs, int num_src, int num_dst, int64_t block_bytes, int* err,

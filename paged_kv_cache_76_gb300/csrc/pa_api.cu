@@ -780,6 +780,13 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   return cuda_status(launch_lse_merge(mp, head_dim, dtype, cs));
 }
 
+int pa_selftest_wait_timeout(int wait_ms, pa_stream stream) {
+  if (wait_ms < 1 || wait_ms > 2000) return PA_ERR_INVALID;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  return cuda_status(launch_wait_timeout(err, (uint64_t)wait_ms * 1000000ull, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int pa_get_device_error(int32_t* host_code, pa_stream stream) {
   if (!host_code) return PA_ERR_INVALID;
   int* err = device_error_ptr();

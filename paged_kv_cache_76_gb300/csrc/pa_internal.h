@@ -125,6 +125,7 @@ cudaError_t launch_chunked_prefill(const CUtensorMap& kmap, const CUtensorMap& v
 // tcgen05/TMEM kernel for blocks of >= 8 tokens (bsub >= 8): chunked prefill
 // (p.causal = 1) and the shared-prefix pass of a decode batch (p.causal = 0,
 // partials).  Two 128-row Q tiles per CTA, 128-key K/V tiles, P kept in TMEM.
+cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int head_dim,
                            int bsub, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,

@@ -32,6 +32,7 @@ __all__ = [
     "verify_split_tokens",
     "verify_workspace_size",
     "get_device_error",
+    "selftest_wait_timeout",
     "launch_count",
     "dtype_code",
     "recording",
@@ -336,6 +337,12 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
         int(max_q_len), int(max_ctas), hq, hkv, d, bs, nb, float(scale), _dev(out, "out"), dtype_code(q.dtype),
         _stream(stream))
     return out
+
+
+def selftest_wait_timeout(wait_ms: int = 50, stream=None) -> None:
+    """Launch the library's bounded-wait self-test (pa_selftest_wait_timeout):
+    afterwards the error word holds PA_DEVERR_TIMEOUT."""
+    check(_lib.lib().pa_selftest_wait_timeout(int(wait_ms), _stream(stream)), "pa_selftest_wait_timeout")
 
 
 def get_device_error(stream=None) -> int:

@@ -52,6 +52,8 @@ def test_host_only_calls(lib):
     assert lib.pa_verify_split_tokens(256, 16, 4, 128) == 128         # explicit
     assert lib.pa_verify_split_tokens(256, 16, 0, 0) == _lib.PA_ERR_INVALID
     assert lib.pa_verify_split_tokens(256, 16, 4, 24) == _lib.PA_ERR_INVALID
+    assert lib.pa_selftest_wait_timeout(0, None) == _lib.PA_ERR_INVALID        # limits checked on the host
+    assert lib.pa_selftest_wait_timeout(2001, None) == _lib.PA_ERR_INVALID
     # shared-prefix suffixes: a quarter of the suffix bound, >= 128, <= the decode default
     assert lib.pa_decode_shared_prefix_split_tokens(160, 16, 2048, 0) == 128    # suffix bound 512
     assert lib.pa_decode_shared_prefix_split_tokens(256, 16, 1024, 0) == 384    # bound 3072 -> 768, capped
