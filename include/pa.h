@@ -608,6 +608,37 @@ int pa_alloc_get_prefix_cache_stats(const pa_alloc* a, pa_prefix_cache_stats* ou
  * and changes nothing.
  * ------------------------------------------------------------------------- */
 int pa_alloc_enable_swap(pa_alloc* a, int num_cpu_blocks);
+
+/* ----------------------------------------------------------------------------
+ * Checkpoint and resume of the host allocator: its whole state (free queue
+ * order, refcounts, every sequence's Block Table, token count and hashing
+ * state, the prefix cache, the swap pool and the counters) as a flat list of
+ * int64 words.
+ *
+ * pa_alloc_export writes the words to out[0..cap) and their number to
+ * *n_out; with out = NULL and cap = 0 it only reports the number.  Returns
+ * PA_ERR_INVALID if cap is smaller than needed (nothing is written then).
+ * Equal states give equal words (sequences and cached hashes are written in
+ * key order).
+ *
+ * pa_alloc_import builds a new allocator (owned by the caller, freed with
+ * pa_alloc_destroy) from such words.  It validates every count, id and range
+ * and the state's consistency (refcounts equal the tables holding each block,
+ * the free queue holds exactly the unheld blocks, the cache holds exactly
+ * the hashed blocks under their hashes); malformed words give PA_ERR_INVALID
+ * and no allocator.  An imported
+ * allocator behaves as the exported one for every later call.
+ *
+ * Layout (version 1): magic 0x504b5641, version, num_blocks, block_size,
+ * caching, num_cpu_blocks, cow_copies, alloc_failures, lookup_blocks,
+ * hit_blocks, evictions; n_free and the free queue head to tail; ref[],
+ * has_hash[] and hash[] of every block; n_cached and (hash, block) pairs;
+ * n_cpu_free and the swap pool's free queue; n_seqs and per sequence (by id):
+ * id, num_tokens, salt, parent hash, hashable, swapped, n_blocks, blocks,
+ * n_pending, pending token ids.
+ * ------------------------------------------------------------------------- */
+int pa_alloc_export(const pa_alloc* a, int64_t* out, int64_t cap, int64_t* n_out);
+int pa_alloc_import(const int64_t* words, int64_t n, pa_alloc** out);
 int pa_alloc_num_free_cpu(const pa_alloc* a);
 /* 1 if seq_id is swapped out, 0 if resident, PA_ERR_INVALID if unknown. */
 int pa_alloc_is_swapped(const pa_alloc* a, int seq_id);

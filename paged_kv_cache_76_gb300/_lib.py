@@ -126,6 +126,8 @@ PROTOTYPES = {
     "pa_vkv_decode": (_I, [_P, _I, _P, _P, _P, _I, _I, _F, _I, _P, _SZ, _P, _P]),
     "pa_vkv_reshape_and_cache": (_I, [_P, _I, _P, _P, _P, _P, _I, _P]),
     "pa_alloc_enable_swap": (_I, [_P, _I]),
+    "pa_alloc_export": (_I, [_P, _P, C.c_int64, C.POINTER(C.c_int64)]),
+    "pa_alloc_import": (_I, [_P, C.c_int64, C.POINTER(_P)]),
     "pa_alloc_num_free_cpu": (_I, [_P]),
     "pa_alloc_is_swapped": (_I, [_P, _I]),
     "pa_alloc_swap_out": (_I, [_P, _I, _I32P, _I, C.POINTER(_I)]),

@@ -44,6 +44,29 @@ class BlockAllocator:
         self._h = h
         self._order_keepalive = order
 
+    def export(self) -> np.ndarray:
+        """The allocator's whole state as int64 words (pa_alloc_export)."""
+        n = C.c_int64(0)
+        _chk(self._L.pa_alloc_export(self._h, None, 0, C.byref(n)), "pa_alloc_export")
+        words = np.zeros(n.value, dtype=np.int64)
+        _chk(self._L.pa_alloc_export(self._h, words.ctypes.data_as(C.c_void_p), n.value, C.byref(n)),
+             "pa_alloc_export")
+        return words
+
+    @classmethod
+    def from_words(cls, words) -> "BlockAllocator":
+        """A new allocator with the state exported as `words` (pa_alloc_import)."""
+        w = np.ascontiguousarray(words, dtype=np.int64)
+        obj = cls.__new__(cls)
+        obj._L = _lib.lib()
+        h = C.c_void_p()
+        _chk(obj._L.pa_alloc_import(w.ctypes.data_as(C.c_void_p), int(w.size), C.byref(h)), "pa_alloc_import")
+        obj._h = h
+        obj.num_blocks = int(w[2])
+        obj.block_size = int(w[3])
+        obj._order_keepalive = None
+        return obj
+
     def close(self):
         if getattr(self, "_h", None):
             self._L.pa_alloc_destroy(self._h)

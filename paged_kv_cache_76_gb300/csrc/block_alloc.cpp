@@ -553,4 +553,194 @@ int pa_alloc_get_prefix_cache_stats(const pa_alloc* a, pa_prefix_cache_stats* ou
   return PA_OK;
 }
 
+// ---------------------------------------------------------------- checkpoint
+// The whole allocator as a flat list of int64 words (layout in include/pa.h);
+// map-ordered parts (sequences, cached hashes) are written in key order so
+// that equal states give equal words.
+namespace {
+constexpr int64_t kExportMagic = 0x504b5641ll;  // "PKVA"
+constexpr int64_t kExportVersion = 1;
+}  // namespace
+
+int pa_alloc_export(const pa_alloc* a, int64_t* out, int64_t cap, int64_t* n_out) {
+  if (!a || !n_out || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
+  std::vector<int64_t> w;
+  w.reserve(16 + 4 * (size_t)a->num_blocks);
+  w.push_back(kExportMagic);
+  w.push_back(kExportVersion);
+  w.push_back(a->num_blocks);
+  w.push_back(a->block_size);
+  w.push_back(a->caching ? 1 : 0);
+  w.push_back(a->num_cpu_blocks);
+  w.push_back(a->cow_copies);
+  w.push_back(a->alloc_failures);
+  w.push_back(a->lookup_blocks);
+  w.push_back(a->hit_blocks);
+  w.push_back(a->evictions);
+  w.push_back(a->num_free);
+  for (int32_t b = a->head; b >= 0; b = a->next[b]) w.push_back(b);
+  for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back(a->ref[b]);
+  for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back(a->has_hash[b]);
+  for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back((int64_t)a->hash[b]);
+  std::vector<std::pair<uint64_t, int32_t>> cached(a->cached.begin(), a->cached.end());
+  std::sort(cached.begin(), cached.end());
+  w.push_back((int64_t)cached.size());
+  for (const auto& kv : cached) {
+    w.push_back((int64_t)kv.first);
+    w.push_back(kv.second);
+  }
+  w.push_back(a->num_cpu_blocks > 0 ? a->cpu.n : 0);
+  if (a->num_cpu_blocks > 0)
+    for (int32_t b = a->cpu.head; b >= 0; b = a->cpu.next[b]) w.push_back(b);
+  std::vector<int> ids;
+  ids.reserve(a->seqs.size());
+  for (const auto& kv : a->seqs) ids.push_back(kv.first);
+  std::sort(ids.begin(), ids.end());
+  w.push_back((int64_t)ids.size());
+  for (int id : ids) {
+    const Seq& q = a->seqs.at(id);
+    w.push_back(id);
+    w.push_back(q.num_tokens);
+    w.push_back((int64_t)q.salt);
+    w.push_back((int64_t)q.parent);
+    w.push_back(q.hashable ? 1 : 0);
+    w.push_back(q.swapped ? 1 : 0);
+    w.push_back((int64_t)q.blocks.size());
+    for (int32_t b : q.blocks) w.push_back(b);
+    w.push_back((int64_t)q.pending.size());
+    for (int32_t t : q.pending) w.push_back(t);
+  }
+  *n_out = (int64_t)w.size();
+  if (cap < (int64_t)w.size()) return cap == 0 && !out ? PA_OK : PA_ERR_INVALID;
+  std::copy(w.begin(), w.end(), out);
+  return PA_OK;
+}
+
+int pa_alloc_import(const int64_t* words, int64_t n, pa_alloc** out) {
+  if (!words || n <= 0 || !out) return PA_ERR_INVALID;
+  *out = nullptr;
+  int64_t i = 0;
+  bool bad = false;
+  auto next = [&](int64_t lo, int64_t hi) -> int64_t {  // next word, required in [lo, hi]
+    if (bad || i >= n) {
+      bad = true;
+      return lo;
+    }
+    const int64_t v = words[i++];
+    if (v < lo || v > hi) bad = true;
+    return v;
+  };
+  auto raw = [&]() -> int64_t {
+    if (bad || i >= n) {
+      bad = true;
+      return 0;
+    }
+    return words[i++];
+  };
+  if (next(kExportMagic, kExportMagic) != kExportMagic || next(kExportVersion, kExportVersion) != kExportVersion)
+    return PA_ERR_INVALID;
+  const int32_t nb = (int32_t)next(1, INT32_MAX), bs = (int32_t)next(1, INT32_MAX);
+  const bool caching = next(0, 1) != 0;
+  const int32_t ncpu = (int32_t)next(0, INT32_MAX);
+  if (bad || nb > n) return PA_ERR_INVALID;  // every block takes at least three words below
+  pa_alloc* a = new (std::nothrow) pa_alloc();
+  if (!a) return PA_ERR_INVALID;
+  a->num_blocks = nb;
+  a->block_size = bs;
+  a->caching = caching;
+  a->cow_copies = next(0, INT64_MAX);
+  a->alloc_failures = next(0, INT64_MAX);
+  a->lookup_blocks = next(0, INT64_MAX);
+  a->hit_blocks = next(0, INT64_MAX);
+  a->evictions = next(0, INT64_MAX);
+  a->ref.assign(nb, 0);
+  a->prev.assign(nb, -1);
+  a->next.assign(nb, -1);
+  a->in_free.assign(nb, 0);
+  a->hash.assign(nb, 0);
+  a->has_hash.assign(nb, 0);
+  const int64_t nfree = next(0, nb);
+  for (int64_t k = 0; !bad && k < nfree; ++k) {
+    const int32_t b = (int32_t)next(0, nb - 1);
+    if (!bad && a->in_free[b]) bad = true;
+    if (!bad) a->push_back(b);
+  }
+  for (int32_t b = 0; !bad && b < nb; ++b) a->ref[b] = (int32_t)next(0, INT32_MAX);
+  for (int32_t b = 0; !bad && b < nb; ++b) a->has_hash[b] = (uint8_t)next(0, 1);
+  for (int32_t b = 0; !bad && b < nb; ++b) a->hash[b] = (uint64_t)raw();
+  for (int32_t b = 0; !bad && b < nb; ++b)
+    if (a->in_free[b] && a->ref[b] != 0) bad = true;  // a free block has no owner
+  const int64_t ncached = next(0, nb);
+  for (int64_t k = 0; !bad && k < ncached; ++k) {
+    const uint64_t h = (uint64_t)raw();
+    const int32_t b = (int32_t)next(0, nb - 1);
+    if (!bad && (!a->has_hash[b] || a->hash[b] != h || !a->cached.emplace(h, b).second)) bad = true;
+  }
+  const int64_t ncpu_free = next(0, ncpu);
+  if (!bad && ncpu > 0) {
+    a->num_cpu_blocks = ncpu;
+    a->cpu.prev.assign(ncpu, -1);
+    a->cpu.next.assign(ncpu, -1);
+    std::vector<uint8_t> seen(ncpu, 0);
+    for (int64_t k = 0; !bad && k < ncpu_free; ++k) {
+      const int32_t b = (int32_t)next(0, ncpu - 1);
+      if (bad || seen[b]) {
+        bad = true;
+        break;
+      }
+      seen[b] = 1;
+      a->cpu.prev[b] = a->cpu.tail;  // append at the tail, in the exported order
+      if (a->cpu.tail < 0) a->cpu.head = b; else a->cpu.next[a->cpu.tail] = b;
+      a->cpu.tail = b;
+      ++a->cpu.n;
+    }
+  }
+  const int64_t nseq = next(0, n);
+  for (int64_t k = 0; !bad && k < nseq; ++k) {
+    const int id = (int)next(0, INT32_MAX);
+    Seq q;
+    q.num_tokens = next(0, INT64_MAX);
+    q.salt = (uint64_t)raw();
+    q.parent = (uint64_t)raw();
+    q.hashable = next(0, 1) != 0;
+    q.swapped = next(0, 1) != 0;
+    if (q.swapped && ncpu == 0) bad = true;
+    const int64_t nbk = next(0, n);
+    const int32_t lim = q.swapped ? ncpu : nb;
+    for (int64_t t = 0; !bad && t < nbk; ++t) q.blocks.push_back((int32_t)next(0, (int64_t)lim - 1));
+    if (!bad && (int64_t)q.blocks.size() * bs < q.num_tokens) bad = true;  // tokens beyond the blocks
+    const int64_t np = next(0, n);
+    for (int64_t t = 0; !bad && t < np; ++t) q.pending.push_back((int32_t)next(INT32_MIN, INT32_MAX));
+    if (!bad && !a->seqs.emplace(id, std::move(q)).second) bad = true;
+  }
+  if (!bad) {
+    // refcounts are the number of resident tables holding the block, a
+    // block is in the free queue exactly when nothing holds it, and no
+    // swapped-out table holds a free swap block
+    std::vector<int64_t> holders(nb, 0);
+    std::vector<uint8_t> cpu_free(ncpu > 0 ? ncpu : 0, 0);
+    for (int32_t b = a->cpu.head; ncpu > 0 && b >= 0; b = a->cpu.next[b]) cpu_free[b] = 1;
+    for (const auto& kv : a->seqs)
+      for (int32_t b : kv.second.blocks) {
+        if (kv.second.swapped) {
+          if (cpu_free[b]) bad = true;
+        } else {
+          ++holders[b];
+        }
+      }
+    for (int32_t b = 0; !bad && b < nb; ++b)
+      if (holders[b] != a->ref[b] || (a->ref[b] == 0) != (a->in_free[b] != 0)) bad = true;
+    // every hashed block is the cache's entry for its hash
+    int64_t hashed = 0;
+    for (int32_t b = 0; b < nb; ++b) hashed += a->has_hash[b];
+    if (hashed != (int64_t)a->cached.size()) bad = true;
+  }
+  if (bad || i != n) {
+    delete a;
+    return PA_ERR_INVALID;
+  }
+  *out = a;
+  return PA_OK;
+}
+
 }  // extern "C"

@@ -168,6 +168,27 @@ int main(int argc, char** argv) {
         hashed += c;
       }
       if (hashed != pst.cached_blocks) { std::printf("hash count %lld vs map %lld\n", (long long)hashed, (long long)pst.cached_blocks); return 8; }
+      if (i % 23 == 0) {
+        // checkpoint: the words import into an allocator with the same state,
+        // and a corrupted copy either imports or is refused, never misbehaves
+        int64_t nw = 0;
+        if (pa_alloc_export(a, nullptr, 0, &nw) != PA_OK || nw <= 0) return 10;
+        std::vector<int64_t> w(nw);
+        if (pa_alloc_export(a, w.data(), nw, &nw) != PA_OK) return 10;
+        pa_alloc* c = nullptr;
+        if (pa_alloc_import(w.data(), nw, &c) != PA_OK) { std::printf("import refused an export\n"); return 10; }
+        if (!(snap(c, live) == after)) { std::printf("imported state differs\n"); pa_alloc_destroy(c); return 10; }
+        std::vector<int64_t> w2(nw);
+        int64_t nw2 = 0;
+        if (pa_alloc_export(c, w2.data(), nw, &nw2) != PA_OK || nw2 != nw || w2 != w) { pa_alloc_destroy(c); return 10; }
+        pa_alloc_destroy(c);
+        std::vector<int64_t> x = w;
+        const size_t k = (size_t)(rng() % (uint64_t)nw);
+        x[k] += (int64_t)(rng() % 7) - 3;
+        pa_alloc* d = nullptr;
+        if (pa_alloc_import(x.data(), nw, &d) == PA_OK) pa_alloc_destroy(d);
+        if (pa_alloc_import(x.data(), nw - 1, &d) == PA_OK) { std::printf("truncated words imported\n"); pa_alloc_destroy(d); return 10; }
+      }
     }
     pa_alloc_destroy(a);
   }
