@@ -619,6 +619,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split", type=int, default=None, help="decode partition size (default: the workload's)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--jsonl", default=None, help="also append the result line to this file")
     ap.add_argument("--e2e-launch", default="auto", choices=["auto", "graph", "eager"],
                     help="kernels of each end-to-end step: eager launches marshalled once (ops.recording), or a "
                          "CUDA graph per buffer set; auto = eager for one-stream steps, graph for steps that fork "
@@ -731,7 +732,10 @@ def main():
                     flush.fill_(i & 0xFF)
                 step.run(stream, evs[i])
         stream.synchronize()
-        dec_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        launch_ms = np.array([a.elapsed_time(b) for a, b in evs])
+        dec_ms = float(np.mean(launch_ms))
+        launch_pct = {"launch_ms_p50": round(float(np.percentile(launch_ms, 50)), 5),
+                      "launch_ms_p99": round(float(np.percentile(launch_ms, 99)), 5)}
 
     # e2e: host buffers through the public API.  Every step copies its inputs
     # from pinned host memory (one buffer), runs the kernels (a CUDA graph per
@@ -909,6 +913,7 @@ def main():
             "prefix_tokens": step.prefix_len,
             "prefix_tflops": round(flops / (dec_ms * 1e-3) / 1e12, 1),
             "avg_launch_ms": round(dec_ms, 5),
+            **launch_pct,
             "timing": "CUDA events around each of K pa_decode_shared_prefix calls (3 kernels) on the bench "
                       "stream, in a second pass of the same K steps",
         }
@@ -932,6 +937,7 @@ def main():
             "traffic": traffic,
             "algorithmic_bytes_per_launch": dec_bytes,
             "avg_launch_ms": round(dec_ms, 5),
+            **launch_pct,
             "timing": (f"CUDA events around each of K pa_verify_decode calls (partial + merge kernels) on the "
                        f"bench stream, in a second pass of the same K steps" if verify else
                        "CUDA events around each of K contiguous decode calls (partial + merge kernels) on the "
@@ -963,6 +969,7 @@ def main():
             "traffic": ptraffic,
             "algorithmic_flops_per_launch": fl,
             "avg_launch_ms": round(dec_ms, 5),
+            **launch_pct,
             "timing": "CUDA events around each of K chunked-prefill launches on the bench stream, in a second "
                       "pass of the same K steps",
         }
@@ -984,6 +991,9 @@ def main():
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(res))
+        if args.jsonl:
+            with open(args.jsonl, "a") as f:
+                f.write(json.dumps(res) + "\n")
 
 
 def reference_arm(args, step, ws, rank, peak):
