@@ -888,7 +888,8 @@ def main():
         if step.vkv is not None:
             vs = step.vkv.stats()
             res["config"]["vmm"] = {"page_bytes": vs["page_bytes"], "pages_mapped": vs["pages_mapped"],
-                                    "bytes_committed": vs["bytes_committed"], "bytes_reserved": vs["bytes_reserved"],
+                                    "bytes_committed": vs["bytes_committed"], "bytes_used": vs["bytes_used"],
+                                    "step_failures": vs["step_failures"], "bytes_reserved": vs["bytes_reserved"],
                                     "map_calls": vs["map_calls"],
                                     "map_us_per_page": round(vs["total_map_ns"] / max(1, vs["map_calls"]) / 1e3, 2),
                                     "setup_s": round(step.vmm_setup_s, 3)}

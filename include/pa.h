@@ -281,6 +281,9 @@ typedef struct {
   int64_t last_step_map_ns;  /* host time the last pa_vkv_step spent mapping   */
   int64_t total_map_ns;
   int64_t active_slots;
+  int64_t step_failures;     /* pa_vkv_step calls refused for want of pages   */
+  int64_t bytes_used;        /* K/V bytes of the last step's tokens; tail
+                                waste = bytes_committed - bytes_used        */
 } pa_vkv_stats;
 
 int pa_vkv_granularity(size_t* out);

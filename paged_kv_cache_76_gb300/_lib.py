@@ -56,7 +56,8 @@ class PrefixCacheStats(C.Structure):
 class VkvStats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in (
         "page_bytes", "slot_pages", "pages_mapped", "pages_pooled", "pages_created", "map_calls", "unmap_calls",
-        "bytes_reserved", "bytes_committed", "last_step_map_ns", "total_map_ns", "active_slots")]
+        "bytes_reserved", "bytes_committed", "last_step_map_ns", "total_map_ns", "active_slots",
+        "step_failures", "bytes_used")]
 
 
 PA_VKV_DRY_RUN = 1

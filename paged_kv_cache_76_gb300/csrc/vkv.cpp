@@ -95,6 +95,8 @@ struct pa_vkv {
   std::vector<CUmemGenericAllocationHandle> handles;
   std::vector<CUmemGenericAllocationHandle> pool;  // created, unmapped
   int64_t created = 0, map_calls = 0, unmap_calls = 0;
+  int64_t step_failures = 0;  // pa_vkv_step calls refused for want of pages
+  int64_t tokens_held = 0;    // tokens of the last successful step, all slots
   int64_t last_map_ns = 0, total_map_ns = 0;
   int32_t* d_slot_tokens = nullptr;
   std::vector<int32_t> h_slot_tokens;
@@ -258,7 +260,10 @@ int pa_vkv_step(pa_vkv* v, const int32_t* lens, pa_stream stream) {
     int64_t reclaimable = 0;
     for (int s = 0; s < v->B; ++s)
       if (!v->active[s]) reclaimable += (int64_t)v->mapped[s] * v->tensors;
-    if (reclaimable < short_by) return PA_ERR_NO_FREE_BLOCKS;
+    if (reclaimable < short_by) {
+      ++v->step_failures;
+      return PA_ERR_NO_FREE_BLOCKS;
+    }
     std::vector<int> donors;
     for (int s = 0; s < v->B && short_by > 0; ++s) {
       if (v->active[s] || v->mapped[s] == 0) continue;
@@ -297,6 +302,7 @@ int pa_vkv_step(pa_vkv* v, const int32_t* lens, pa_stream stream) {
       CUmemGenericAllocationHandle h = 0;
       if (d.create(&h, (size_t)v->G, &prop, 0) != CUDA_SUCCESS) {
         for (auto x : got) v->pool.push_back(x);
+        ++v->step_failures;
         return PA_ERR_NO_FREE_BLOCKS;
       }
       ++v->created;
@@ -326,6 +332,8 @@ int pa_vkv_step(pa_vkv* v, const int32_t* lens, pa_stream stream) {
     }
   v->last_map_ns =
       std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now() - t0).count();
+  v->tokens_held = 0;
+  for (int s = 0; s < v->B; ++s) v->tokens_held += lens[s];
   v->total_map_ns += v->last_map_ns;
   bool changed = false;
   for (int s = 0; s < v->B; ++s) {
@@ -377,6 +385,8 @@ int pa_vkv_get_stats(const pa_vkv* v, pa_vkv_stats* out) {
   int64_t act = 0;
   for (char a : v->active) act += a ? 1 : 0;
   st.active_slots = act;
+  st.step_failures = v->step_failures;
+  st.bytes_used = v->tokens_held * v->row * v->tensors;
   *out = st;
   return PA_OK;
 }

@@ -57,6 +57,7 @@ def test_random_scripts_match_the_oracle(seed):
     c = _c(B, L, layers, hkv, d, page_bytes=page, max_pages=budget)
     o = OVirtualKV(B, L, layers, hkv, d, 2, page, budget)
     lens = [0] * B
+    refused = 0
     for step in range(300):
         kind = rng.choice(["alloc", "free", "step", "step", "step", "bad"])
         if kind == "alloc":
@@ -77,6 +78,11 @@ def test_random_scripts_match_the_oracle(seed):
             assert rc[0] == ro[0], (step, rc, ro)
             if rc[0] == "ok":
                 lens = new
+                # the monitoring counters: bytes the tokens hold, refused steps
+                assert c.stats()["bytes_used"] == sum(lens) * row * 2 * layers
+            elif rc[0] == "nopages":
+                refused += 1
+            assert c.stats()["step_failures"] == refused
         else:  # a length past the reservation, or on an inactive slot
             bad = [0] * B
             bad[int(rng.integers(0, B))] = L + 16
