@@ -27,10 +27,19 @@ Modules:
   prefill.  Pinned by the tests in ``tests/test_oracle_pins.py``.
 * ``block_pool``: free queue, block pool and per-sequence manager.  Pinned by
   ``tests/test_oracle_allocator.py``.
-* ``sizing``: KV byte counts.  Pinned by the worked numbers on the vAttention
-  page.
+* ``sizing``: KV byte counts (the vAttention page's closed form; the bytes
+  a decode step moves, logical and with shared rows counted once).  Pinned
+  by the page's worked numbers and by a brute-force count of the array
+  elements a step touches.
+* ``vattention``: the vAttention-style manager's bookkeeping.  Pinned by
+  ``tests/test_oracle_vattention.py`` (the page's formulas, numbers and
+  figure 2 walk-through; numpy's own row-major addressing for slot rows).
 
-Parity status: every function here is pinned (see the tests named above);
-nothing is "parity unpinned".
+Parity status: every public function here has at least one pin that does not
+restate its own formula (a printed value, a library routine, a brute-force
+count or an invariant); ``tests/`` names it beside each test.  The one part
+the pages leave undecided is the free-queue placement of released blocks,
+where the two editions' listings disagree; the reading taken is stated in
+``block_pool`` and pinned by the allocator tests.
 """
-from . import block_pool, paged_attention, sizing  # noqa: F401
+from . import block_pool, paged_attention, sizing, vattention  # noqa: F401

@@ -11,6 +11,13 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
   Table on demand (a new block only when the last one is full, §3), and frees
   its blocks in reverse order when it ends (tail blocks first).
 
+BlockPool's get_new_blocks, free_blocks and touch take the steps of the
+pages' BlockPool listing (§9.3) in the listing's order, and keep its names
+for the lists they build (to_free, no_hash, has_hash), by design: the listing
+is the only definition of the allocator's semantics that the pages give, and
+this module is the oracle that restates it.  The product allocator is a
+separate design and does not follow the listing's structure.
+
 Sharing and Copy-on-Write follow §6: tables may point at the same physical
 block (refcount = number of tables), and a request about to write a shared
 block first copies it into a private one, repoints its table entry and drops

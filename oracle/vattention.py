@@ -135,9 +135,6 @@ class VirtualKV:
     def committed_bytes(self) -> int:
         return self.pages_in_use() * self.G
 
-    def used_bytes(self, lens) -> int:
-        return sum(int(n) for n in lens) * self.h * self.tensors
-
     def run(self, ops):
         """Replay a script of ("alloc",) / ("free", slot) / ("step", lens) ops; returns alloc results."""
         got = []

@@ -386,6 +386,98 @@ def test_kv_size_closed_form_matches_the_printed_numbers():
     assert 2 * t["layers"] * t["page_mb"] == t["printed_mb"]
 
 
-def test_decode_step_bytes_counts_each_term():
-    # one request, L=17, Hq=4, Hkv=2, D=8, bs=16: KV 2*17*2*8*2, q+o 2*4*8*2, table 2 blocks*4, len 4
-    assert sizing.decode_step_bytes([17], 4, 2, 8, 16) == 1088 + 128 + 8 + 4
+def _touched_bytes(tables, lens, Hq, Hkv, D, bs, q_len, nb, unique):
+    """Brute force: mark every array element one decode step reads or writes.
+
+    Real arrays of the step's dtypes (fp16 cache, q and out; int32 tables and
+    lengths) get one boolean mask each; every (request, logical token) marks
+    its K and V rows through the Block Table, and each request marks its
+    query and output rows, the table entries that cover its tokens and its
+    length.  Bytes = marked elements x itemsize, summed over the arrays.
+    With ``unique`` the K/V masks are shared by the batch (a row read twice
+    counts once); otherwise every request gets fresh K/V masks.
+    """
+    B = len(lens)
+    arrays = {
+        "k": np.zeros((nb, bs, Hkv, D), np.float16), "v": np.zeros((nb, bs, Hkv, D), np.float16),
+        "q": np.zeros((B, q_len, Hq, D), np.float16), "o": np.zeros((B, q_len, Hq, D), np.float16),
+        "table": np.asarray(tables, np.int32), "lens": np.asarray(lens, np.int32),
+    }
+    total = 0
+
+    def fresh(names):
+        return {n: np.zeros(arrays[n].shape, bool) for n in names}
+
+    masks = fresh(arrays)
+    for r in range(B):
+        if not unique and r:
+            for n, m in fresh(["k", "v"]).items():
+                total += int(masks[n].sum()) * arrays[n].itemsize
+                masks[n] = m
+        for t in range(int(lens[r])):
+            blk = int(arrays["table"][r][t // bs])
+            masks["k"][blk, t % bs] = True
+            masks["v"][blk, t % bs] = True
+            masks["table"][r, t // bs] = True
+        masks["q"][r] = True
+        masks["o"][r] = True
+        masks["lens"][r] = True
+    for n, m in masks.items():
+        total += int(m.sum()) * arrays[n].itemsize
+    return total
+
+
+@pytest.mark.parametrize("q_len", [1, 4])
+def test_decode_step_bytes_equals_a_count_of_touched_elements(q_len):
+    rng = np.random.default_rng(11)
+    Hq, Hkv, D, bs, nb = 6, 2, 8, 4, 40
+    lens = [1, 4, 5, 13, 0, 9]
+    perm = rng.permutation(nb)
+    tables, k = [], 0
+    for L in lens:  # private blocks for every request: no row is shared
+        n = -(-L // bs)
+        tables.append(list(perm[k:k + n]) + [-1] * (4 - n))
+        k += n
+    want = _touched_bytes(tables, lens, Hq, Hkv, D, bs, q_len, nb, unique=False)
+    assert sizing.decode_step_bytes(lens, Hq, Hkv, D, bs, 2, q_len) == want
+    # nothing shared: every row is unique, so the two counts agree
+    assert sizing.unique_kv_bytes(tables, lens, Hq, Hkv, D, bs, 2, q_len) == want
+    assert _touched_bytes(tables, lens, Hq, Hkv, D, bs, q_len, nb, unique=True) == want
+
+
+def test_unique_kv_bytes_counts_a_shared_prefix_once():
+    """"2.1 PagedAttention" §6: Block Tables of several requests point at one
+    prefix.  Three requests share two full blocks and a third, partial one
+    (read to different depths); each has a private tail."""
+    Hq, Hkv, D, bs, nb = 4, 1, 8, 4, 16
+    shared = [3, 7, 9]
+    tables = [shared + [0, -1], shared + [5, 6], shared + [-1, -1]]
+    lens = [13, 19, 10]      # tokens 0-7 (blocks 3, 7) by all; block 9 to depth 4, 4, 2
+    brute = _touched_bytes(tables, lens, Hq, Hkv, D, bs, 1, nb, unique=True)
+    assert sizing.unique_kv_bytes(tables, lens, Hq, Hkv, D, bs) == brute
+    # by hand: distinct rows = 8 (blocks 3, 7) + 4 (block 9) + 1 (block 0) + 4 + 3 (blocks 5, 6) = 20
+    row = 2 * Hkv * D * 2
+    per_req = sum(2 * Hq * D * 2 + 4 * (-(-L // bs)) + 4 for L in lens)
+    assert brute == 20 * row + per_req
+    # the logical count reads the shared rows once per request
+    assert sizing.decode_step_bytes(lens, Hq, Hkv, D, bs) == sum(lens) * row + per_req
+
+
+def test_unique_kv_bytes_of_a_2048_token_shared_prefix():
+    """The prefix-shared decode shape: a 2048-token prefix is 128 blocks of 16
+    tokens held by every request (refcount = batch), then private suffixes.
+    Closed form: (2048 + sum of suffixes) K+V rows, plus the per-request terms."""
+    Hq, Hkv, D, bs = 4, 2, 8, 16
+    prefix_blocks = list(range(100, 228))
+    assert len(prefix_blocks) * bs == 2048
+    suffix = [16, 17, 40, 512, 1]
+    tables, nxt = [], 1000
+    for s in suffix:
+        n = -(-s // bs)
+        tables.append(prefix_blocks + list(range(nxt, nxt + n)))
+        nxt += n
+    lens = [2048 + s for s in suffix]
+    row = 2 * Hkv * D * 2
+    per_req = sum(2 * Hq * D * 2 + 4 * (-(-L // bs)) + 4 for L in lens)
+    assert sizing.unique_kv_bytes(tables, lens, Hq, Hkv, D, bs) == (2048 + sum(suffix)) * row + per_req
+    assert sizing.decode_step_bytes(lens, Hq, Hkv, D, bs) == (5 * 2048 + sum(suffix)) * row + per_req

@@ -5,12 +5,40 @@ import json
 import os
 import random
 
+import numpy as np
 import pytest
 
 from oracle.vattention import NoPages, VAttnError, VirtualKV, pages_for, slot_row, tail_commit_bytes
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "kv_sizing.json")
 MiB = 1 << 20
+
+
+def test_slot_row_is_numpys_row_of_the_contiguous_layout():
+    """Brute force: a [slots][max_len][H][D] array, flattened to token rows by
+    numpy, holds token t of slot s at row slot_row(s, t, max_len)."""
+    S, L, H, D = 3, 7, 2, 4
+    a = np.arange(S * L * H * D).reshape(S, L, H, D)
+    rows = a.reshape(S * L, H, D)
+    for s in range(S):
+        for t in range(L):
+            assert np.array_equal(rows[slot_row(s, t, L)], a[s, t])
+
+
+def test_slot_row_lands_on_the_pages_offset_of_the_request_slot():
+    """"vAttention 完全拆解", core abstraction: slot reqId of a [B][L][H][D]
+    tensor starts at byte offset(reqId) = reqId * L * H * D * P.  Numpy's
+    row-major index of (reqId, t, 0, 0) in the Yi-34B worker's shape (golden
+    fixture: L = 200000, H = 4, D = 128, P = 2), times P, must equal the
+    page's offset plus t rows, and the row slot_row gives times the row size."""
+    g = json.load(open(GOLDEN))["per_layer_k_or_v_slot"]
+    L, H, D, P = g["length"], g["kv_heads"], g["head_dim"], g["elem_bytes"]
+    B = 500
+    for req, t in [(0, 0), (1, 0), (3, 5), (499, 199999), (250, 123456)]:
+        byte = int(np.ravel_multi_index((req, t, 0, 0), (B, L, H, D))) * P
+        assert byte == req * L * H * D * P + t * H * D * P       # the page's offset(reqId), then t rows
+        assert slot_row(req, t, L) * H * D * P == byte
+    assert L * H * D * P == g["exact_bytes"]                     # one slot = the printed ~200 MB
 
 
 def test_pages_for_is_the_page_formula_with_whole_tiles():
@@ -79,7 +107,8 @@ def test_figure_two_walkthrough():
     lens[r3] = per_page + 40
     v.step(lens)
     assert v.map_calls == calls and v.mapped[r3] == 2      # ... and its mapped pages
-    assert slot_row(r3, 5, v.L) == r3 * v.L + 5
+    # R3 reads its token 5 from the row the page's offset(reqId) puts it at
+    assert slot_row(r3, 5, v.L) * h == r3 * v.L * 1 * 512 * 2 + 5 * 1 * 512 * 2   # offset(reqId) + 5 rows
 
 
 def test_shortage_is_all_or_nothing_and_reclaims_inactive_slots_first():
