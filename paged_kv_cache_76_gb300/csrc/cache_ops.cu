@@ -188,9 +188,7 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t
   const int row_vecs = row_bytes / 16;
   const int64_t total = (int64_t)num_tokens * row_vecs;
   if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  return launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+  return launch_pdl(reshape_and_cache_kernel, dim3(copy_grid(total)), dim3(256), 0, stream,
                     static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, static_cast<uint4*>(k_cache),
                     static_cast<uint4*>(v_cache), num_tokens, row_vecs, num_slots, err);
 }
@@ -202,9 +200,7 @@ cudaError_t launch_reshape_and_cache_slots(const void* k, const void* v, const i
   const int row_vecs = row_bytes / 16;
   const int64_t total = (int64_t)num_tokens * row_vecs;
   if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  return launch_pdl(reshape_and_cache_slots_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+  return launch_pdl(reshape_and_cache_slots_kernel, dim3(copy_grid(total)), dim3(256), 0, stream,
                     static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_ids, positions,
                     static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, row_vecs, num_slots,
                     contig_len, slot_tokens, err);

@@ -266,6 +266,8 @@ int shared_prefix_setup(int num_seqs, int q_heads, int head_dim, int max_blocks_
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+int num_sms() { return sm_count(); }
+
 }  // namespace pa
 
 using namespace pa;

@@ -128,6 +128,15 @@ cudaError_t launch_chunked_prefill(const CUtensorMap& kmap, const CUtensorMap& v
 cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_attn_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int head_dim,
                            int bsub, pa_dtype dt, cudaStream_t stream);
+// SMs of the current device (cached per device; 0 if the query fails).
+int num_sms();
+// Grid of a grid-stride copy kernel: enough 256-thread CTAs for `total`
+// vectors, at most 16 per SM of the current device.
+inline unsigned copy_grid(int64_t total) {
+  const int64_t cap = 16 * (int64_t)(num_sms() > 0 ? num_sms() : 1);
+  const int64_t want = (total + 255) / 256;
+  return (unsigned)(want < cap ? want : cap);
+}
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
                                      void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,
                                      cudaStream_t stream);
