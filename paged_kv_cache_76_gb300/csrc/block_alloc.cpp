@@ -709,27 +709,31 @@ int pa_alloc_import(const int64_t* words, int64_t n, pa_alloc** out) {
     const int32_t lim = q.swapped ? ncpu : nb;
     for (int64_t t = 0; !bad && t < nbk; ++t) q.blocks.push_back((int32_t)next(0, (int64_t)lim - 1));
     if (!bad && (int64_t)q.blocks.size() * bs < q.num_tokens) bad = true;  // tokens beyond the blocks
-    const int64_t np = next(0, n);
+    const int64_t np = next(0, (int64_t)bs - 1);  // token ids of a block not yet full
     for (int64_t t = 0; !bad && t < np; ++t) q.pending.push_back((int32_t)next(INT32_MIN, INT32_MAX));
     if (!bad && !a->seqs.emplace(id, std::move(q)).second) bad = true;
   }
   if (!bad) {
     // refcounts are the number of resident tables holding the block, a
-    // block is in the free queue exactly when nothing holds it, and no
-    // swapped-out table holds a free swap block
+    // block is in the free queue exactly when nothing holds it, and every
+    // swap block is either in the swap pool's free queue or held by exactly
+    // one swapped-out table, exactly once (swap blocks are never shared)
     std::vector<int64_t> holders(nb, 0);
+    std::vector<int64_t> cpu_holders(ncpu > 0 ? ncpu : 0, 0);
     std::vector<uint8_t> cpu_free(ncpu > 0 ? ncpu : 0, 0);
     for (int32_t b = a->cpu.head; ncpu > 0 && b >= 0; b = a->cpu.next[b]) cpu_free[b] = 1;
     for (const auto& kv : a->seqs)
       for (int32_t b : kv.second.blocks) {
         if (kv.second.swapped) {
-          if (cpu_free[b]) bad = true;
+          ++cpu_holders[b];
         } else {
           ++holders[b];
         }
       }
     for (int32_t b = 0; !bad && b < nb; ++b)
       if (holders[b] != a->ref[b] || (a->ref[b] == 0) != (a->in_free[b] != 0)) bad = true;
+    for (int32_t b = 0; !bad && b < ncpu; ++b)
+      if (cpu_holders[b] + cpu_free[b] != 1) bad = true;
     // every hashed block is the cache's entry for its hash
     int64_t hashed = 0;
     for (int32_t b = 0; b < nb; ++b) hashed += a->has_hash[b];

@@ -142,6 +142,63 @@ def test_malformed_words_are_refused():
             BlockAllocator.from_words(v)
 
 
+def _seq_words(w):
+    """Index of each sequence's record in exported words: {seq id: (index of its
+    block count, index of its pending count)}, following the export layout."""
+    nb = int(w[2])
+    i = 11
+    nfree = int(w[i]); i += 1 + nfree
+    i += 3 * nb                                   # refcounts, hash flags, hashes
+    ncached = int(w[i]); i += 1 + 2 * ncached
+    ncpu_free = int(w[i]); i += 1 + ncpu_free
+    nseq = int(w[i]); i += 1
+    out = {}
+    for _ in range(nseq):
+        sid = int(w[i])
+        nblk_at = i + 6
+        nblk = int(w[nblk_at])
+        np_at = nblk_at + 1 + nblk
+        out[sid] = (nblk_at, np_at)
+        i = np_at + 1 + int(w[np_at])
+    assert i == len(w)
+    return out
+
+
+def test_a_swap_block_held_twice_is_refused():
+    """Two swapped-out sequences must not hold the same swap block, and no
+    swap block may be neither free nor held (it would leak, and the next two
+    swap-outs would both get the other one)."""
+    a = BlockAllocator(8, 4)
+    a.enable_swap(4)
+    for s in (1, 2):
+        a.add_seq(s)
+        a.append_slots(s, 3)
+        a.swap_out(s)
+    w = a.export()
+    BlockAllocator.from_words(w)
+    at = _seq_words(w)
+    b1, b2 = int(w[at[1][0] + 1]), int(w[at[2][0] + 1])
+    assert b1 != b2
+    x = w.copy()
+    x[at[2][0] + 1] = b1                          # sequence 2 now claims sequence 1's swap block
+    with pytest.raises(_lib.PAError):
+        BlockAllocator.from_words(x)
+
+
+def test_pending_tokens_of_a_full_block_are_refused():
+    w = _valid_words()
+    at = _seq_words(w)
+    sid = next(s for s, (_, p) in at.items() if int(w[p]) > 0)
+    p = at[sid][1]
+    n = int(w[p])
+    x = np.concatenate([w[:p], [4], w[p + 1:p + 1 + n], np.zeros(4 - n, w.dtype), w[p + 1 + n:]])
+    assert len(x) == len(w) + 4 - n
+    with pytest.raises(_lib.PAError):             # block_size 4: at most 3 pending token ids
+        BlockAllocator.from_words(x)
+    y = np.concatenate([w[:p], [3], w[p + 1:p + 1 + n], np.zeros(3 - n, w.dtype), w[p + 1 + n:]])
+    BlockAllocator.from_words(y)                  # 3 is still a valid count
+
+
 def test_random_corruptions_never_crash_and_what_imports_round_trips():
     w = _valid_words()
     rng = np.random.default_rng(4)
