@@ -96,7 +96,7 @@ struct pa_vkv {
   std::vector<CUmemGenericAllocationHandle> pool;  // created, unmapped
   int64_t created = 0, map_calls = 0, unmap_calls = 0;
   int64_t step_failures = 0;  // pa_vkv_step calls refused for want of pages
-  int64_t tokens_held = 0;    // tokens of the last successful step, all slots
+  std::vector<int32_t> held;  // per slot: tokens of the last successful step (0 once the slot is freed)
   int64_t last_map_ns = 0, total_map_ns = 0;
   int32_t* d_slot_tokens = nullptr;
   std::vector<int32_t> h_slot_tokens;
@@ -190,6 +190,7 @@ int pa_vkv_create(int num_slots, int max_len, int num_layers, int kv_heads, int 
   v->tensor_bytes = (int64_t)num_slots * slot_bytes;
   v->mapped.assign(num_slots, 0);
   v->active.assign(num_slots, 0);
+  v->held.assign(num_slots, 0);
   v->h_slot_tokens.assign(num_slots, 0);
   if (!dry) {
     const Driver& d = driver();
@@ -242,6 +243,7 @@ int pa_vkv_alloc_slot(pa_vkv* v, int* slot_out) {
 int pa_vkv_free_slot(pa_vkv* v, int slot) {
   if (!v || slot < 0 || slot >= v->B || !v->active[slot]) return PA_ERR_INVALID;
   v->active[slot] = 0;  // its pages stay mapped for the slot's next request
+  v->held[slot] = 0;    // but its tokens no longer count as used
   return PA_OK;
 }
 
@@ -332,8 +334,7 @@ int pa_vkv_step(pa_vkv* v, const int32_t* lens, pa_stream stream) {
     }
   v->last_map_ns =
       std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now() - t0).count();
-  v->tokens_held = 0;
-  for (int s = 0; s < v->B; ++s) v->tokens_held += lens[s];
+  for (int s = 0; s < v->B; ++s) v->held[s] = lens[s];  // nonzero only on active slots (checked above)
   v->total_map_ns += v->last_map_ns;
   bool changed = false;
   for (int s = 0; s < v->B; ++s) {
@@ -386,7 +387,9 @@ int pa_vkv_get_stats(const pa_vkv* v, pa_vkv_stats* out) {
   for (char a : v->active) act += a ? 1 : 0;
   st.active_slots = act;
   st.step_failures = v->step_failures;
-  st.bytes_used = v->tokens_held * v->row * v->tensors;
+  int64_t tokens = 0;
+  for (int s = 0; s < v->B; ++s) tokens += v->active[s] ? v->held[s] : 0;
+  st.bytes_used = tokens * v->row * v->tensors;
   *out = st;
   return PA_OK;
 }

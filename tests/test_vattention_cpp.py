@@ -69,6 +69,8 @@ def test_random_scripts_match_the_oracle(seed):
             assert rc[0] == ro[0]
             if rc[0] == "ok":
                 lens[s] = 0
+                # a freed slot's tokens stop counting at once, before the next step
+                assert c.stats()["bytes_used"] == sum(lens) * row * 2 * layers
         elif kind == "step":
             new = list(lens)
             for s in range(B):
@@ -87,6 +89,12 @@ def test_random_scripts_match_the_oracle(seed):
             bad = [0] * B
             bad[int(rng.integers(0, B))] = L + 16
             assert _do(c, "step", np.array(bad))[0] == _do(o, "step", bad)[0] == "err"
+            idle = [s for s in range(B) if not o.active[s]]
+            if idle:
+                bad = list(lens)
+                bad[idle[0]] = 16
+                assert _do(c, "step", np.array(bad))[0] == _do(o, "step", bad)[0] == "err"
+            assert c.stats()["bytes_used"] == sum(lens) * row * 2 * layers
         _same(c, o)
 
 
