@@ -435,7 +435,10 @@ int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* con
  *   workspace then.  Requests that fit one partition need no scratch.
  * - Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is looked up again when the
+ *   device's current context changes (after cudaDeviceReset the library's
+ *   device code is loaded anew and the array may move); the first call after
+ *   such a reset should also come before any capture.
  * - Sharing: all calls share the one array, which keeps the last call's
  *   contents.  Nothing in it has to start at zero (every partial the merge
  *   reads is written earlier in the same call).  Calls that overlap on the

@@ -11,8 +11,11 @@
 // The array is a file-scope __device__ variable of PA_DECODE_NOALLOC_SCRATCH_BYTES:
 // every GPU that loads the library holds it until the process exits.  Host
 // code must not pass the array's name to a kernel (on the host it is only a
-// stand-in symbol); the device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call there.
+// stand-in symbol); the device address is looked up with cudaGetSymbolAddress,
+// with that device current, on the first call there, and again whenever the
+// device's current context is not the one the address was taken in (after
+// cudaDeviceReset, or once the primary context was released and created anew,
+// the module is loaded again and the array may sit at another address).
 #include <mutex>
 
 #include "pa_internal.h"
@@ -26,18 +29,48 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // id of the context each address belongs to
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context; 0 if there is none yet
+// or the driver cannot say (then the address is looked up on every call).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<CtxGetCurrentFn>(fn)
+               : nullptr;
+  }();
+  static CtxGetIdFn get_id = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<CtxGetIdFn>(fn)
+               : nullptr;
+  }();
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 // Device address of the scratch array on the current device (nullptr on error).
 void* scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-    g_scratch_ptr[dev] = p;
-  }
-  return g_scratch_ptr[dev];
+  if (g_scratch_ptr[dev] && ctx != 0 && ctx == g_scratch_ctx[dev]) return g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+  g_scratch_ptr[dev] = p;
+  g_scratch_ctx[dev] = current_context_id();  // the lookup made the device's context current
+  return p;
 }
 
 }  // namespace
