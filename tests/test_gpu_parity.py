@@ -100,6 +100,18 @@ DECODE_CASES = [
     # the largest partitions (256 table entries per warp) on both block sizes
     (8, 2, 128, 16, "bf16", [4096, 4097, 9000, 1], 4096),
     (4, 1, 64, 4, "fp16", [1024, 1025, 2100], 1024),
+    # 16-token partitions: exactly 32 partitions in the widest row (the
+    # one-warp merge at its limit, lane c = partition c) ...
+    (8, 2, 128, 16, "bf16", [512, 500, 17, 1], 16),
+    (16, 4, 64, 16, "fp16", [511, 512, 33], 16),
+    # ... and more than 32 (the block-per-row merge), up to 512 partitions
+    (8, 2, 128, 16, "bf16", [1, 512, 513, 528, 2000], 16),
+    (16, 4, 64, 16, "fp16", [2000, 512, 513, 528, 1], 16),
+    (8, 8, 128, 16, "fp16", [3000, 700, 16], 16),
+    (16, 4, 64, 16, "bf16", [528, 16, 4000], 16),
+    (4, 1, 64, 4, "bf16", [128, 129, 700], 16),
+    (16, 2, 128, 32, "bf16", [1024, 1056, 2000], 32),
+    (64, 8, 128, 16, "bf16", [8192, 4097, 33], 16),
 ]
 
 

@@ -56,6 +56,10 @@ VERIFY_CASES = [
     (5, 12, 2, 64, 8, "fp16", [300, 77, 5], 0),                    # 30 columns
     (6, 4, 1, 128, 16, "bf16", [4096, 3000], 512),                 # 24 columns, many partitions
     (1, 28, 4, 128, 16, "bf16", [300, 1029], 256),                 # q_len 1
+    # 16-token partitions: more than 32 per row (the block-per-row merge)
+    (4, 32, 8, 128, 16, "bf16", [512, 2000, 515, 3], 16),
+    (4, 16, 4, 64, 16, "fp16", [1500, 40, 513], 16),
+    (8, 32, 8, 128, 16, "bf16", [1030, 9, 600], 16),
 ]
 
 
@@ -71,6 +75,21 @@ def test_verify_matches_the_oracle(case):
         for i in range(q_len):
             if L - (q_len - 1 - i) <= 0:
                 assert torch.count_nonzero(out[r, i]) == 0
+    assert ops().get_device_error() == 0
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_verify_with_exactly_32_partitions(dt):
+    """The widest table covers 512 tokens in 16-token partitions: 32 partitions,
+    the one-warp merge at its limit (lane c = partition c)."""
+    q_len, hq, hkv, d, bs = 4, 32, 8, 128, 16
+    lens = [512, 509, 100, 4]
+    q, kc, vc, tables, lens_t = _case(6, q_len, hq, hkv, d, bs, dt, lens, extra_blocks=0)
+    assert tables.shape[1] * bs // 16 == 32
+    scale = 1 / np.sqrt(d)
+    out = ops().verify_decode(q, kc, vc, tables, lens_t, scale, split_tokens=16)
+    ref = opa.verify_decode(to_f64(q), to_f64(kc), to_f64(vc), tables.cpu().numpy(), lens, scale)
+    assert_close(out, ref, f"verify 32 partitions {dt}")
     assert ops().get_device_error() == 0
 
 
