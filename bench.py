@@ -672,6 +672,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--split", type=int, default=None, help="decode partition size (default: the workload's)")
+    ap.add_argument("--block-size", type=int, default=None, choices=[4, 8, 16, 32],
+                    help="tokens per block for the decode workloads built from one context draw "
+                         "(llama8b_gqa_decode, long_context_splitk_decode, spec_verify_decode); default 16")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--jsonl", default=None, help="also append the result line to this file")
     ap.add_argument("--e2e-launch", default="auto", choices=["auto", "graph", "eager"],
@@ -693,7 +696,12 @@ def main():
         ap.error("--warmup must be >= 3")
 
     ws, rank, local = dist_env()
-    wl = W.WORKLOADS[args.workload]()
+    if args.block_size is not None and args.block_size != 16:
+        if args.workload not in ("llama8b_gqa_decode", "long_context_splitk_decode", "spec_verify_decode"):
+            ap.error("--block-size applies to llama8b_gqa_decode, long_context_splitk_decode, spec_verify_decode")
+        wl = W.WORKLOADS[args.workload](block_size=args.block_size)
+    else:
+        wl = W.WORKLOADS[args.workload]()
     if args.split is not None:
         wl.split_tokens = args.split
     if args.impl == "reference":
@@ -915,6 +923,8 @@ def main():
             "batch": n_dec,
             "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "head_dim": wl.head_dim,
             "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+            "allocator": {"waste_slots": step.alloc.stats()["waste_slots"],
+                          "table_entries": int(np.sum(np.ceil(step.dec_lens / wl.block_size))) if n_dec else 0},
             "context_lens": [int(min(step.dec_lens)), int(max(step.dec_lens))] if n_dec else None,
             "mean_context": float(np.mean(step.dec_lens)) if n_dec else None,
             "split_tokens": step.split if n_dec else None,

@@ -159,15 +159,19 @@ def custom_decode(batch: int, len_lo: int, len_hi: int, q_heads: int, kv_heads: 
     )
 
 
-def llama8b_gqa_decode(seed: int = 0, batch: int = 64, len_lo: int = 512, len_hi: int = 4096) -> Workload:
-    """Batch 64, 32 q heads / 8 KV heads, D=128, bs=16, bf16 N(0,1), lens U{512..4096}."""
-    wl = custom_decode(batch, len_lo, len_hi, 32, 8, 128, 16, "bf16", seed, name="llama8b_gqa_decode")
+def llama8b_gqa_decode(seed: int = 0, batch: int = 64, len_lo: int = 512, len_hi: int = 4096,
+                       block_size: int = 16) -> Workload:
+    """Batch 64, 32 q heads / 8 KV heads, D=128, bs=16, bf16 N(0,1), lens U{512..4096}.
+
+    ``block_size`` other than 16 gives the same contexts in blocks of another
+    size (the block-size trade-off of "2.1 PagedAttention" §4 and §10)."""
+    wl = custom_decode(batch, len_lo, len_hi, 32, 8, 128, block_size, "bf16", seed, name="llama8b_gqa_decode")
     wl.note = "one query token per request; pool 1.5x needed, shuffled free list"
     return wl
 
 
 def spec_verify_decode(seed: int = 0, batch: int = 64, len_lo: int = 512, len_hi: int = 4096,
-                       k: int = 3) -> Workload:
+                       k: int = 3, block_size: int = 16) -> Workload:
     """Verify step of speculative decoding on the llama8b_gqa_decode shape.
 
     Batch 64, 32 q heads / 8 KV heads, D=128, bs=16, bf16 N(0,1); each
@@ -175,7 +179,7 @@ def spec_verify_decode(seed: int = 0, batch: int = 64, len_lo: int = 512, len_hi
     whose K/V this step writes; k+1 = 4 queries per request (the last
     accepted token and the drafts), 16 query rows per KV head.
     """
-    wl = custom_decode(batch, len_lo, len_hi, 32, 8, 128, 16, "bf16", seed, name="spec_verify_decode")
+    wl = custom_decode(batch, len_lo, len_hi, 32, 8, 128, block_size, "bf16", seed, name="spec_verify_decode")
     wl.q_len = k + 1
     wl.setup_ops, wl.step_ops = _decode_scripts(wl.decode_seqs, wl.decode_lens, k + 1)
     wl.note = f"k={k} draft tokens per request written this step; k+1 causal queries per request"
@@ -188,9 +192,9 @@ def _renamed(wl: Workload, name: str) -> Workload:
 
 
 def long_context_splitk_decode(seed: int = 0, batch: int = 8, len_lo: int = 32768,
-                               len_hi: int = 131072) -> Workload:
+                               len_hi: int = 131072, block_size: int = 16) -> Workload:
     """Batch 8, 64 q heads / 8 KV heads, D=128, bs=16, lens U{32768..131072}, 512-token splits."""
-    wl = custom_decode(batch, len_lo, len_hi, 64, 8, 128, 16, "bf16", seed, split_tokens=512,
+    wl = custom_decode(batch, len_lo, len_hi, 64, 8, 128, block_size, "bf16", seed, split_tokens=512,
                        name="long_context_splitk_decode")
     wl.note = "context partitioned into 512-token chunks merged by log-sum-exp"
     return wl
