@@ -103,8 +103,13 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_traffic(profile_name: str, source_file: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+def kernel_traffic(profile_name: str, source_file: str, block_size: int = 16):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source.
+
+    The summaries were taken on the workloads' own 16-token blocks; another
+    block size is another launch, whose traffic they do not give (None)."""
+    if block_size != 16:
+        return None
     path = os.path.join(ROOT, "profiles", profile_name)
     if not os.path.exists(path):
         return None
@@ -959,7 +964,8 @@ def main():
     if step.dec and step.prefix_len:
         ub = nb["decode_unique"]
         # DRAM traffic of the call's dominant kernel, the suffix decode pass
-        straffic = kernel_traffic(f"decode_partial_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/decode.cu")
+        straffic = kernel_traffic(f"decode_partial_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/decode.cu",
+                                  wl.block_size)
         flops = 4 * len(wl.decode_seqs) * wl.q_heads * wl.head_dim * step.prefix_len
         res["roofline"] = {
             "kernel": "pa_decode_shared_prefix (tcgen05 prefix pass + suffix decode + merge)",
@@ -986,7 +992,7 @@ def main():
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
         prof = (f"decode_partial_{wl.name}.md" if step.layout == "paged" else
                 f"decode_contiguous_{step.layout}_{wl.name}.md")
-        traffic = kernel_traffic(prof, "paged_kv_cache_76_gb300/csrc/decode.cu")
+        traffic = kernel_traffic(prof, "paged_kv_cache_76_gb300/csrc/decode.cu", wl.block_size)
         verify = wl.q_len > 1
         res["roofline"] = {
             "kernel": ("decode_partial_kernel with q_len=k+1 + lse_merge (pa_verify_decode)" if verify
@@ -1020,7 +1026,7 @@ def main():
         # flops of the visible (query, key) pairs against the measured bf16 peak
         tpeak, tkind = measured_tensor_peak()
         fl = nb["prefill_flops"]
-        ptraffic = kernel_traffic(f"attn_tc_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/attn_tc.cu") \
+        ptraffic = kernel_traffic(f"attn_tc_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/attn_tc.cu", wl.block_size) \
             if wl.block_size >= 8 else None
         res["roofline"] = {
             "kernel": "attn_tc_kernel" if wl.block_size >= 8 else "chunked_prefill_kernel",
