@@ -182,13 +182,16 @@ class Step:
     """Device buffers and host copies of one workload step; runs it through the C ABI."""
 
     def __init__(self, wl: W.Workload, device: torch.device, value_seed: int, overlap_streams: bool = True,
-                 shared_prefix: bool = True, kv_layout: str = "paged"):
+                 shared_prefix: bool = True, kv_layout: str = "paged", verify_impl: str = "mma",
+                 verify_ctas: int = 0):
         from paged_kv_cache_76_gb300 import ops
         from paged_kv_cache_76_gb300.allocator import BlockAllocator
         self.ops = ops
         self._rec = None  # a plan being recorded (record_plan)
         self.wl = wl
         self.dev = device
+        self.verify_impl = verify_impl
+        self.verify_ctas = verify_ctas
         a = BlockAllocator(wl.num_blocks, wl.block_size, wl.free_order)
         a.run(wl.setup_ops)
         slots, pairs = a.run(wl.step_ops)
@@ -440,8 +443,12 @@ class Step:
         elif self.dec and wl.q_len > 1:
             if ev is not None:
                 ev[0].record(stream)
-            o.verify_decode(d["q_decode"], self.k_cache, self.v_cache, d["dec_tables"], d["dec_lens"], wl.scale,
-                            out=self.out_dec, split_tokens=self.split, workspace=self.workspace, stream=stream)
+            if self.verify_impl == "tc":
+                o.verify_decode_tc(d["q_decode"], self.k_cache, self.v_cache, d["dec_tables"], d["dec_lens"],
+                                   wl.scale, out=self.out_dec, max_ctas=self.verify_ctas, stream=stream)
+            else:
+                o.verify_decode(d["q_decode"], self.k_cache, self.v_cache, d["dec_tables"], d["dec_lens"], wl.scale,
+                                out=self.out_dec, split_tokens=self.split, workspace=self.workspace, stream=stream)
             if ev is not None:
                 ev[1].record(stream)
         elif self.dec:
@@ -692,6 +699,12 @@ def main():
     ap.add_argument("--kv-layout", default="paged", choices=["paged", "contiguous", "vmm"],
                     help="decode-only workloads: paged blocks (default), or one contiguous K/V per request slot in "
                          "plain memory or in on-demand-mapped virtual memory (the vAttention comparison)")
+    ap.add_argument("--verify-impl", default="auto", choices=["auto", "mma", "tc"],
+                    help="verify workloads: the warp-MMA partition kernel with its merge (pa_verify_decode), the "
+                         "tcgen05 one-tile kernel (pa_verify_decode_tc), or auto: tcgen05 when a unit has more than "
+                         "16 (query, group head) columns and blocks of >= 8 tokens (measured faster there)")
+    ap.add_argument("--verify-ctas", type=int, default=0,
+                    help="--verify-impl tc: CTAs of the kernel (0: one per (request, KV head) unit)")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="decode a shared prefix per request instead of once for the batch")
     ap.add_argument("--prefill-ctas", type=int, default=None,
@@ -724,8 +737,12 @@ def main():
     from paged_kv_cache_76_gb300 import _lib
     _lib.lib()  # fails loudly if the CUDA library is missing
 
+    if args.verify_impl == "auto":
+        cols = wl.q_len * (wl.q_heads // wl.kv_heads)
+        args.verify_impl = "tc" if wl.q_len > 1 and cols > 16 and wl.block_size >= 8 else "mma"
     step = Step(wl, device, value_seed=1000 * rank, overlap_streams=not args.serial,
-                shared_prefix=not args.no_shared_prefix, kv_layout=args.kv_layout)
+                shared_prefix=not args.no_shared_prefix, kv_layout=args.kv_layout, verify_impl=args.verify_impl,
+                verify_ctas=args.verify_ctas)
     peak, peak_kind = measured_peaks()
 
     stream = torch.cuda.Stream(device)
@@ -934,6 +951,7 @@ def main():
             "mean_context": float(np.mean(step.dec_lens)) if n_dec else None,
             "split_tokens": step.split if n_dec else None,
             "queries_per_request": wl.q_len,
+            "verify_impl": step.verify_impl if wl.q_len > 1 else None,
             "kv_layout": step.layout,
             "prefill_chunks": step.chunks if step.pre else None,
             "copy_pairs": step.n_pairs,
@@ -992,10 +1010,13 @@ def main():
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
         prof = (f"decode_partial_{wl.name}.md" if step.layout == "paged" else
                 f"decode_contiguous_{step.layout}_{wl.name}.md")
-        traffic = kernel_traffic(prof, "paged_kv_cache_76_gb300/csrc/decode.cu", wl.block_size)
         verify = wl.q_len > 1
+        traffic = (None if verify and step.verify_impl == "tc" else   # the summaries are the partition kernel's
+                   kernel_traffic(prof, "paged_kv_cache_76_gb300/csrc/decode.cu", wl.block_size))
         res["roofline"] = {
-            "kernel": ("decode_partial_kernel with q_len=k+1 + lse_merge (pa_verify_decode)" if verify
+            "kernel": ("attn_tile_kernel, causal over each request's k+1 queries (pa_verify_decode_tc)"
+                       if verify and step.verify_impl == "tc" else
+                       "decode_partial_kernel with q_len=k+1 + lse_merge (pa_verify_decode)" if verify
                        else "decode_partial_kernel" if step.layout == "paged" else
                        f"decode_partial_kernel, contiguous mode + lse_merge ({step.layout} memory)"),
             "bound": "hbm",
@@ -1008,7 +1029,9 @@ def main():
             "algorithmic_bytes_per_launch": dec_bytes,
             "avg_launch_ms": round(dec_ms, 5),
             **launch_pct,
-            "timing": (f"CUDA events around each of K pa_verify_decode calls (partial + merge kernels) on the "
+            "timing": ("CUDA events around each of K pa_verify_decode_tc calls on the bench stream, in a second "
+                       "pass of the same K steps" if verify and step.verify_impl == "tc" else
+                       f"CUDA events around each of K pa_verify_decode calls (partial + merge kernels) on the "
                        f"bench stream, in a second pass of the same K steps" if verify else
                        "CUDA events around each of K contiguous decode calls (partial + merge kernels) on the "
                        "bench stream, in a second pass of the same K steps" if step.layout != "paged" else

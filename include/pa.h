@@ -239,6 +239,32 @@ int pa_verify_decode(const void* q, const void* k_cache, const void* v_cache, co
                      void* workspace, size_t workspace_bytes, void* out, pa_dtype dtype, pa_stream stream);
 
 /* ----------------------------------------------------------------------------
+ * pa_verify_decode_tc - the same verify attention on the tensor cores.
+ *
+ * The computation of pa_verify_decode ("Khám phá vLLM … phần 2",
+ * speculative decoding: query i of request r attends tokens
+ * [0, context_lens[r] - (q_len-1-i))), read as what it also is: a chunked
+ * prefill of a q_len-token chunk at the end of the context.  The
+ * (query, group head) rows of one (request, KV head) - at most 128 - are one
+ * work unit of a tcgen05 kernel (tensor memory, TMA gathers) that walks the
+ * whole context in 128-key tiles; no workspace, no merge.  A unit's gather
+ * cost does not depend on its row count, so this form pays when the rows are
+ * many (k = 7 drafts x 4 group heads = 32) and the batch gives every SM units.
+ *   q, out        [num_seqs][q_len][q_heads][head_dim], as pa_verify_decode
+ *   q_len         >= 1, with (q_heads / kv_heads) * q_len <= 128
+ *   block_size    8, 16 or 32 (the gather's boxes hold 8-row swizzle atoms)
+ *   max_ctas      0: one CTA per unit; > 0: that many CTAs, each taking units
+ *                 b, b + max_ctas, ... (one CTA per SM fits)
+ * Results equal pa_verify_decode's within the attention tolerance (the sums
+ * are taken in another order); a query that sees no token gives a zero row.
+ * Errors as pa_chunked_prefill.
+ * ------------------------------------------------------------------------- */
+int pa_verify_decode_tc(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_len, int q_heads,
+                        int kv_heads, int head_dim, int block_size, int num_blocks, float scale, int max_ctas,
+                        void* out, pa_dtype dtype, pa_stream stream);
+
+/* ----------------------------------------------------------------------------
  * Contiguous virtual KV, vAttention style ("vAttention 完全拆解") - the
  * competing design, built as a comparison baseline for the paged kernels.
  *

@@ -84,6 +84,7 @@ PROTOTYPES = {
     "pa_selftest_wait_timeout": (_I, [_I, _P]),
     "pa_verify_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "pa_verify_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P, _I, _P]),
+    "pa_verify_decode_tc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
     "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
     "pa_chunked_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P]),
     "pa_decode_shared_prefix_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),

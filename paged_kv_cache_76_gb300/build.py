@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
 SOURCES = ["pa_api.cu", "decode.cu", "prefill.cu", "cache_ops.cu", "block_alloc.cpp", "decode_noalloc.cu", "attn_tc.cu",
-           "vkv.cpp"]
+           "attn_tile.cu", "vkv.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

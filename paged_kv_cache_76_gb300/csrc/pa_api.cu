@@ -638,6 +638,48 @@ int pa_chunked_prefill(const void* q, const int32_t* q_start, const int32_t* con
   return cuda_status(launch_chunked_prefill(km, vm, p, head_dim, bsub, dtype, st_));
 }
 
+int pa_verify_decode_tc(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int q_len, int q_heads,
+                        int kv_heads, int head_dim, int block_size, int num_blocks, float scale, int max_ctas,
+                        void* out, pa_dtype dtype, pa_stream stream) {
+  int st = check_kv_shape(num_blocks, block_size, kv_heads, head_dim, dtype);
+  if (st != PA_OK) return st;
+  if (block_size < 8 || num_seqs < 0 || num_seqs > 65535 || q_len < 1 || q_heads <= 0 || q_heads % kv_heads != 0 ||
+      (q_heads / kv_heads) * q_len > 128 || max_blocks_per_seq <= 0 || !std::isfinite(scale))
+    return PA_ERR_INVALID;
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_INVALID;
+  CUtensorMap km, vm;
+  if (!kv_map(k_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &km) ||
+      !kv_map(v_cache, num_blocks, block_size, kv_heads, head_dim, dtype, &vm))
+    return PA_ERR_CUDA;
+  int* err = device_error_ptr();
+  if (!err) return PA_ERR_CUDA;
+  PrefillParams p{};
+  p.q = q;
+  p.lens = context_lens;
+  p.tables = block_tables;
+  p.out = out;
+  p.err = err;
+  p.maxblk = max_blocks_per_seq;
+  p.num_reqs = num_seqs;
+  p.total_q = num_seqs * q_len;
+  p.max_q_len = q_len;
+  p.fixed_q_len = q_len;
+  p.q_heads = q_heads;
+  p.kv_heads = kv_heads;
+  p.group = q_heads / kv_heads;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = 1;
+  p.max_ctas = max_ctas;
+  return cuda_status(launch_attn_tile(km, vm, p, head_dim, block_size < 16 ? block_size : 16, dtype,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int q_heads, int head_dim, int max_blocks_per_seq,
                                               int block_size, int prefix_len, int split_tokens) {
   if (block_size < 8)  // 4-token blocks: plain pa_decode is used

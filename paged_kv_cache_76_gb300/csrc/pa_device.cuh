@@ -184,6 +184,15 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, cached in L2 only).
+// Only the first `src_bytes` (0 or 16) are read; the rest of the 16 is zeroed.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// every cp.async group this thread committed has landed (visible to this thread)
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
 // ----------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores) and tensor memory
 // ----------------------------------------------------------------------------

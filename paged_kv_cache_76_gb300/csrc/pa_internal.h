@@ -100,6 +100,11 @@ struct PrefillParams {
   // tcgen05 path: CTAs launched (each takes work units b, b + gridDim.x, ...);
   // <= 0 launches one CTA per unit
   int max_ctas;
+  // > 0 (one-tile kernel, causal): every request has fixed_q_len queries, rows
+  // r*fixed_q_len.. of q and out (q_start unused), and a context shorter than
+  // that leaves the first queries without keys (zero rows): the speculative
+  // verify
+  int fixed_q_len;
   float* part_o;
   float* part_m;
   float* part_l;
@@ -137,6 +142,10 @@ inline unsigned copy_grid(int64_t total) {
   const int64_t want = (total + 255) / 256;
   return (unsigned)(want < cap ? want : cap);
 }
+// tcgen05 kernel with one 128-row tile per (request, KV head) work unit and
+// Q, P in tensor memory (causal with fixed_q_len: the speculative verify).
+cudaError_t launch_attn_tile(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
+                             int head_dim, int bsub, pa_dtype dt, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int32_t* slots, int num_tokens,
                                      void* k_cache, void* v_cache, int64_t num_slots, int row_bytes, int* err,
                                      cudaStream_t stream);

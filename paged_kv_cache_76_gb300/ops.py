@@ -317,6 +317,23 @@ def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_t
     return out
 
 
+def verify_decode_tc(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, max_ctas=0, stream=None):
+    """pa_verify_decode_tc: ``q`` is [num_seqs, k+1, q_heads, head_dim]; the
+    verify attention on the tcgen05 kernel (no workspace)."""
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    B, ql, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("head_dim mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    _keep(out)
+    _launch("pa_verify_decode_tc", _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _i32(block_tables, "block_tables"), int(block_tables.shape[1]), _i32(context_lens, "context_lens"), B,
+            ql, hq, hkv, d, bs, nb, float(scale), int(max_ctas), _dev(out, "out"), dtype_code(q.dtype),
+            _stream(stream))
+    return out
+
+
 def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, scale, max_q_len, out=None,
                     stream=None, max_ctas=0):
     """pa_chunked_prefill; ``max_ctas`` > 0 caps the CTAs (SMs) the tensor-core path uses."""

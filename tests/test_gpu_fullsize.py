@@ -56,6 +56,25 @@ def test_spec_verify_decode_full_size():
     _no_err()
 
 
+def test_spec_verify_decode_k7_tensor_core_form_full_size():
+    """The k = 7 verify workload as bench.py times it by default (32 query
+    columns per KV head: pa_verify_decode_tc), sampled requests against the
+    oracle, and every row against the warp-MMA form within the tolerance."""
+    from paged_kv_cache_76_gb300 import ops
+    wl = W.WORKLOADS["spec_verify_decode_k7"]()
+    vals = W.make_values(wl, device="cuda")
+    dev = DeviceStep(wl, vals)
+    dev.run()                                   # reshape_and_cache + pa_verify_decode
+    tc = ops.verify_decode_tc(dev.q_decode, dev.k_cache, dev.v_cache, dev.dec_tables, dev.dec_lens, wl.scale)
+    torch.cuda.synchronize()
+    rows = list(range(3, 64, 8))
+    ref = oracle_step(wl, vals, decode_rows=rows, compact=True)
+    assert_close(tc[rows], ref["decode"], "verify k7 tensor-core form sampled")
+    d = (tc.float() - dev.out_decode.float()).abs()
+    assert d.max().item() <= 2e-2 and d.mean().item() <= 1e-3
+    _no_err()
+
+
 def test_long_context_splitk_decode_full_size():
     wl = W.long_context_splitk_decode()
     vals = W.make_values(wl, device="cuda")

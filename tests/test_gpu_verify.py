@@ -167,3 +167,55 @@ def test_rising_scores_move_the_reference_per_column(q_len, split):
         dec = ops().decode(q[:, i].contiguous(), kc, vc, tables, li, scale, split_tokens=dsplit)
         assert torch.equal(out[:, i], dec), i
     assert ops().get_device_error() == 0
+
+
+# ---------------------------------------------------------------- tensor-core form (pa_verify_decode_tc)
+TC_CASES = [c for c in VERIFY_CASES if c[4] >= 8 and (c[1] // c[2]) * c[0] <= 128] + [
+    # q_len, q_heads, kv_heads, head_dim, block_size, dtype, lens, split_tokens (unused)
+    (8, 32, 8, 128, 16, "bf16", [2339, 130, 17, 4096, 1], 0),      # the k = 7 workload's shape: 32 rows
+    (16, 64, 8, 128, 16, "bf16", [700, 129, 300], 0),              # 128 rows: a full tile
+    (4, 28, 4, 128, 8, "fp16", [1000, 33, 257, 2], 0),             # 28 rows, 8-token blocks
+    (5, 16, 2, 64, 32, "bf16", [640, 77, 3], 0),                   # D = 64, 32-token blocks
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=[f"q{c[0]}_h{c[1]}x{c[2]}_d{c[3]}_bs{c[4]}_{c[5]}" for c in TC_CASES])
+def test_verify_tc_matches_the_oracle(case):
+    q_len, hq, hkv, d, bs, dt, lens, _ = case
+    q, kc, vc, tables, lens_t = _case(7, q_len, hq, hkv, d, bs, dt, lens)
+    scale = 1 / np.sqrt(d)
+    out = torch.full_like(q, float("nan"))
+    ops().verify_decode_tc(q, kc, vc, tables, lens_t, scale, out=out)
+    ref = opa.verify_decode(to_f64(q), to_f64(kc), to_f64(vc), tables.cpu().numpy(), lens, scale)
+    assert_close(out, ref, f"verify tc {case}")
+    for r, L in enumerate(lens):
+        for i in range(q_len):
+            if L - (q_len - 1 - i) <= 0:
+                assert torch.count_nonzero(out[r, i]) == 0
+    assert ops().get_device_error() == 0
+
+
+def test_verify_tc_persistent_grid_gives_the_same_bits_and_matches_the_mma_form():
+    q_len, hq, hkv, d, bs = 8, 32, 8, 128, 16
+    lens = [3000, 1, 6, 700, 129, 4096, 2048, 17, 900]
+    q, kc, vc, tables, lens_t = _case(8, q_len, hq, hkv, d, bs, "bf16", lens)
+    scale = 1 / np.sqrt(d)
+    a = ops().verify_decode_tc(q, kc, vc, tables, lens_t, scale)
+    b = ops().verify_decode_tc(q, kc, vc, tables, lens_t, scale, max_ctas=5)
+    assert torch.equal(a, b)
+    m = ops().verify_decode(q, kc, vc, tables, lens_t, scale)
+    err = (to_f64(a) - to_f64(m))
+    assert np.abs(err).max() <= 2 * 1e-2 and np.abs(err).mean() <= 1e-3
+    assert ops().get_device_error() == 0
+
+
+def test_verify_tc_argument_checks():
+    from paged_kv_cache_76_gb300 import _lib
+    q, kc, vc, tables, lens_t = _case(9, 8, 32, 8, 128, 16, "bf16", [100, 200])
+    with pytest.raises(_lib.PAError):                       # 17 queries x 8 group heads > 128 rows
+        q2 = torch.zeros(2, 17, 64, 128, dtype=torch.bfloat16, device="cuda")
+        ops().verify_decode_tc(q2, kc, vc, tables, lens_t, 0.1)
+    q4, kc4, vc4, t4, l4 = _case(9, 4, 8, 8, 64, 4, "fp16", [50, 60])
+    with pytest.raises(_lib.PAError):                       # 4-token blocks: no tcgen05 gather
+        ops().verify_decode_tc(q4, kc4, vc4, t4, l4, 0.1)
+    assert ops().get_device_error() == 0
