@@ -1011,7 +1011,8 @@ def main():
         prof = (f"decode_partial_{wl.name}.md" if step.layout == "paged" else
                 f"decode_contiguous_{step.layout}_{wl.name}.md")
         verify = wl.q_len > 1
-        traffic = (None if verify and step.verify_impl == "tc" else   # the summaries are the partition kernel's
+        traffic = (kernel_traffic(f"attn_tile_{wl.name}.md", "paged_kv_cache_76_gb300/csrc/attn_tile.cu",
+                                  wl.block_size) if verify and step.verify_impl == "tc" else
                    kernel_traffic(prof, "paged_kv_cache_76_gb300/csrc/decode.cu", wl.block_size))
         res["roofline"] = {
             "kernel": ("attn_tile_kernel, causal over each request's k+1 queries (pa_verify_decode_tc)"
