@@ -96,16 +96,18 @@ constexpr int B_OFREE = B_QFULL + 1;          // the unit's O read out (8 warps)
 constexpr int B_MMADONE = B_OFREE + 1;        // every MMA of the CTA complete (commit)
 static_assert(B_MMADONE + 1 == 4 * 3 + 2 + 2 + 6, "barrier count");
 
-// One work unit: a tile of 128 rows of one (request, KV head) for the causal
-// prefill, or of one (prefix key range, KV head) for the shared-prefix pass.
-// Units are numbered z-major, then head, then row tile in reverse (the last
-// row tiles of a causal chunk see the most keys, so they come first).
+// One work unit: the rows of one (request, KV head), at most 128: query i of
+// the request's fixed_q_len queries times head g of the group, row i*G + g
+// (rows past 128 of a larger request would be further units; the ABI limits
+// q_len * group to 128).  Units are numbered request-major, then head.
 struct TcUnit {
   int z, h, row0, r, qs, chunk, p0, k0, kend, rows, ntiles;
 };
 
-// Geometry of unit u from immutable inputs only.  false: the request's
-// q_start/context_lens are inconsistent (the unit is skipped).
+// Geometry of unit u from immutable inputs only: row (query i, head g) sees
+// keys 0 .. p0 + i, p0 = context - q_len (negative for a context shorter
+// than q_len: its first queries see no key).  false: the request's context
+// length is out of range (the unit is skipped).
 __device__ __forceinline__ bool tc_unit(const PrefillParams& p, int u, int row_tiles, TcUnit& w) {
   const int per_z = row_tiles * p.kv_heads;
   w.z = u / per_z;
@@ -114,40 +116,18 @@ __device__ __forceinline__ bool tc_unit(const PrefillParams& p, int u, int row_t
   w.row0 = (row_tiles - 1 - (rem - w.h * row_tiles)) * kRows;
   w.ntiles = 0;
   const int G = p.group;
-  if (p.causal) {
-    // request r = z, chunk at absolute position p0, row (query i, head g)
-    // sees keys 0 .. p0+i
-    w.r = w.z;
-    // fixed_q_len (speculative verify): request r's queries are rows
-    // r*q_len.. of q, and a context shorter than q_len leaves its first
-    // queries without keys (zero rows)
-    const bool fixed = p.fixed_q_len > 0;
-    w.qs = fixed ? w.r * p.fixed_q_len : __ldg(p.q_start + w.r);
-    const int qe = fixed ? w.qs + p.fixed_q_len : __ldg(p.q_start + w.r + 1);
-    w.chunk = qe - w.qs;
-    const int ctx = __ldg(p.lens + w.r);
-    w.p0 = ctx - w.chunk;
-    if (w.qs < 0 || qe < w.qs || qe > p.total_q || w.chunk > p.max_q_len || (w.p0 < 0 && !fixed) || ctx < 0 ||
-        ctx > p.maxblk * p.block_size)
-      return false;
-    w.k0 = 0;
-    w.rows = w.chunk * G;
-    if (w.row0 >= w.rows) return true;
-    const int last_row = min(w.row0 + kRows, w.rows) - 1;
-    w.kend = w.p0 + last_row / G + 1;
-    if (w.kend <= 0) return true;  // no row sees a key (ntiles = 0)
-  } else {
-    // one virtual request of total_q queries (the decode batch); keys
-    // [k0, kend) = split z of the prefix, visible to every row
-    w.r = 0;
-    w.qs = 0;
-    w.chunk = p.total_q;
-    w.p0 = 0;
-    w.k0 = w.z * p.key_split;
-    w.kend = min(w.k0 + p.key_split, p.prefix_len);
-    w.rows = w.chunk * G;
-    if (w.row0 >= w.rows || w.k0 >= w.kend) return true;
-  }
+  w.r = w.z;
+  w.qs = w.r * p.fixed_q_len;
+  w.chunk = p.fixed_q_len;
+  const int ctx = __ldg(p.lens + w.r);
+  w.p0 = ctx - w.chunk;
+  if (ctx < 0 || ctx > p.maxblk * p.block_size) return false;
+  w.k0 = 0;
+  w.rows = w.chunk * G;
+  if (w.row0 >= w.rows) return true;
+  const int last_row = min(w.row0 + kRows, w.rows) - 1;
+  w.kend = w.p0 + last_row / G + 1;
+  if (w.kend <= 0) return true;  // no row sees a key (ntiles = 0)
   w.ntiles = (w.kend - w.k0 + kKeys - 1) / kKeys;
   return true;
 }
@@ -180,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.group;
   // CTA b (linear block index) takes units b, b + nctas, ...
   const int row_tiles = (p.max_q_len * G + kRows - 1) / kRows;
-  const int nunits = row_tiles * p.kv_heads * (p.causal ? p.num_reqs : (p.prefix_len + p.key_split - 1) / p.key_split);
+  const int nunits = row_tiles * p.kv_heads * p.num_reqs;
   const int cta0 = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   const int nctas = gridDim.x * gridDim.y * gridDim.z;
 
@@ -394,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // units whose rows see no key at all (a verify request shorter than its
     // queries) are skipped by every role; their rows are written as zeros here
-    if (p.causal && p.fixed_q_len > 0) {
+    {
       TcUnit z;
       for (int uz = cta0; uz < nunits; uz += nctas) {
         if (!tc_unit(p, uz, row_tiles, z) || z.ntiles > 0 || z.row0 >= z.rows) continue;
@@ -425,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int grow = w.row0 + row;
       const bool valid = grow < w.rows;
       const int qi = grow / G, g = grow % G;
-      const int lim = !valid ? -1 : (p.causal ? w.p0 + qi : w.kend - 1);  // last key this row may see
+      const int lim = !valid ? -1 : w.p0 + qi;  // last key this row may see
       const bool wvalid = __any_sync(kAll, valid);  // else: only keep the barrier phases
       float m = -INFINITY, l = 0.f;  // running (possibly stale) max in log2 units, sum of this warp's keys
       for (int j = 0; j < w.ntiles; ++j, ++gt) {
@@ -579,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("bar.sync %0, %1;\n" ::"r"(1 + quarter), "r"(64) : "memory");
       if (!wvalid) {
         // nothing of this warp's rows is written
-      } else if (p.causal) {
+      } else {
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
                                               ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D + kh * DH);
@@ -596,25 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           Elem<T>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
                                           Elem<T>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
           }
-        }
-      } else {
-        // shared-prefix partial of this key range: unnormalised o, m, l
-        const size_t pr = ((size_t)qi * p.q_heads + w.h * G + g) * p.max_splits + w.z;
-        float4* po = reinterpret_cast<float4*>(p.part_o + pr * D + kh * DH);
-#pragma unroll
-        for (int c = 0; c < DH / 32; ++c) {
-          float ov[32];
-          tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);
-          tmem_wait_ld();
-          if (valid) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              po[8 * c + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
-          }
-        }
-        if (valid && kh == 0) {
-          p.part_m[pr] = m;
-          p.part_l[pr] = lt;
         }
       }
       tc_fence_before();  // O read out before the next unit's first P.V overwrites it
@@ -654,8 +615,11 @@ cudaError_t launch_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
+  // every request has fixed_q_len queries, and their rows fit one unit
+  if (p.fixed_q_len <= 0 || p.max_q_len != p.fixed_q_len || p.fixed_q_len * p.group > kRows)
+    return cudaErrorInvalidValue;
   const int row_tiles = (p.max_q_len * p.group + kRows - 1) / kRows;
-  const int zdim = p.causal ? p.num_reqs : (p.prefix_len + p.key_split - 1) / p.key_split;
+  const int zdim = p.num_reqs;
   const long long nunits = (long long)row_tiles * p.kv_heads * zdim;
   if (nunits <= 0) return cudaSuccess;
   if (nunits > INT32_MAX) return cudaErrorInvalidValue;
