@@ -13,14 +13,16 @@
 //  * P stays in tensor memory: the softmax writes P (bf16/fp16) over the
 //    first half of its S columns and O += P V reads A from TMEM, so P never
 //    crosses shared memory (about a quarter of the per-tile SMEM traffic).
-//  * Three producer warps issue the TMA gather: one warp issuing 16-row
-//    boxes moves about 27 B/clk per SM, several warps together more.
+//  * Two producer warps (K and V) issue the TMA gather: one warp issuing
+//    16-row boxes moves about 27 B/clk per SM, more than the 256 rows of a
+//    K/V tile need at this kernel's period.
 //  * The softmax holds its whole S row in registers (one TMEM round trip per
 //    tile).
 //
 // Warp roles (384 threads = 12 warps, so that each thread may hold 168
 // registers; one CTA per SM):
-//   warps 0,1   S issuers, one thread per Q tile x: per key tile j,
+//   warps 0,1   S issuers, one warp per Q tile x (one elected lane issues,
+//               with warp-uniform descriptors): per key tile j,
 //                 S_x(j) = Q_x K_j^T
 //               S_x(j) overwrites P_x(j-1), so it is issued once P.V_x(j-1)
 //               has completed.  The two issuers wait only on their own tile;
@@ -32,7 +34,7 @@
 //               = row.  It loads its S row, takes the row maximum, writes
 //               P = 2^(s*scale*log2e - m) into TMEM and sums it; after each
 //               half of P the group meets at a named barrier and its first
-//               thread issues O_x += P_x(j) V_j for that half.  The running
+//               warp issues O_x += P_x(j) V_j for that half.  The running
 //               maximum m is raised only when a row maximum exceeds it by
 //               more than 2^8 (O is then rescaled in TMEM); the final O / sum
 //               uses the same m, so this is exact.
@@ -55,6 +57,7 @@ constexpr int kKeys = 128;  // keys per K/V tile (N of S, K of P.V)
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kMmaWarp = 0;  // warps 0, 1: MMA issuers of Q tiles A, B (warp 0 owns TMEM)
+constexpr unsigned kAll = 0xffffffffu;
 constexpr int kKWarp = 2;
 constexpr int kVWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;
@@ -253,11 +256,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(full0 + t % nst), (t / nst) & 1);
   } else if (warp < kKWarp) {
     // ---------------------------------------------------------------- MMA issuers
-    // One thread per Q tile: warp 0 issues tile A's MMAs, warp 1 tile B's.
+    // One warp per Q tile: warp 0 issues tile A's MMAs, warp 1 tile B's.
     // tcgen05.mma issue blocks while the tensor pipe is busy, so a single
     // issuer serialises its waits behind the other tile's MMAs; two issuers
-    // wait only on their own tile, and the pipe interleaves their work.
-    if (lane == 0) {
+    // wait only on their own tile, and the pipe interleaves their work.  The
+    // whole warp runs the loop (its waits are voted, so control flow stays
+    // warp-uniform) and one elected lane issues each MMA and commit, with
+    // descriptors that are warp-uniform values.
+    {
       const int x = warp;
       bool ok = true;
       const uint32_t kbase = smem_u32(smem + L::K_OFF);
@@ -269,38 +275,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tc_unit(p, u, row_tiles, w)) {
           if (x == 0) {
             griddep_wait();
-            record_error(p.err, PA_DEVERR_QUERY_RANGE);
+            if (lane == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
           }
           continue;
         }
         if (w.ntiles <= 0) continue;
         // Q_x of this unit is in smem; the softmax warps have also finished
         // the previous unit (its last P.V completed and O_x was read out).
-        if (!mbar_wait(bar(B_QFULL + x), nu & 1)) { ok = false; break; }
+        if (!__all_sync(kAll, mbar_wait(bar(B_QFULL + x), nu & 1))) { ok = false; break; }
         // Tile B starts half a key tile behind tile A (once P_A(0) is being
         // written), so that the two softmaxes alternate instead of overlapping.
-        if (x == 1 && nu == 0 && !mbar_wait(bar(B_PLO), 0)) { ok = false; break; }
+        if (x == 1 && nu == 0 && !__all_sync(kAll, mbar_wait(bar(B_PLO), 0))) { ok = false; break; }
         ++nu;
         for (int j = 0; ok && j < w.ntiles; ++j, ++gt) {
           const int sk = gt % kKStages;
           // S_x(j) = Q_x K_j^T.  It overwrites P_x(j-1): wait for P.V_x(j-1).
-          if (!mbar_wait(bar(B_KFULL + sk), (gt / kKStages) & 1)) { ok = false; break; }
-          if (j > 0 && !mbar_wait(bar(B_OFULL + x), (gt - 1) & 1)) { ok = false; break; }
+          if (!__all_sync(kAll, mbar_wait(bar(B_KFULL + sk), (gt / kKStages) & 1))) { ok = false; break; }
+          if (j > 0 && !__all_sync(kAll, mbar_wait(bar(B_OFULL + x), (gt - 1) & 1))) { ok = false; break; }
           tc_fence_after();
           const uint32_t kb = kbase + sk * Tile::BYTES;
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * L::QHALF + (ks & 3) * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
-            tc_mma_f16(sd, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+            tc_mma_f16_warp(sd, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
           }
-          tc_commit(bar(B_SFULL + x));
-          tc_commit(bar(B_KEMPTY + sk));  // this issuer is done with K_j
+          tc_commit_warp(bar(B_SFULL + x));
+          tc_commit_warp(bar(B_KEMPTY + sk));  // this issuer is done with K_j
           // O_x += P_x(j) V_j is issued by tile x's softmax group itself
         }
       }
-      if (!ok) record_error(p.err, PA_DEVERR_TIMEOUT);
-      tc_commit(bar(B_MMADONE));
+      if (!ok && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
+      tc_commit_warp(bar(B_MMADONE));
     }
   } else {
     // ---------------------------------------------------------------- softmax
@@ -313,13 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t scol = tmem + lane_addr + S_COL + x * kKeys;
     const uint32_t ocol = tmem + lane_addr + O_COL + x * D;
     uint8_t* qt = smem + L::Q_OFF + x * L::QTILE;
-    // The group's first thread issues the group's P.V MMAs: the named barrier
-    // 1 + x (the group's 128 threads, with an AND vote that keeps every exit
-    // uniform) replaces a hand-off to another warp.
-    const bool leader = quarter == 0 && lane == 0;
+    // The group's first warp issues the group's P.V MMAs (one elected lane,
+    // warp-uniform operands): the named barrier 1 + x (the group's 128
+    // threads, with an AND vote that keeps every exit uniform) replaces a
+    // hand-off to another warp.
+    const bool leader = quarter == 0;
     const uint32_t sd0 = tmem + S_COL + x * kKeys, od0 = tmem + O_COL + x * D;
     const uint32_t vbase = smem_u32(smem + L::V_OFF);
-    bool lok = true;  // leader: every V wait succeeded
+    bool lok = true;  // leader warp: every V wait succeeded
     bool ok = true;
     int gt = 0;  // key tiles processed by this CTA
     for (int u = cta0; ok && u < nunits; u += nctas) {
@@ -454,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             tc_fence_after();
             const int vst = gt % kVStages;
-            if (hh == 0 && lok) lok = mbar_wait(bar(B_VFULL + vst), (gt / kVStages) & 1);
+            if (hh == 0 && lok) lok = __all_sync(kAll, mbar_wait(bar(B_VFULL + vst), (gt / kVStages) & 1));
             if (lok) {  // else S_x(j+1) never comes and the group stops at its next vote
               const uint32_t vb = vbase + vst * Tile::BYTES;
 #pragma unroll
@@ -462,11 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
                 const int kk = hh * (PSTEPS / 2) + k4;
                 const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
-                tc_mma_f16_ts(od0, sd0 + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+                tc_mma_f16_ts_warp(od0, sd0 + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
               }
               if (hh == 1) {
-                tc_commit(bar(B_OFULL + x));
-                tc_commit(bar(B_VEMPTY + vst));  // this group is done with V_j
+                tc_commit_warp(bar(B_OFULL + x));
+                tc_commit_warp(bar(B_VEMPTY + vst));  // this group is done with V_j
               }
             }
           }
@@ -518,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();  // O_x read out before the next unit's P.V overwrites it
     }
-    if ((!ok && lane == 0) || (leader && !lok)) record_error(p.err, PA_DEVERR_TIMEOUT);
-    if (leader) tc_commit(bar(B_MMADONE));  // this group's P.V MMAs have completed
+    if (lane == 0 && (!ok || (leader && !lok))) record_error(p.err, PA_DEVERR_TIMEOUT);
+    if (leader) tc_commit_warp(bar(B_MMADONE));  // this group's P.V MMAs have completed
   }
 
   // ------------------------------------------------------------------ teardown

@@ -53,6 +53,7 @@ constexpr int kRows = 128;  // rows per unit (M of every MMA)
 constexpr int kKeys = 128;      // keys per K/V tile (N of S, K of P.V)
 constexpr int kKStages = 3;
 constexpr int kVStages = 3;
+constexpr unsigned kAll = 0xffffffffu;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSWarp = 8;    // issues S = Q K^T; owns the TMEM allocation
 constexpr int kPvWarp = 9;   // issues O += P V
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!tc_unit(p, u, row_tiles, w)) {
         if (report) {
           griddep_wait();
-          record_error(p.err, PA_DEVERR_QUERY_RANGE);
+          if (lane == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
         }
         continue;
       }
@@ -259,18 +260,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S(gs) = Q K(gs)^T into buffer gs % 2, up to two key tiles ahead of the
     // softmax: the buffer is free once the softmax has read S(gs - 2); a
     // unit's first S needs the unit's Q in TMEM.  (An MMA issue costs its
-    // thread about 100 clk, so S and P.V have an issuing thread each.)
-    if (lane == 0) {
+    // thread about 100 clk, so S and P.V have an issuing warp each.)  The
+    // whole warp runs the loop with voted waits and one elected lane issues
+    // (warp-uniform descriptors).
+    {
       bool ok = true;
       const uint32_t kbase = smem_u32(smem + L::K_OFF);
       int gs = 0, ns = 0;  // key tiles and units of this CTA's stream
       TcUnit w;
       for (int u = next_unit(cta0, w, true); ok && u < nunits; u = next_unit(u + nctas, w, true), ++ns) {
-        if (!mbar_wait(bar(B_QFULL), ns & 1)) { ok = false; break; }
+        if (!__all_sync(kAll, mbar_wait(bar(B_QFULL), ns & 1))) { ok = false; break; }
         for (int j = 0; j < w.ntiles; ++j, ++gs) {
           const int b = gs & 1, sk = gs % kKStages;
-          if ((gs >= 2 && !mbar_wait(bar(B_SFREE + b), ((gs - 2) >> 1) & 1)) ||
-              !mbar_wait(bar(B_KFULL + sk), (gs / kKStages) & 1)) {
+          if (!__all_sync(kAll, (gs < 2 || mbar_wait(bar(B_SFREE + b), ((gs - 2) >> 1) & 1)) &&
+                                    mbar_wait(bar(B_KFULL + sk), (gs / kKStages) & 1))) {
             ok = false;
             break;
           }
@@ -279,34 +282,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
-            tc_mma_f16_ts(tmem + S_COL + b * kKeys, tmem + Q_COL + ks * 8, bd, IDESC_S, ks > 0 ? 1u : 0u);
+            tc_mma_f16_ts_warp(tmem + S_COL + b * kKeys, tmem + Q_COL + ks * 8, bd, IDESC_S, ks > 0 ? 1u : 0u);
           }
-          tc_commit(bar(B_SFULL + b));
-          tc_commit(bar(B_KEMPTY + sk));  // K(gs) read
+          tc_commit_warp(bar(B_SFULL + b));
+          tc_commit_warp(bar(B_KEMPTY + sk));  // K(gs) read
         }
       }
-      if (!ok) record_error(p.err, PA_DEVERR_TIMEOUT);
-      tc_commit(bar(B_MMADONE));
+      if (!ok && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
+      tc_commit_warp(bar(B_MMADONE));
     }
   } else if (warp == kPvWarp) {
     // ---------------------------------------------------------------- P.V issuer
     // O += P(gp) V(gp) in two 64-key halves, each once its half of P is in
     // TMEM; the unit's first P.V overwrites O, which the previous unit's
-    // epilogue must have read out.
-    if (lane == 0) {
+    // epilogue must have read out.  Warp-converged like the S issuer.
+    {
       bool ok = true;
       const uint32_t vbase = smem_u32(smem + L::V_OFF);
       int gp = 0, np = 0;  // key tiles and units of this CTA's stream
       TcUnit w;
       for (int u = next_unit(cta0, w, false); ok && u < nunits; u = next_unit(u + nctas, w, false), ++np) {
-        if (np > 0 && !mbar_wait(bar(B_OFREE), (np - 1) & 1)) { ok = false; break; }
+        if (np > 0 && !__all_sync(kAll, mbar_wait(bar(B_OFREE), (np - 1) & 1))) { ok = false; break; }
         for (int j = 0; j < w.ntiles; ++j, ++gp) {
           const int sv = gp % kVStages;
           const uint32_t vb = vbase + sv * Tile::BYTES;
-          if (!mbar_wait(bar(B_VFULL + sv), (gp / kVStages) & 1)) { ok = false; break; }
+          if (!__all_sync(kAll, mbar_wait(bar(B_VFULL + sv), (gp / kVStages) & 1))) { ok = false; break; }
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            if (!mbar_wait(bar(hh ? B_PHI : B_PLO), gp & 1)) {
+            if (!__all_sync(kAll, mbar_wait(bar(hh ? B_PHI : B_PLO), gp & 1))) {
               ok = false;
               break;
             }
@@ -316,16 +319,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               // A = P[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
               const int kk = hh * 4 + k4;
               const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
-              tc_mma_f16_ts(tmem + O_COL, tmem + P_COL + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_f16_ts_warp(tmem + O_COL, tmem + P_COL + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
             }
           }
           if (!ok) break;
-          tc_commit(bar(B_PVDONE));
-          tc_commit(bar(B_VEMPTY + sv));  // V(gp) read
+          tc_commit_warp(bar(B_PVDONE));
+          tc_commit_warp(bar(B_VEMPTY + sv));  // V(gp) read
         }
       }
-      if (!ok) record_error(p.err, PA_DEVERR_TIMEOUT);
-      tc_commit(bar(B_MMADONE));
+      if (!ok && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
+      tc_commit_warp(bar(B_MMADONE));
     }
   } else if (warp < kSoftmaxWarps) {
     // ---------------------------------------------------------------- softmax
@@ -337,7 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr float kRescale = 8.f;
     const uint32_t qst = smem_u32(smem + L::Q_OFF) + row * (D * 2);  // this row's staged Q
     float* lsum = reinterpret_cast<float*>(smem + L::L_OFF);
-    constexpr unsigned kAll = 0xffffffffu;
 
     // this thread's half of its Q row for unit w -> shared memory (16-byte
     // chunks, XOR-swizzled by row); rows past the unit are zero
