@@ -1,6 +1,8 @@
-"""Batch-size limits on the GPU: an empty batch is a no-op, and the largest
-batch the grid allows (65535 requests) decodes correctly on sampled rows
-(against the float64 oracle on a compacted copy of the blocks they read)."""
+"""Batch-size limits on the GPU: an empty batch (and an empty prefill, copy
+or scatter) is a no-op, and the largest batch the grid allows (65535
+requests) decodes and verifies correctly on sampled rows, the verify on both
+kernels (against the float64 oracle on a compacted copy of the blocks they
+read)."""
 import numpy as np
 import pytest
 import torch
@@ -38,11 +40,24 @@ def test_empty_batch_is_a_no_op():
     q4 = torch.empty(0, 3, 8, 128, device="cuda", dtype=torch.bfloat16)
     out4 = ops().verify_decode(q4, kc, vc, tables, lens, 0.1)
     assert out4.shape == (0, 3, 8, 128)
+    out5 = ops().verify_decode_tc(q4, kc, vc, tables, lens, 0.1)
+    assert out5.shape == (0, 3, 8, 128)
+    # no prefill request, no new token, no block pair: nothing runs, nothing is written
+    kc0, vc0 = kc.clone(), vc.clone()
+    qp = torch.empty(0, 8, 128, device="cuda", dtype=torch.bfloat16)
+    q_start = torch.zeros(1, device="cuda", dtype=torch.int32)
+    outp = ops().chunked_prefill(qp, q_start, lens, kc, vc, tables, 0.1, 0)
+    assert outp.shape == (0, 8, 128)
+    kn = torch.empty(0, 2, 128, device="cuda", dtype=torch.bfloat16)
+    ops().reshape_and_cache(kn, kn, torch.empty(0, device="cuda", dtype=torch.int32), kc, vc)
+    ops().copy_blocks(kc, vc, torch.empty(0, 2, device="cuda", dtype=torch.int32))
+    torch.cuda.synchronize()
+    assert torch.equal(kc, kc0) and torch.equal(vc, vc0)
     assert ops().get_device_error() == 0
 
 
-@pytest.mark.parametrize("q_len", [1, 3])
-def test_the_largest_batch_matches_the_oracle_on_sampled_rows(q_len):
+@pytest.mark.parametrize("q_len,tc", [(1, False), (3, False), (3, True)], ids=["decode", "verify", "verify_tc"])
+def test_the_largest_batch_matches_the_oracle_on_sampled_rows(q_len, tc):
     B, hq, hkv, d, bs = 65535, 4, 1, 64, 16
     rng = np.random.default_rng(7)
     lens = (1 + (np.arange(B) * 7919) % 31).astype(np.int32)   # 1..31 tokens: one or two blocks
@@ -58,6 +73,8 @@ def test_the_largest_batch_matches_the_oracle_on_sampled_rows(q_len):
     l_dev = torch.from_numpy(lens).cuda()
     if q_len == 1:
         out = ops().decode(q[:, 0].contiguous(), kc, vc, t_dev, l_dev, scale).unsqueeze(1)
+    elif tc:  # one tcgen05 work unit per (request, KV head): 65535 of them
+        out = ops().verify_decode_tc(q, kc, vc, t_dev, l_dev, scale)
     else:
         out = ops().verify_decode(q, kc, vc, t_dev, l_dev, scale)
     torch.cuda.synchronize()
@@ -74,4 +91,4 @@ def test_the_largest_batch_matches_the_oracle_on_sampled_rows(q_len):
         ref = opa.decode(q_s[:, 0], kc_s, vc_s, t_s, l_s, scale)[:, None]
     else:
         ref = opa.verify_decode(q_s, kc_s, vc_s, t_s, l_s, scale)
-    assert_close(out[rows], ref, f"largest batch q_len {q_len}")
+    assert_close(out[rows], ref, f"largest batch q_len {q_len}{' tensor cores' if tc else ''}")

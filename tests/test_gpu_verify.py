@@ -176,6 +176,9 @@ TC_CASES = [c for c in VERIFY_CASES if c[4] >= 8 and (c[1] // c[2]) * c[0] <= 12
     (16, 64, 8, 128, 16, "bf16", [700, 129, 300], 0),              # 128 rows: a full tile
     (4, 28, 4, 128, 8, "fp16", [1000, 33, 257, 2], 0),             # 28 rows, 8-token blocks
     (5, 16, 2, 64, 32, "bf16", [640, 77, 3], 0),                   # D = 64, 32-token blocks
+    (8, 64, 8, 128, 16, "bf16", [900, 5, 64], 0),                  # 64 rows: two lane quarters, all full
+    (11, 24, 8, 128, 16, "fp16", [300, 12, 1], 0),                 # 33 rows: the second quarter holds one
+    (13, 40, 8, 64, 8, "bf16", [500, 20], 0),                      # 65 rows: one 128-row unit per CTA
 ]
 
 
