@@ -142,7 +142,7 @@ int check_kv_shape(int num_blocks, int block_size, int kv_heads, int head_dim, p
   if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_INVALID;
   if (kv_heads <= 0 || kv_heads > 1024 || num_blocks <= 0) return PA_ERR_INVALID;
   // row coordinates (one past the pool included) must fit the TMA's int32
-  if ((int64_t)(num_blocks + 1) * block_size > INT32_MAX) return PA_ERR_INVALID;
+  if (((int64_t)num_blocks + 1) * block_size > INT32_MAX) return PA_ERR_INVALID;
   return PA_OK;
 }
 
@@ -426,6 +426,8 @@ int lse_merge_impl(const void* workspace, size_t workspace_bytes, const int32_t*
   if (dtype != PA_FP16 && dtype != PA_BF16) return PA_ERR_DTYPE;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_INVALID;
   if (num_seqs < 0 || q_heads <= 0 || q_len < 1) return PA_ERR_INVALID;
+  // the merge kernels number their (request, query, head) rows in int32
+  if ((int64_t)num_seqs * q_len * q_heads > (int64_t)INT32_MAX - 8) return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
   DecodeSetup s;
   int st = decode_setup(num_seqs * q_len, q_heads, head_dim, max_blocks_per_seq, block_size, split_tokens, &s);
@@ -556,6 +558,7 @@ int pa_verify_split_tokens(int max_blocks_per_seq, int block_size, int q_len, in
 size_t pa_verify_workspace_size(int num_seqs, int q_len, int q_heads, int head_dim, int max_blocks_per_seq,
                                 int block_size, int split_tokens) {
   if (num_seqs < 0 || q_len < 1 || q_heads <= 0 || head_dim <= 0) return 0;
+  if ((int64_t)num_seqs * q_len > INT32_MAX) return 0;
   split_tokens = pa_verify_split_tokens(max_blocks_per_seq, block_size, q_len, split_tokens);
   if (split_tokens < 0) return 0;
   DecodeSetup s;
@@ -709,7 +712,7 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   if (num_seqs < 0 || num_seqs > 65535 || q_heads <= 0 || q_heads % kv_heads != 0 || q_heads / kv_heads > 16)
     return PA_ERR_INVALID;
   if (max_blocks_per_seq <= 0 || !std::isfinite(scale)) return PA_ERR_INVALID;
-  if (prefix_len <= 0 || prefix_len % block_size != 0 || prefix_len > max_blocks_per_seq * block_size)
+  if (prefix_len <= 0 || prefix_len % block_size != 0 || prefix_len > (int64_t)max_blocks_per_seq * block_size)
     return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
   if (block_size < 8)  // no tensor-core prefix pass for 4-token blocks: same result through pa_decode

@@ -113,3 +113,20 @@ def test_newer_calls_reject_bad_arguments_before_touching_the_gpu(lib):
     # shared prefix: prefix not a multiple of the block size
     assert lib.pa_decode_shared_prefix(16, 16, 16, 16, 20, 16, 8, 16, 2, 8, 2, 128, 16, 64, 0.1, 0, 16, 1 << 20,
                                        16, 1, None, None) == inv
+
+
+def test_sizes_past_the_int32_index_math_are_refused_on_the_host(lib):
+    inv = _lib.PA_ERR_INVALID
+    big = 2**31 - 1
+    # a pool whose last row coordinate (one past it included) passes int32
+    assert lib.pa_copy_blocks(16, 16, 16, 1, big, 16, 1, 64, 1, None) == inv
+    assert lib.pa_copy_blocks(16, 16, 16, 1, big // 16, 16, 1, 64, 1, None) == inv
+    # merge rows (request x query x head) past int32
+    assert lib.pa_lse_merge(16, 1 << 40, 16, 1 << 20, 4096, 128, 4, 16, 0, 16, 1, None) == inv
+    assert lib.pa_lse_merge(16, 1 << 40, 16, 65536, 32768, 128, 4, 16, 0, 16, 1, None) == inv   # 2^31 rows
+    assert lib.pa_lse_merge(16, 1 << 40, 16, 65535, 32768, 128, 4, 16, 0, 16, 1, None) == _lib.PA_OK  # fits; one partition: nothing to merge
+    # a workspace size query whose request x query count passes int32 is 0 (invalid)
+    assert lib.pa_verify_workspace_size(1 << 30, 8, 8, 128, 64, 16, 128) == 0
+    # a shared prefix against a table whose token capacity passes int32
+    assert lib.pa_decode_shared_prefix(16, 16, 16, 16, 1024, 16, big, 16, 2, 8, 2, 128, 16, 64, 0.1, 0, 16,
+                                       1 << 20, 16, 1, None, None) == inv
