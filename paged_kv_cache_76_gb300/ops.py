@@ -132,14 +132,48 @@ def _cache_dims(k_cache: torch.Tensor):
     return k_cache.shape
 
 
+# The C calls take raw pointers and sizes; these checks are what keeps a
+# mismatched tensor from being read as the wrong type, past its end, or from
+# another GPU's memory.
+def _check_caches(k_cache, v_cache):
+    _cache_dims(k_cache)
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype or v_cache.device != k_cache.device:
+        raise ValueError("k_cache and v_cache must agree in shape, dtype and device")
+
+
+def _check_index(ref, name: str, t, rows: int, cols: int = None, table: bool = False):
+    """An index tensor on ref's device with `rows` leading entries; 2-D with
+    `cols` columns if given, 2-D if `table`."""
+    if t.device != ref.device:
+        raise ValueError(f"{name} is on {t.device}, not {ref.device}")
+    two_d = table or cols is not None
+    if t.dim() == 0 or t.shape[0] != rows or (two_d and t.dim() != 2) or (cols is not None and t.shape[1] != cols):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}: {rows} rows{' x ' + str(cols) if cols else ''} expected")
+
+
+def _check_attention(q, k_cache, v_cache, out):
+    """q, both caches and out share one dtype and device; out has q's shape."""
+    _check_caches(k_cache, v_cache)
+    if k_cache.dtype != q.dtype or out.dtype != q.dtype:
+        raise TypeError(f"q ({q.dtype}), the caches ({k_cache.dtype}) and out ({out.dtype}) must share a dtype")
+    if k_cache.device != q.device or out.device != q.device:
+        raise ValueError("q, the caches and out must be on one device")
+    if out.shape != q.shape:
+        raise ValueError(f"out has shape {tuple(out.shape)}, q {tuple(q.shape)}")
+
+
 def launch_count() -> int:
     return int(_lib.lib().pa_launch_count())
 
 
 def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None):
     nb, bs, hkv, d = _cache_dims(k_cache)
-    if v_cache.shape != k_cache.shape or k.shape != v.shape or k.shape[1:] != (hkv, d):
-        raise ValueError("shape mismatch")
+    _check_caches(k_cache, v_cache)
+    if k.shape != v.shape or k.dim() != 3 or k.shape[1:] != (hkv, d):
+        raise ValueError("k and v are [num_tokens, kv_heads, head_dim] of the cache")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or k.device != k_cache.device or v.device != k.device:
+        raise ValueError("k and v must have the cache's dtype and device")
+    _check_index(k, "slot_mapping", slot_mapping, int(k.shape[0]))
     _launch(
         "pa_reshape_and_cache",
         _dev(k, "k"), _dev(v, "v"), _i32(slot_mapping, "slot_mapping"), int(k.shape[0]),
@@ -150,6 +184,8 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None):
 def copy_blocks(k_cache, v_cache, pairs, stream=None):
     """``pairs``: int32 [n, 2] (src, dst) on the cache's device."""
     nb, bs, hkv, d = _cache_dims(k_cache)
+    _check_caches(k_cache, v_cache)
+    _check_index(k_cache, "pairs", pairs, int(pairs.shape[0]) if pairs.dim() else -1, 2)
     _launch(
         "pa_copy_blocks",
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(pairs, "pairs"), int(pairs.shape[0]),
@@ -192,11 +228,19 @@ def decode_workspace_size(num_seqs, q_heads, head_dim, max_blocks_per_seq, block
                                                    block_size, split_tokens))
 
 
+def _check_decode(q, k_cache, v_cache, block_tables, context_lens, out):
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    if q.dim() != 3 or q.shape[2] != d:
+        raise ValueError("q is [num_seqs, q_heads, head_dim] of the cache's head_dim")
+    _check_attention(q, k_cache, v_cache, out)
+    _check_index(q, "block_tables", block_tables, int(q.shape[0]), table=True)
+    _check_index(q, "context_lens", context_lens, int(q.shape[0]))
+
+
 def _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, workspace):
     nb, bs, hkv, d = _cache_dims(k_cache)
     B, hq, dq = q.shape
-    if dq != d or out.shape != q.shape or block_tables.shape[0] != B or context_lens.shape[0] != B:
-        raise ValueError("shape mismatch")
+    _check_decode(q, k_cache, v_cache, block_tables, context_lens, out)
     maxblk = int(block_tables.shape[1])
     ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
         if workspace is not None else (None, 0)
@@ -218,6 +262,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, spl
            stream=None):
     if out is None:
         out = torch.empty_like(q)
+    _check_decode(q, k_cache, v_cache, block_tables, context_lens, out)
     if workspace is None:
         workspace = make_workspace(q, block_tables, k_cache.shape[1], split_tokens)
     args = _decode_args(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, workspace)
@@ -234,7 +279,11 @@ def decode_partial(q, k_cache, v_cache, block_tables, context_lens, scale, out, 
 
 def lse_merge(workspace, context_lens, q, block_tables, block_size, out, split_tokens=0, stream=None):
     B, hq, d = q.shape
-    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    if out.shape != q.shape or out.device != q.device:
+        raise ValueError("out must have q's shape and device")
+    _check_index(q, "context_lens", context_lens, B)
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (None, 0)
     _launch("pa_lse_merge", ws_ptr, ws_bytes, _i32(context_lens, "context_lens"), B, hq, d,
             int(block_tables.shape[1]), block_size, int(split_tokens), _dev(out, "out"), dtype_code(out.dtype),
             _stream(stream))
@@ -260,8 +309,11 @@ def verify_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=No
     B, ql, hq, dq = q.shape
     if out is None:
         out = torch.empty_like(q)
-    if dq != d or out.shape != q.shape or block_tables.shape[0] != B or context_lens.shape[0] != B:
-        raise ValueError("shape mismatch")
+    if dq != d:
+        raise ValueError("head_dim mismatch")
+    _check_attention(q, k_cache, v_cache, out)
+    _check_index(q, "block_tables", block_tables, B, table=True)
+    _check_index(q, "context_lens", context_lens, B)
     maxblk = int(block_tables.shape[1])
     if workspace is None:
         n = verify_workspace_size(B, ql, hq, d, maxblk, bs, split_tokens)
@@ -299,10 +351,15 @@ def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_t
     of ``q``, the prefix's K/V and the previous use of ``workspace``."""
     nb, bs, hkv, d = _cache_dims(k_cache)
     B, hq, dq = q.shape
-    if dq != d or block_tables.shape[0] != B or context_lens.shape[0] != B:
-        raise ValueError("shape mismatch")
+    if dq != d:
+        raise ValueError("head_dim mismatch")
     if out is None:
         out = torch.empty_like(q)
+    _check_attention(q, k_cache, v_cache, out)
+    _check_index(q, "block_tables", block_tables, B, table=True)
+    _check_index(q, "context_lens", context_lens, B)
+    if prefix_blocks.device != q.device or prefix_blocks.numel() < int(prefix_len) // bs:
+        raise ValueError("prefix_blocks must hold prefix_len / block_size block ids on q's device")
     maxblk = int(block_tables.shape[1])
     if workspace is None:
         n = decode_shared_prefix_workspace_size(B, hq, d, maxblk, bs, int(prefix_len), split_tokens)
@@ -312,7 +369,8 @@ def decode_shared_prefix(q, k_cache, v_cache, prefix_blocks, prefix_len, block_t
         "pa_decode_shared_prefix",
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _i32(prefix_blocks, "prefix_blocks"),
         int(prefix_len), _i32(block_tables, "block_tables"), maxblk, _i32(context_lens, "context_lens"), B, hq, hkv,
-        d, bs, nb, float(scale), int(split_tokens), workspace.data_ptr(), workspace.numel(), _dev(out, "out"),
+        d, bs, nb, float(scale), int(split_tokens), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _dev(out, "out"),
         dtype_code(q.dtype), _stream(stream), prefix_stream.cuda_stream if prefix_stream is not None else None)
     return out
 
@@ -326,6 +384,9 @@ def verify_decode_tc(q, k_cache, v_cache, block_tables, context_lens, scale, out
         raise ValueError("head_dim mismatch")
     if out is None:
         out = torch.empty_like(q)
+    _check_attention(q, k_cache, v_cache, out)
+    _check_index(q, "block_tables", block_tables, B, table=True)
+    _check_index(q, "context_lens", context_lens, B)
     _keep(out)
     _launch("pa_verify_decode_tc", _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
             _i32(block_tables, "block_tables"), int(block_tables.shape[1]), _i32(context_lens, "context_lens"), B,
@@ -342,10 +403,12 @@ def chunked_prefill(q, q_start, context_lens, k_cache, v_cache, block_tables, sc
     if dq != d:
         raise ValueError("head_dim mismatch")
     R = int(context_lens.shape[0])
-    if q_start.shape[0] != R + 1 or block_tables.shape[0] != R:
-        raise ValueError("q_start must have num_reqs+1 entries")
     if out is None:
         out = torch.empty_like(q)
+    _check_attention(q, k_cache, v_cache, out)
+    _check_index(q, "context_lens", context_lens, R)
+    _check_index(q, "q_start", q_start, R + 1)
+    _check_index(q, "block_tables", block_tables, R, table=True)
     _keep(out)
     _launch(
         "pa_chunked_prefill",

@@ -42,6 +42,25 @@ def _i32(t, name):
     return _dev(t, name)
 
 
+def _rows(ref, *named):
+    """Each (name, tensor, rows) is on ref's device with `rows` leading entries:
+    the C calls read them by pointer, past their end otherwise."""
+    for name, t, rows in named:
+        if t.device != ref.device:
+            raise ValueError(f"{name} is on {t.device}, not {ref.device}")
+        if t.dim() == 0 or t.shape[0] != rows:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}: {rows} rows expected")
+
+
+def _check_contiguous_kv(k_cache, v_cache, dtype, head_dim):
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("caches are [num_slots, max_len, kv_heads, head_dim], K and V alike")
+    if k_cache.dtype != dtype or v_cache.dtype != dtype or k_cache.shape[3] != head_dim:
+        raise ValueError("the caches must have the data's dtype and head_dim")
+    if v_cache.device != k_cache.device:
+        raise ValueError("k_cache and v_cache must be on one device")
+
+
 def _code(dt):
     if dt == torch.bfloat16:
         return _lib.PA_BF16
@@ -137,6 +156,9 @@ class VirtualKV:
         B, hq, d = q.shape
         if out is None:
             out = torch.empty_like(q)
+        if d != self.head_dim or q.dtype != self.dtype or out.dtype != q.dtype or out.shape != q.shape:
+            raise ValueError("q and out are [num_seqs, q_heads, head_dim] of the KV's head_dim and dtype")
+        _rows(q, ("slot_ids", slot_ids, B), ("context_lens", context_lens, B), ("out", out, B))
         if workspace is None:
             n = int(self._L.pa_decode_workspace_size(B, hq, d, self.max_len // 16, 16, int(split_tokens)))
             workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
@@ -148,6 +170,11 @@ class VirtualKV:
         return out
 
     def reshape_and_cache(self, layer, k, v, slot_ids, positions, stream=None):
+        if k.shape != v.shape or k.dim() != 3 or tuple(k.shape[1:]) != (self.kv_heads, self.head_dim) or \
+                k.dtype != self.dtype or v.dtype != self.dtype:
+            raise ValueError("k and v are [num_tokens, kv_heads, head_dim] of the KV's dtype")
+        n = int(k.shape[0])
+        _rows(k, ("v", v, n), ("slot_ids", slot_ids, n), ("positions", positions, n))
         _launch("pa_vkv_reshape_and_cache", self._h, int(layer), _dev(k, "k"), _dev(v, "v"),
                 _i32(slot_ids, "slot_ids"), _i32(positions, "positions"), int(k.shape[0]), _stream(stream))
 
@@ -159,6 +186,14 @@ def decode_contiguous(q, k_cache, v_cache, slot_ids, context_lens, scale, slot_t
     B, hq, dq = q.shape
     if out is None:
         out = torch.empty_like(q)
+    _check_contiguous_kv(k_cache, v_cache, q.dtype, dq)
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must have q's shape and dtype")
+    _rows(q, ("context_lens", context_lens, B), ("out", out, B), ("k_cache", k_cache, ns))
+    if slot_ids is not None:
+        _rows(q, ("slot_ids", slot_ids, B))
+    if slot_tokens is not None:
+        _rows(q, ("slot_tokens", slot_tokens, ns))
     lib = _lib.lib()
     if workspace is None:
         n = int(lib.pa_decode_workspace_size(B, hq, d, L // 16, 16, int(split_tokens)))
@@ -176,6 +211,13 @@ def decode_contiguous(q, k_cache, v_cache, slot_ids, context_lens, scale, slot_t
 
 def reshape_and_cache_slots(k, v, slot_ids, positions, k_cache, v_cache, slot_tokens=None, stream=None):
     ns, L, hkv, d = k_cache.shape
+    _check_contiguous_kv(k_cache, v_cache, k.dtype, d)
+    if k.shape != v.shape or k.dim() != 3 or tuple(k.shape[1:]) != (hkv, d) or v.dtype != k.dtype:
+        raise ValueError("k and v are [num_tokens, kv_heads, head_dim] of the cache")
+    n = int(k.shape[0])
+    _rows(k, ("v", v, n), ("slot_ids", slot_ids, n), ("positions", positions, n), ("k_cache", k_cache, ns))
+    if slot_tokens is not None:
+        _rows(k, ("slot_tokens", slot_tokens, ns))
     _launch(
         "pa_reshape_and_cache_slots",
         _dev(k, "k"), _dev(v, "v"), _i32(slot_ids, "slot_ids"), _i32(positions, "positions"), int(k.shape[0]),
