@@ -58,7 +58,8 @@ typedef enum {
   PA_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed              */
   PA_ERR_DEVICE_CHECK = -5,   /* pa_get_device_error found a recorded error     */
   PA_ERR_SHARED_BLOCK = -6,   /* append into a shared partial block: cow first  */
-  PA_ERR_WORKSPACE = -7       /* workspace missing or smaller than required     */
+  PA_ERR_WORKSPACE = -7,      /* workspace missing or smaller than required     */
+  PA_ERR_HOST_MEMORY = -8     /* a host allocation failed; nothing changed      */
 } pa_status;
 
 typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;

@@ -21,6 +21,7 @@ PA_ERR_CUDA = -4
 PA_ERR_DEVICE_CHECK = -5
 PA_ERR_SHARED_BLOCK = -6
 PA_ERR_WORKSPACE = -7
+PA_ERR_HOST_MEMORY = -8
 
 PA_FP16 = 0
 PA_BF16 = 1
@@ -41,6 +42,11 @@ class PAError(RuntimeError):
     def __init__(self, status, what=""):
         self.status = status
         super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class PAHostMemoryError(PAError, MemoryError):
+    """PA_ERR_HOST_MEMORY: a host allocation inside the library failed (the
+    call changed nothing)."""
 
 
 class AllocStats(C.Structure):
@@ -171,6 +177,8 @@ def status_string(status: int) -> str:
 
 
 def check(status: int, what: str = ""):
+    if status == PA_ERR_HOST_MEMORY:
+        raise PAHostMemoryError(status, what)
     if status < 0:
         raise PAError(status, what)
     return status

@@ -21,14 +21,18 @@
 //    free queue; swap-out moves a request's blocks there (pairs for the
 //    copy) and releases its GPU blocks as a free would, swap-in takes new GPU
 //    blocks and returns the CPU ones.
-// Every entry point validates first and mutates only once success is certain.
+// Every entry point validates first and mutates only once success is certain;
+// the host memory an entry point needs is allocated before it mutates
+// anything, and a failed allocation returns PA_ERR_HOST_MEMORY (pa_guarded).
 #include <algorithm>
 #include <cstdint>
+#include <memory>
 #include <new>
 #include <unordered_map>
 #include <vector>
 
 #include "pa.h"
+#include "pa_guard.h"
 
 namespace {
 
@@ -187,6 +191,7 @@ static int grow(pa_alloc* a, Seq* s, int n_tokens, int32_t* slots_out) {
     ++a->alloc_failures;
     return PA_ERR_NO_FREE_BLOCKS;
   }
+  if (need > 0) s->blocks.reserve(s->blocks.size() + (size_t)need);  // may throw: before any change
   for (int64_t i = 0; i < need; ++i) s->blocks.push_back(a->take());
   if (slots_out) {
     for (int64_t t = cur; t < cur + n_tokens; ++t)
@@ -199,74 +204,81 @@ static int grow(pa_alloc* a, Seq* s, int n_tokens, int32_t* slots_out) {
 extern "C" {
 
 int pa_alloc_create(int num_blocks, int block_size, const int32_t* initial_free_order, pa_alloc** out) {
-  if (!out || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID;
-  *out = nullptr;
-  if (initial_free_order) {
-    std::vector<uint8_t> seen(num_blocks, 0);
-    for (int i = 0; i < num_blocks; ++i) {
-      int32_t b = initial_free_order[i];
-      if (b < 0 || b >= num_blocks || seen[b]) return PA_ERR_INVALID;
-      seen[b] = 1;
+  return pa_guarded([&]() -> int {
+    if (!out || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID;
+    *out = nullptr;
+    if (initial_free_order) {
+      std::vector<uint8_t> seen(num_blocks, 0);
+      for (int i = 0; i < num_blocks; ++i) {
+        int32_t b = initial_free_order[i];
+        if (b < 0 || b >= num_blocks || seen[b]) return PA_ERR_INVALID;
+        seen[b] = 1;
+      }
     }
-  }
-  pa_alloc* a = new (std::nothrow) pa_alloc();
-  if (!a) return PA_ERR_INVALID;
-  a->num_blocks = num_blocks;
-  a->block_size = block_size;
-  a->ref.assign(num_blocks, 0);
-  a->prev.assign(num_blocks, -1);
-  a->next.assign(num_blocks, -1);
-  a->in_free.assign(num_blocks, 0);
-  a->hash.assign(num_blocks, 0);
-  a->has_hash.assign(num_blocks, 0);
-  for (int i = 0; i < num_blocks; ++i) a->push_back(initial_free_order ? initial_free_order[i] : i);
-  *out = a;
-  return PA_OK;
+    std::unique_ptr<pa_alloc> a(new pa_alloc());
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->ref.assign(num_blocks, 0);
+    a->prev.assign(num_blocks, -1);
+    a->next.assign(num_blocks, -1);
+    a->in_free.assign(num_blocks, 0);
+    a->hash.assign(num_blocks, 0);
+    a->has_hash.assign(num_blocks, 0);
+    for (int i = 0; i < num_blocks; ++i) a->push_back(initial_free_order ? initial_free_order[i] : i);
+    *out = a.release();
+    return PA_OK;
+  });
 }
 
 void pa_alloc_destroy(pa_alloc* a) { delete a; }
 
 int pa_alloc_add_seq(pa_alloc* a, int seq_id) {
-  if (!a || seq_id < 0 || a->find(seq_id)) return PA_ERR_INVALID;
-  a->seqs.emplace(seq_id, Seq());
-  return PA_OK;
+  return pa_guarded([&]() -> int {
+    if (!a || seq_id < 0 || a->find(seq_id)) return PA_ERR_INVALID;
+    a->seqs.emplace(seq_id, Seq());
+    return PA_OK;
+  });
 }
 
 int pa_alloc_append_slots(pa_alloc* a, int seq_id, int n_tokens, int32_t* slots_out) {
-  if (!a || n_tokens < 0) return PA_ERR_INVALID;
-  Seq* s = a->find(seq_id);
-  if (!s || s->swapped) return PA_ERR_INVALID;
-  const int st = grow(a, s, n_tokens, slots_out);
-  if (st == PA_OK && n_tokens > 0) {  // token ids unknown: nothing more is hashed
-    s->hashable = false;
-    s->pending.clear();
-  }
-  return st;
+  return pa_guarded([&]() -> int {
+    if (!a || n_tokens < 0) return PA_ERR_INVALID;
+    Seq* s = a->find(seq_id);
+    if (!s || s->swapped) return PA_ERR_INVALID;
+    const int st = grow(a, s, n_tokens, slots_out);
+    if (st == PA_OK && n_tokens > 0) {  // token ids unknown: nothing more is hashed
+      s->hashable = false;
+      s->pending.clear();
+    }
+    return st;
+  });
 }
 
 int pa_alloc_share(pa_alloc* a, int dst_seq, int src_seq, int n_tokens) {
-  if (!a || dst_seq == src_seq) return PA_ERR_INVALID;
-  Seq* d = a->find(dst_seq);
-  Seq* s = a->find(src_seq);
-  if (!d || !s || d->swapped || s->swapped || !d->blocks.empty() || d->num_tokens != 0) return PA_ERR_INVALID;
-  if (n_tokens < 0 || n_tokens > s->num_tokens) return PA_ERR_INVALID;
-  const int64_t nblk = cdiv64(n_tokens, a->block_size);
-  d->blocks.assign(s->blocks.begin(), s->blocks.begin() + nblk);
-  for (int32_t b : d->blocks) a->touch(b);
-  d->num_tokens = n_tokens;
-  // the hash chain continues into dst only from a full, hashed last block
-  d->salt = s->salt;
-  d->pending.clear();
-  if (n_tokens == 0) {
-    d->parent = s->salt;
-    d->hashable = true;
-  } else if (n_tokens % a->block_size == 0 && a->has_hash[d->blocks.back()]) {
-    d->parent = a->hash[d->blocks.back()];
-    d->hashable = true;
-  } else {
-    d->hashable = false;
-  }
-  return PA_OK;
+  return pa_guarded([&]() -> int {
+    if (!a || dst_seq == src_seq) return PA_ERR_INVALID;
+    Seq* d = a->find(dst_seq);
+    Seq* s = a->find(src_seq);
+    if (!d || !s || d->swapped || s->swapped || !d->blocks.empty() || d->num_tokens != 0) return PA_ERR_INVALID;
+    if (n_tokens < 0 || n_tokens > s->num_tokens) return PA_ERR_INVALID;
+    const int64_t nblk = cdiv64(n_tokens, a->block_size);
+    d->blocks.assign(s->blocks.begin(), s->blocks.begin() + nblk);
+    for (int32_t b : d->blocks) a->touch(b);
+    d->num_tokens = n_tokens;
+    // the hash chain continues into dst only from a full, hashed last block
+    d->salt = s->salt;
+    d->pending.clear();
+    if (n_tokens == 0) {
+      d->parent = s->salt;
+      d->hashable = true;
+    } else if (n_tokens % a->block_size == 0 && a->has_hash[d->blocks.back()]) {
+      d->parent = a->hash[d->blocks.back()];
+      d->hashable = true;
+    } else {
+      d->hashable = false;
+    }
+    return PA_OK;
+  });
 }
 
 int pa_alloc_cow(pa_alloc* a, int seq_id, int logical_block, int32_t* src_dst_out) {
@@ -292,29 +304,32 @@ int pa_alloc_cow(pa_alloc* a, int seq_id, int logical_block, int32_t* src_dst_ou
 }
 
 int pa_alloc_free_seq(pa_alloc* a, int seq_id) {
-  if (!a) return PA_ERR_INVALID;
-  auto it = a->seqs.find(seq_id);
-  if (it == a->seqs.end()) return PA_ERR_INVALID;
-  const std::vector<int32_t>& blocks = it->second.blocks;
-  if (it->second.swapped) {  // swap-pool blocks back to that pool's head, last first
-    for (int32_t c : blocks) a->cpu.push_front(c);
+  return pa_guarded([&]() -> int {
+    if (!a) return PA_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_INVALID;
+    const std::vector<int32_t>& blocks = it->second.blocks;
+    if (it->second.swapped) {  // swap-pool blocks back to that pool's head, last first
+      for (int32_t c : blocks) a->cpu.push_front(c);
+      a->seqs.erase(it);
+      return PA_OK;
+    }
+    // reverse order: tail block first; zero-count blocks are prepended keeping
+    // that order, i.e. pushed to the front from the last of them to the first
+    // (blocks without a hash); blocks with a hash are appended at the tail in
+    // release order, so they are evicted last and a request's first block last
+    std::vector<int32_t> no_hash, with_hash;
+    no_hash.reserve(blocks.size());
+    with_hash.reserve(blocks.size());
+    for (auto rit = blocks.rbegin(); rit != blocks.rend(); ++rit) {
+      a->ref[*rit] -= 1;
+      if (a->ref[*rit] == 0) (a->has_hash[*rit] ? with_hash : no_hash).push_back(*rit);
+    }
+    for (auto rit = no_hash.rbegin(); rit != no_hash.rend(); ++rit) a->push_front(*rit);
+    for (int32_t b : with_hash) a->push_back(b);
     a->seqs.erase(it);
     return PA_OK;
-  }
-  // reverse order: tail block first; zero-count blocks are prepended keeping
-  // that order, i.e. pushed to the front from the last of them to the first
-  // (blocks without a hash); blocks with a hash are appended at the tail in
-  // release order, so they are evicted last and a request's first block last
-  std::vector<int32_t> no_hash, with_hash;
-  no_hash.reserve(blocks.size());
-  for (auto rit = blocks.rbegin(); rit != blocks.rend(); ++rit) {
-    a->ref[*rit] -= 1;
-    if (a->ref[*rit] == 0) (a->has_hash[*rit] ? with_hash : no_hash).push_back(*rit);
-  }
-  for (auto rit = no_hash.rbegin(); rit != no_hash.rend(); ++rit) a->push_front(*rit);
-  for (int32_t b : with_hash) a->push_back(b);
-  a->seqs.erase(it);
-  return PA_OK;
+  });
 }
 
 int pa_alloc_block_table(const pa_alloc* a, int seq_id, int32_t* out, int cap, int* n_out) {
@@ -404,10 +419,12 @@ int pa_alloc_get_stats(const pa_alloc* a, pa_alloc_stats* out) {
 }
 
 int pa_alloc_enable_swap(pa_alloc* a, int num_cpu_blocks) {
-  if (!a || num_cpu_blocks <= 0 || a->num_cpu_blocks > 0) return PA_ERR_INVALID;
-  a->num_cpu_blocks = num_cpu_blocks;
-  a->cpu.init(num_cpu_blocks);
-  return PA_OK;
+  return pa_guarded([&]() -> int {
+    if (!a || num_cpu_blocks <= 0 || a->num_cpu_blocks > 0) return PA_ERR_INVALID;
+    a->num_cpu_blocks = num_cpu_blocks;
+    a->cpu.init(num_cpu_blocks);
+    return PA_OK;
+  });
 }
 
 int pa_alloc_num_free_cpu(const pa_alloc* a) { return a ? a->cpu.n : PA_ERR_INVALID; }
@@ -419,56 +436,61 @@ int pa_alloc_is_swapped(const pa_alloc* a, int seq_id) {
 }
 
 int pa_alloc_swap_out(pa_alloc* a, int seq_id, int32_t* pairs_out, int cap, int* n_out) {
-  if (!a || a->num_cpu_blocks <= 0) return PA_ERR_INVALID;
-  Seq* s = a->find(seq_id);
-  if (!s || s->swapped) return PA_ERR_INVALID;
-  const int n = (int)s->blocks.size();
-  if (n_out) *n_out = n;
-  if (n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID;
-  if (n > a->cpu.n) {
-    ++a->alloc_failures;
-    return PA_ERR_NO_FREE_BLOCKS;
-  }
-  std::vector<int32_t> cpu_blocks(n);
-  for (int i = 0; i < n; ++i) {
-    cpu_blocks[i] = a->cpu.pop_front();
-    pairs_out[2 * i] = s->blocks[i];
-    pairs_out[2 * i + 1] = cpu_blocks[i];
-  }
-  // release the GPU blocks exactly as pa_alloc_free_seq does
-  std::vector<int32_t> no_hash, with_hash;
-  for (auto rit = s->blocks.rbegin(); rit != s->blocks.rend(); ++rit) {
-    a->ref[*rit] -= 1;
-    if (a->ref[*rit] == 0) (a->has_hash[*rit] ? with_hash : no_hash).push_back(*rit);
-  }
-  for (auto rit = no_hash.rbegin(); rit != no_hash.rend(); ++rit) a->push_front(*rit);
-  for (int32_t b : with_hash) a->push_back(b);
-  s->blocks = std::move(cpu_blocks);
-  s->swapped = true;
-  return PA_OK;
+  return pa_guarded([&]() -> int {
+    if (!a || a->num_cpu_blocks <= 0) return PA_ERR_INVALID;
+    Seq* s = a->find(seq_id);
+    if (!s || s->swapped) return PA_ERR_INVALID;
+    const int n = (int)s->blocks.size();
+    if (n_out) *n_out = n;
+    if (n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID;
+    if (n > a->cpu.n) {
+      ++a->alloc_failures;
+      return PA_ERR_NO_FREE_BLOCKS;
+    }
+    std::vector<int32_t> cpu_blocks(n), no_hash, with_hash;
+    no_hash.reserve(n);
+    with_hash.reserve(n);
+    for (int i = 0; i < n; ++i) {
+      cpu_blocks[i] = a->cpu.pop_front();
+      pairs_out[2 * i] = s->blocks[i];
+      pairs_out[2 * i + 1] = cpu_blocks[i];
+    }
+    // release the GPU blocks exactly as pa_alloc_free_seq does
+    for (auto rit = s->blocks.rbegin(); rit != s->blocks.rend(); ++rit) {
+      a->ref[*rit] -= 1;
+      if (a->ref[*rit] == 0) (a->has_hash[*rit] ? with_hash : no_hash).push_back(*rit);
+    }
+    for (auto rit = no_hash.rbegin(); rit != no_hash.rend(); ++rit) a->push_front(*rit);
+    for (int32_t b : with_hash) a->push_back(b);
+    s->blocks = std::move(cpu_blocks);
+    s->swapped = true;
+    return PA_OK;
+  });
 }
 
 int pa_alloc_swap_in(pa_alloc* a, int seq_id, int32_t* pairs_out, int cap, int* n_out) {
-  if (!a) return PA_ERR_INVALID;
-  Seq* s = a->find(seq_id);
-  if (!s || !s->swapped) return PA_ERR_INVALID;
-  const int n = (int)s->blocks.size();
-  if (n_out) *n_out = n;
-  if (n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID;
-  if (n > a->num_free) {
-    ++a->alloc_failures;
-    return PA_ERR_NO_FREE_BLOCKS;
-  }
-  std::vector<int32_t> gpu_blocks(n);
-  for (int i = 0; i < n; ++i) {
-    gpu_blocks[i] = a->take();
-    pairs_out[2 * i] = s->blocks[i];
-    pairs_out[2 * i + 1] = gpu_blocks[i];
-  }
-  for (int32_t c : s->blocks) a->cpu.push_front(c);  // last block ends at the head
-  s->blocks = std::move(gpu_blocks);
-  s->swapped = false;
-  return PA_OK;
+  return pa_guarded([&]() -> int {
+    if (!a) return PA_ERR_INVALID;
+    Seq* s = a->find(seq_id);
+    if (!s || !s->swapped) return PA_ERR_INVALID;
+    const int n = (int)s->blocks.size();
+    if (n_out) *n_out = n;
+    if (n > cap || (n > 0 && !pairs_out)) return PA_ERR_INVALID;
+    if (n > a->num_free) {
+      ++a->alloc_failures;
+      return PA_ERR_NO_FREE_BLOCKS;
+    }
+    std::vector<int32_t> gpu_blocks(n);
+    for (int i = 0; i < n; ++i) {
+      gpu_blocks[i] = a->take();
+      pairs_out[2 * i] = s->blocks[i];
+      pairs_out[2 * i + 1] = gpu_blocks[i];
+    }
+    for (int32_t c : s->blocks) a->cpu.push_front(c);  // last block ends at the head
+    s->blocks = std::move(gpu_blocks);
+    s->swapped = false;
+    return PA_OK;
+  });
 }
 
 uint64_t pa_block_hash(uint64_t parent, const int32_t* tokens, int n) {
@@ -483,58 +505,69 @@ int pa_alloc_enable_prefix_caching(pa_alloc* a) {
 
 int pa_alloc_add_seq_cached(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, uint64_t salt,
                             int* n_cached_out) {
-  if (!a || seq_id < 0 || a->find(seq_id) || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID;
-  const int64_t bs = a->block_size;
-  // longest run of cached prompt blocks, looked up in order (nothing changes yet)
-  std::vector<int32_t> hits;
-  uint64_t parent = salt;
-  if (a->caching && n_tokens > 0) {
-    const int64_t nfull = (int64_t)(n_tokens - 1) / bs;  // leave >= 1 token to compute
-    for (int64_t i = 0; i < nfull; ++i) {
-      const uint64_t h = hash_block(parent, tokens + i * bs, bs);
-      ++a->lookup_blocks;
-      auto it = a->cached.find(h);
-      if (it == a->cached.end()) break;
-      hits.push_back(it->second);
-      parent = h;
+  return pa_guarded([&]() -> int {
+    if (!a || seq_id < 0 || a->find(seq_id) || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID;
+    const int64_t bs = a->block_size;
+    // longest run of cached prompt blocks, looked up in order (nothing changes yet)
+    std::vector<int32_t> hits;
+    uint64_t parent = salt;
+    if (a->caching && n_tokens > 0) {
+      const int64_t nfull = (int64_t)(n_tokens - 1) / bs;  // leave >= 1 token to compute
+      for (int64_t i = 0; i < nfull; ++i) {
+        const uint64_t h = hash_block(parent, tokens + i * bs, bs);
+        ++a->lookup_blocks;
+        auto it = a->cached.find(h);
+        if (it == a->cached.end()) break;
+        hits.push_back(it->second);
+        parent = h;
+      }
     }
-  }
-  a->hit_blocks += (int64_t)hits.size();
-  Seq sq;
-  sq.salt = salt;
-  sq.parent = parent;
-  sq.blocks = hits;
-  sq.num_tokens = (int64_t)hits.size() * bs;
-  for (int32_t b : hits) a->touch(b);
-  a->seqs.emplace(seq_id, std::move(sq));
-  if (n_cached_out) *n_cached_out = (int)(hits.size() * bs);
-  return PA_OK;
+    a->hit_blocks += (int64_t)hits.size();
+    Seq sq;
+    sq.salt = salt;
+    sq.parent = parent;
+    sq.blocks = hits;
+    sq.num_tokens = (int64_t)hits.size() * bs;
+    a->seqs.emplace(seq_id, std::move(sq));  // may throw: before any block changes hands
+    for (int32_t b : hits) a->touch(b);
+    if (n_cached_out) *n_cached_out = (int)(hits.size() * bs);
+    return PA_OK;
+  });
 }
 
 int pa_alloc_append_tokens(pa_alloc* a, int seq_id, const int32_t* tokens, int n_tokens, int32_t* slots_out) {
-  if (!a || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID;
-  Seq* s = a->find(seq_id);
-  if (!s || s->swapped) return PA_ERR_INVALID;
-  const int64_t first = s->num_tokens;
-  const int st = grow(a, s, n_tokens, slots_out);
-  if (st != PA_OK || !s->hashable) return st;
-  // register every block these tokens fill (unless its hash is already cached)
-  const int64_t bs = a->block_size;
-  for (int i = 0; i < n_tokens; ++i) {
-    s->pending.push_back(tokens[i]);
-    if ((int64_t)s->pending.size() == bs) {
-      const uint64_t h = hash_block(s->parent, s->pending.data(), bs);
-      const int32_t b = s->blocks[(first + i) / bs];
-      if (a->caching && a->cached.find(h) == a->cached.end()) {
-        a->cached.emplace(h, b);
-        a->hash[b] = h;
-        a->has_hash[b] = 1;
+  return pa_guarded([&]() -> int {
+    if (!a || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID;
+    Seq* s = a->find(seq_id);
+    if (!s || s->swapped) return PA_ERR_INVALID;
+    const int64_t first = s->num_tokens;
+    const int st = grow(a, s, n_tokens, slots_out);
+    if (st != PA_OK || !s->hashable) return st;
+    // register every block these tokens fill (unless its hash is already
+    // cached).  The slots are taken at this point, so a failed host allocation
+    // here only ends the sequence's caching (it stays correct, uncached).
+    const int64_t bs = a->block_size;
+    try {
+      for (int i = 0; i < n_tokens; ++i) {
+        s->pending.push_back(tokens[i]);
+        if ((int64_t)s->pending.size() == bs) {
+          const uint64_t h = hash_block(s->parent, s->pending.data(), bs);
+          const int32_t b = s->blocks[(first + i) / bs];
+          if (a->caching && a->cached.find(h) == a->cached.end()) {
+            a->cached.emplace(h, b);
+            a->hash[b] = h;
+            a->has_hash[b] = 1;
+          }
+          s->parent = h;
+          s->pending.clear();
+        }
       }
-      s->parent = h;
+    } catch (const std::bad_alloc&) {
+      s->hashable = false;
       s->pending.clear();
     }
-  }
-  return PA_OK;
+    return PA_OK;
+  });
 }
 
 int pa_alloc_block_hash(const pa_alloc* a, int block_id, uint64_t* hash_out, int* is_cached_out) {
@@ -563,188 +596,190 @@ constexpr int64_t kExportVersion = 1;
 }  // namespace
 
 int pa_alloc_export(const pa_alloc* a, int64_t* out, int64_t cap, int64_t* n_out) {
-  if (!a || !n_out || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
-  std::vector<int64_t> w;
-  w.reserve(16 + 4 * (size_t)a->num_blocks);
-  w.push_back(kExportMagic);
-  w.push_back(kExportVersion);
-  w.push_back(a->num_blocks);
-  w.push_back(a->block_size);
-  w.push_back(a->caching ? 1 : 0);
-  w.push_back(a->num_cpu_blocks);
-  w.push_back(a->cow_copies);
-  w.push_back(a->alloc_failures);
-  w.push_back(a->lookup_blocks);
-  w.push_back(a->hit_blocks);
-  w.push_back(a->evictions);
-  w.push_back(a->num_free);
-  for (int32_t b = a->head; b >= 0; b = a->next[b]) w.push_back(b);
-  for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back(a->ref[b]);
-  for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back(a->has_hash[b]);
-  for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back((int64_t)a->hash[b]);
-  std::vector<std::pair<uint64_t, int32_t>> cached(a->cached.begin(), a->cached.end());
-  std::sort(cached.begin(), cached.end());
-  w.push_back((int64_t)cached.size());
-  for (const auto& kv : cached) {
-    w.push_back((int64_t)kv.first);
-    w.push_back(kv.second);
-  }
-  w.push_back(a->num_cpu_blocks > 0 ? a->cpu.n : 0);
-  if (a->num_cpu_blocks > 0)
-    for (int32_t b = a->cpu.head; b >= 0; b = a->cpu.next[b]) w.push_back(b);
-  std::vector<int> ids;
-  ids.reserve(a->seqs.size());
-  for (const auto& kv : a->seqs) ids.push_back(kv.first);
-  std::sort(ids.begin(), ids.end());
-  w.push_back((int64_t)ids.size());
-  for (int id : ids) {
-    const Seq& q = a->seqs.at(id);
-    w.push_back(id);
-    w.push_back(q.num_tokens);
-    w.push_back((int64_t)q.salt);
-    w.push_back((int64_t)q.parent);
-    w.push_back(q.hashable ? 1 : 0);
-    w.push_back(q.swapped ? 1 : 0);
-    w.push_back((int64_t)q.blocks.size());
-    for (int32_t b : q.blocks) w.push_back(b);
-    w.push_back((int64_t)q.pending.size());
-    for (int32_t t : q.pending) w.push_back(t);
-  }
-  *n_out = (int64_t)w.size();
-  if (cap < (int64_t)w.size()) return cap == 0 && !out ? PA_OK : PA_ERR_INVALID;
-  std::copy(w.begin(), w.end(), out);
-  return PA_OK;
+  return pa_guarded([&]() -> int {
+    if (!a || !n_out || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
+    std::vector<int64_t> w;
+    w.reserve(16 + 4 * (size_t)a->num_blocks);
+    w.push_back(kExportMagic);
+    w.push_back(kExportVersion);
+    w.push_back(a->num_blocks);
+    w.push_back(a->block_size);
+    w.push_back(a->caching ? 1 : 0);
+    w.push_back(a->num_cpu_blocks);
+    w.push_back(a->cow_copies);
+    w.push_back(a->alloc_failures);
+    w.push_back(a->lookup_blocks);
+    w.push_back(a->hit_blocks);
+    w.push_back(a->evictions);
+    w.push_back(a->num_free);
+    for (int32_t b = a->head; b >= 0; b = a->next[b]) w.push_back(b);
+    for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back(a->ref[b]);
+    for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back(a->has_hash[b]);
+    for (int32_t b = 0; b < a->num_blocks; ++b) w.push_back((int64_t)a->hash[b]);
+    std::vector<std::pair<uint64_t, int32_t>> cached(a->cached.begin(), a->cached.end());
+    std::sort(cached.begin(), cached.end());
+    w.push_back((int64_t)cached.size());
+    for (const auto& kv : cached) {
+      w.push_back((int64_t)kv.first);
+      w.push_back(kv.second);
+    }
+    w.push_back(a->num_cpu_blocks > 0 ? a->cpu.n : 0);
+    if (a->num_cpu_blocks > 0)
+      for (int32_t b = a->cpu.head; b >= 0; b = a->cpu.next[b]) w.push_back(b);
+    std::vector<int> ids;
+    ids.reserve(a->seqs.size());
+    for (const auto& kv : a->seqs) ids.push_back(kv.first);
+    std::sort(ids.begin(), ids.end());
+    w.push_back((int64_t)ids.size());
+    for (int id : ids) {
+      const Seq& q = a->seqs.at(id);
+      w.push_back(id);
+      w.push_back(q.num_tokens);
+      w.push_back((int64_t)q.salt);
+      w.push_back((int64_t)q.parent);
+      w.push_back(q.hashable ? 1 : 0);
+      w.push_back(q.swapped ? 1 : 0);
+      w.push_back((int64_t)q.blocks.size());
+      for (int32_t b : q.blocks) w.push_back(b);
+      w.push_back((int64_t)q.pending.size());
+      for (int32_t t : q.pending) w.push_back(t);
+    }
+    *n_out = (int64_t)w.size();
+    if (cap < (int64_t)w.size()) return cap == 0 && !out ? PA_OK : PA_ERR_INVALID;
+    std::copy(w.begin(), w.end(), out);
+    return PA_OK;
+  });
 }
 
 int pa_alloc_import(const int64_t* words, int64_t n, pa_alloc** out) {
-  if (!words || n <= 0 || !out) return PA_ERR_INVALID;
-  *out = nullptr;
-  int64_t i = 0;
-  bool bad = false;
-  auto next = [&](int64_t lo, int64_t hi) -> int64_t {  // next word, required in [lo, hi]
-    if (bad || i >= n) {
-      bad = true;
-      return lo;
-    }
-    const int64_t v = words[i++];
-    if (v < lo || v > hi) bad = true;
-    return v;
-  };
-  auto raw = [&]() -> int64_t {
-    if (bad || i >= n) {
-      bad = true;
-      return 0;
-    }
-    return words[i++];
-  };
-  if (next(kExportMagic, kExportMagic) != kExportMagic || next(kExportVersion, kExportVersion) != kExportVersion)
-    return PA_ERR_INVALID;
-  const int32_t nb = (int32_t)next(1, INT32_MAX), bs = (int32_t)next(1, INT32_MAX);
-  const bool caching = next(0, 1) != 0;
-  const int32_t ncpu = (int32_t)next(0, INT32_MAX);
-  if (bad || nb > n) return PA_ERR_INVALID;  // every block takes at least three words below
-  pa_alloc* a = new (std::nothrow) pa_alloc();
-  if (!a) return PA_ERR_INVALID;
-  a->num_blocks = nb;
-  a->block_size = bs;
-  a->caching = caching;
-  a->cow_copies = next(0, INT64_MAX);
-  a->alloc_failures = next(0, INT64_MAX);
-  a->lookup_blocks = next(0, INT64_MAX);
-  a->hit_blocks = next(0, INT64_MAX);
-  a->evictions = next(0, INT64_MAX);
-  a->ref.assign(nb, 0);
-  a->prev.assign(nb, -1);
-  a->next.assign(nb, -1);
-  a->in_free.assign(nb, 0);
-  a->hash.assign(nb, 0);
-  a->has_hash.assign(nb, 0);
-  const int64_t nfree = next(0, nb);
-  for (int64_t k = 0; !bad && k < nfree; ++k) {
-    const int32_t b = (int32_t)next(0, nb - 1);
-    if (!bad && a->in_free[b]) bad = true;
-    if (!bad) a->push_back(b);
-  }
-  for (int32_t b = 0; !bad && b < nb; ++b) a->ref[b] = (int32_t)next(0, INT32_MAX);
-  for (int32_t b = 0; !bad && b < nb; ++b) a->has_hash[b] = (uint8_t)next(0, 1);
-  for (int32_t b = 0; !bad && b < nb; ++b) a->hash[b] = (uint64_t)raw();
-  for (int32_t b = 0; !bad && b < nb; ++b)
-    if (a->in_free[b] && a->ref[b] != 0) bad = true;  // a free block has no owner
-  const int64_t ncached = next(0, nb);
-  for (int64_t k = 0; !bad && k < ncached; ++k) {
-    const uint64_t h = (uint64_t)raw();
-    const int32_t b = (int32_t)next(0, nb - 1);
-    if (!bad && (!a->has_hash[b] || a->hash[b] != h || !a->cached.emplace(h, b).second)) bad = true;
-  }
-  const int64_t ncpu_free = next(0, ncpu);
-  if (!bad && ncpu > 0) {
-    a->num_cpu_blocks = ncpu;
-    a->cpu.prev.assign(ncpu, -1);
-    a->cpu.next.assign(ncpu, -1);
-    std::vector<uint8_t> seen(ncpu, 0);
-    for (int64_t k = 0; !bad && k < ncpu_free; ++k) {
-      const int32_t b = (int32_t)next(0, ncpu - 1);
-      if (bad || seen[b]) {
+  return pa_guarded([&]() -> int {
+    if (!words || n <= 0 || !out) return PA_ERR_INVALID;
+    *out = nullptr;
+    int64_t i = 0;
+    bool bad = false;
+    auto next = [&](int64_t lo, int64_t hi) -> int64_t {  // next word, required in [lo, hi]
+      if (bad || i >= n) {
         bad = true;
-        break;
+        return lo;
       }
-      seen[b] = 1;
-      a->cpu.prev[b] = a->cpu.tail;  // append at the tail, in the exported order
-      if (a->cpu.tail < 0) a->cpu.head = b; else a->cpu.next[a->cpu.tail] = b;
-      a->cpu.tail = b;
-      ++a->cpu.n;
+      const int64_t v = words[i++];
+      if (v < lo || v > hi) bad = true;
+      return v;
+    };
+    auto raw = [&]() -> int64_t {
+      if (bad || i >= n) {
+        bad = true;
+        return 0;
+      }
+      return words[i++];
+    };
+    if (next(kExportMagic, kExportMagic) != kExportMagic || next(kExportVersion, kExportVersion) != kExportVersion)
+      return PA_ERR_INVALID;
+    const int32_t nb = (int32_t)next(1, INT32_MAX), bs = (int32_t)next(1, INT32_MAX);
+    const bool caching = next(0, 1) != 0;
+    const int32_t ncpu = (int32_t)next(0, INT32_MAX);
+    // every block takes at least three words below, and every swap block one
+    // (in the swap pool's free queue or in a swapped-out table)
+    if (bad || nb > n || ncpu > n) return PA_ERR_INVALID;
+    std::unique_ptr<pa_alloc> a(new pa_alloc());
+    a->num_blocks = nb;
+    a->block_size = bs;
+    a->caching = caching;
+    a->cow_copies = next(0, INT64_MAX);
+    a->alloc_failures = next(0, INT64_MAX);
+    a->lookup_blocks = next(0, INT64_MAX);
+    a->hit_blocks = next(0, INT64_MAX);
+    a->evictions = next(0, INT64_MAX);
+    a->ref.assign(nb, 0);
+    a->prev.assign(nb, -1);
+    a->next.assign(nb, -1);
+    a->in_free.assign(nb, 0);
+    a->hash.assign(nb, 0);
+    a->has_hash.assign(nb, 0);
+    const int64_t nfree = next(0, nb);
+    for (int64_t k = 0; !bad && k < nfree; ++k) {
+      const int32_t b = (int32_t)next(0, nb - 1);
+      if (!bad && a->in_free[b]) bad = true;
+      if (!bad) a->push_back(b);
     }
-  }
-  const int64_t nseq = next(0, n);
-  for (int64_t k = 0; !bad && k < nseq; ++k) {
-    const int id = (int)next(0, INT32_MAX);
-    Seq q;
-    q.num_tokens = next(0, INT64_MAX);
-    q.salt = (uint64_t)raw();
-    q.parent = (uint64_t)raw();
-    q.hashable = next(0, 1) != 0;
-    q.swapped = next(0, 1) != 0;
-    if (q.swapped && ncpu == 0) bad = true;
-    const int64_t nbk = next(0, n);
-    const int32_t lim = q.swapped ? ncpu : nb;
-    for (int64_t t = 0; !bad && t < nbk; ++t) q.blocks.push_back((int32_t)next(0, (int64_t)lim - 1));
-    if (!bad && (int64_t)q.blocks.size() * bs < q.num_tokens) bad = true;  // tokens beyond the blocks
-    const int64_t np = next(0, (int64_t)bs - 1);  // token ids of a block not yet full
-    for (int64_t t = 0; !bad && t < np; ++t) q.pending.push_back((int32_t)next(INT32_MIN, INT32_MAX));
-    if (!bad && !a->seqs.emplace(id, std::move(q)).second) bad = true;
-  }
-  if (!bad) {
-    // refcounts are the number of resident tables holding the block, a
-    // block is in the free queue exactly when nothing holds it, and every
-    // swap block is either in the swap pool's free queue or held by exactly
-    // one swapped-out table, exactly once (swap blocks are never shared)
-    std::vector<int64_t> holders(nb, 0);
-    std::vector<int64_t> cpu_holders(ncpu > 0 ? ncpu : 0, 0);
-    std::vector<uint8_t> cpu_free(ncpu > 0 ? ncpu : 0, 0);
-    for (int32_t b = a->cpu.head; ncpu > 0 && b >= 0; b = a->cpu.next[b]) cpu_free[b] = 1;
-    for (const auto& kv : a->seqs)
-      for (int32_t b : kv.second.blocks) {
-        if (kv.second.swapped) {
-          ++cpu_holders[b];
-        } else {
-          ++holders[b];
-        }
-      }
+    for (int32_t b = 0; !bad && b < nb; ++b) a->ref[b] = (int32_t)next(0, INT32_MAX);
+    for (int32_t b = 0; !bad && b < nb; ++b) a->has_hash[b] = (uint8_t)next(0, 1);
+    for (int32_t b = 0; !bad && b < nb; ++b) a->hash[b] = (uint64_t)raw();
     for (int32_t b = 0; !bad && b < nb; ++b)
-      if (holders[b] != a->ref[b] || (a->ref[b] == 0) != (a->in_free[b] != 0)) bad = true;
-    for (int32_t b = 0; !bad && b < ncpu; ++b)
-      if (cpu_holders[b] + cpu_free[b] != 1) bad = true;
-    // every hashed block is the cache's entry for its hash
-    int64_t hashed = 0;
-    for (int32_t b = 0; b < nb; ++b) hashed += a->has_hash[b];
-    if (hashed != (int64_t)a->cached.size()) bad = true;
-  }
-  if (bad || i != n) {
-    delete a;
-    return PA_ERR_INVALID;
-  }
-  *out = a;
-  return PA_OK;
+      if (a->in_free[b] && a->ref[b] != 0) bad = true;  // a free block has no owner
+    const int64_t ncached = next(0, nb);
+    for (int64_t k = 0; !bad && k < ncached; ++k) {
+      const uint64_t h = (uint64_t)raw();
+      const int32_t b = (int32_t)next(0, nb - 1);
+      if (!bad && (!a->has_hash[b] || a->hash[b] != h || !a->cached.emplace(h, b).second)) bad = true;
+    }
+    const int64_t ncpu_free = next(0, ncpu);
+    if (!bad && ncpu > 0) {
+      a->num_cpu_blocks = ncpu;
+      a->cpu.prev.assign(ncpu, -1);
+      a->cpu.next.assign(ncpu, -1);
+      std::vector<uint8_t> seen(ncpu, 0);
+      for (int64_t k = 0; !bad && k < ncpu_free; ++k) {
+        const int32_t b = (int32_t)next(0, ncpu - 1);
+        if (bad || seen[b]) {
+          bad = true;
+          break;
+        }
+        seen[b] = 1;
+        a->cpu.prev[b] = a->cpu.tail;  // append at the tail, in the exported order
+        if (a->cpu.tail < 0) a->cpu.head = b; else a->cpu.next[a->cpu.tail] = b;
+        a->cpu.tail = b;
+        ++a->cpu.n;
+      }
+    }
+    const int64_t nseq = next(0, n);
+    for (int64_t k = 0; !bad && k < nseq; ++k) {
+      const int id = (int)next(0, INT32_MAX);
+      Seq q;
+      q.num_tokens = next(0, INT64_MAX);
+      q.salt = (uint64_t)raw();
+      q.parent = (uint64_t)raw();
+      q.hashable = next(0, 1) != 0;
+      q.swapped = next(0, 1) != 0;
+      if (q.swapped && ncpu == 0) bad = true;
+      const int64_t nbk = next(0, n);
+      const int32_t lim = q.swapped ? ncpu : nb;
+      for (int64_t t = 0; !bad && t < nbk; ++t) q.blocks.push_back((int32_t)next(0, (int64_t)lim - 1));
+      if (!bad && (int64_t)q.blocks.size() * bs < q.num_tokens) bad = true;  // tokens beyond the blocks
+      const int64_t np = next(0, (int64_t)bs - 1);  // token ids of a block not yet full
+      for (int64_t t = 0; !bad && t < np; ++t) q.pending.push_back((int32_t)next(INT32_MIN, INT32_MAX));
+      if (!bad && !a->seqs.emplace(id, std::move(q)).second) bad = true;
+    }
+    if (!bad) {
+      // refcounts are the number of resident tables holding the block, a
+      // block is in the free queue exactly when nothing holds it, and every
+      // swap block is either in the swap pool's free queue or held by exactly
+      // one swapped-out table, exactly once (swap blocks are never shared)
+      std::vector<int64_t> holders(nb, 0);
+      std::vector<int64_t> cpu_holders(ncpu > 0 ? ncpu : 0, 0);
+      std::vector<uint8_t> cpu_free(ncpu > 0 ? ncpu : 0, 0);
+      for (int32_t b = a->cpu.head; ncpu > 0 && b >= 0; b = a->cpu.next[b]) cpu_free[b] = 1;
+      for (const auto& kv : a->seqs)
+        for (int32_t b : kv.second.blocks) {
+          if (kv.second.swapped) {
+            ++cpu_holders[b];
+          } else {
+            ++holders[b];
+          }
+        }
+      for (int32_t b = 0; !bad && b < nb; ++b)
+        if (holders[b] != a->ref[b] || (a->ref[b] == 0) != (a->in_free[b] != 0)) bad = true;
+      for (int32_t b = 0; !bad && b < ncpu; ++b)
+        if (cpu_holders[b] + cpu_free[b] != 1) bad = true;
+      // every hashed block is the cache's entry for its hash
+      int64_t hashed = 0;
+      for (int32_t b = 0; b < nb; ++b) hashed += a->has_hash[b];
+      if (hashed != (int64_t)a->cached.size()) bad = true;
+    }
+    if (bad || i != n) return PA_ERR_INVALID;
+    *out = a.release();
+    return PA_OK;
+  });
 }
 
 }  // extern "C"

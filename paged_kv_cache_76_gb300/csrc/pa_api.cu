@@ -284,6 +284,7 @@ const char* pa_status_string(int status) {
     case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
     case PA_ERR_SHARED_BLOCK: return "PA_ERR_SHARED_BLOCK";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_HOST_MEMORY: return "PA_ERR_HOST_MEMORY";
     default: return "PA_UNKNOWN_STATUS";
   }
 }

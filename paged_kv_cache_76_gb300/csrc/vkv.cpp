@@ -23,9 +23,11 @@
 #include <chrono>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <vector>
 
 #include "pa.h"
+#include "pa_guard.h"
 #include "pa_internal.h"
 
 namespace {
@@ -157,63 +159,59 @@ int pa_vkv_granularity(size_t* out) {
 
 int pa_vkv_create(int num_slots, int max_len, int num_layers, int kv_heads, int head_dim, pa_dtype dtype,
                   size_t page_bytes, int64_t max_pages, int flags, pa_vkv** out) {
-  if (!out) return PA_ERR_INVALID;
-  *out = nullptr;
-  if (dtype != PA_FP16 && dtype != PA_BF16) return PA_ERR_DTYPE;
-  if (num_slots <= 0 || max_len <= 0 || max_len % 16 != 0 || num_layers <= 0 || kv_heads <= 0 ||
-      (head_dim != 64 && head_dim != 128) || max_pages < 0 || (flags & ~PA_VKV_DRY_RUN))
-    return PA_ERR_INVALID;
-  const bool dry = (flags & PA_VKV_DRY_RUN) != 0;
-  if (page_bytes == 0) {
-    if (dry) return PA_ERR_INVALID;
-    int st = pa_vkv_granularity(&page_bytes);
-    if (st != PA_OK) return st;
-  }
-  const int64_t row = (int64_t)kv_heads * head_dim * 2;
-  const int64_t slot_bytes = (int64_t)max_len * row;
-  // slots must start on page boundaries, and row coordinates must fit TMA's int32
-  if (slot_bytes % (int64_t)page_bytes != 0) return PA_ERR_INVALID;
-  if ((int64_t)num_slots * max_len + 16 > INT32_MAX) return PA_ERR_INVALID;
-  pa_vkv* v = new pa_vkv;
-  v->B = num_slots;
-  v->L = max_len;
-  v->layers = num_layers;
-  v->kv_heads = kv_heads;
-  v->head_dim = head_dim;
-  v->dtype = dtype;
-  v->tensors = 2 * num_layers;
-  v->row = row;
-  v->G = (int64_t)page_bytes;
-  v->slot_pages = slot_bytes / v->G;
-  v->max_pages = max_pages;
-  v->dry = dry;
-  v->tensor_bytes = (int64_t)num_slots * slot_bytes;
-  v->mapped.assign(num_slots, 0);
-  v->active.assign(num_slots, 0);
-  v->held.assign(num_slots, 0);
-  v->h_slot_tokens.assign(num_slots, 0);
-  if (!dry) {
-    const Driver& d = driver();
-    if (!d.ok || cudaGetDevice(&v->device) != cudaSuccess) {
-      delete v;
-      return PA_ERR_CUDA;
+  return pa_guarded([&]() -> int {
+    if (!out) return PA_ERR_INVALID;
+    *out = nullptr;
+    if (dtype != PA_FP16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (num_slots <= 0 || max_len <= 0 || max_len % 16 != 0 || num_layers <= 0 || kv_heads <= 0 ||
+        (head_dim != 64 && head_dim != 128) || max_pages < 0 || (flags & ~PA_VKV_DRY_RUN))
+      return PA_ERR_INVALID;
+    const bool dry = (flags & PA_VKV_DRY_RUN) != 0;
+    if (page_bytes == 0) {
+      if (dry) return PA_ERR_INVALID;
+      int st = pa_vkv_granularity(&page_bytes);
+      if (st != PA_OK) return st;
     }
-    v->handles.assign((size_t)v->tensors * num_slots * v->slot_pages, 0);
-    if (d.reserve(&v->base, (size_t)(v->tensors * v->tensor_bytes), (size_t)v->G, 0, 0) != CUDA_SUCCESS) {
-      delete v;
-      return PA_ERR_CUDA;
+    const int64_t row = (int64_t)kv_heads * head_dim * 2;
+    const int64_t slot_bytes = (int64_t)max_len * row;
+    // slots must start on page boundaries, and row coordinates must fit TMA's int32
+    if (slot_bytes % (int64_t)page_bytes != 0) return PA_ERR_INVALID;
+    if ((int64_t)num_slots * max_len + 16 > INT32_MAX) return PA_ERR_INVALID;
+    std::unique_ptr<pa_vkv> v(new pa_vkv);
+    v->B = num_slots;
+    v->L = max_len;
+    v->layers = num_layers;
+    v->kv_heads = kv_heads;
+    v->head_dim = head_dim;
+    v->dtype = dtype;
+    v->tensors = 2 * num_layers;
+    v->row = row;
+    v->G = (int64_t)page_bytes;
+    v->slot_pages = slot_bytes / v->G;
+    v->max_pages = max_pages;
+    v->dry = dry;
+    v->tensor_bytes = (int64_t)num_slots * slot_bytes;
+    v->mapped.assign(num_slots, 0);
+    v->active.assign(num_slots, 0);
+    v->held.assign(num_slots, 0);
+    v->h_slot_tokens.assign(num_slots, 0);
+    if (!dry) {
+      const Driver& d = driver();
+      if (!d.ok || cudaGetDevice(&v->device) != cudaSuccess) return PA_ERR_CUDA;
+      v->handles.assign((size_t)v->tensors * num_slots * v->slot_pages, 0);  // host memory before any CUDA resource
+      if (d.reserve(&v->base, (size_t)(v->tensors * v->tensor_bytes), (size_t)v->G, 0, 0) != CUDA_SUCCESS)
+        return PA_ERR_CUDA;
+      if (cudaMalloc(&v->d_slot_tokens, sizeof(int32_t) * num_slots) != cudaSuccess ||
+          cudaMemset(v->d_slot_tokens, 0, sizeof(int32_t) * num_slots) != cudaSuccess) {
+        cudaGetLastError();
+        d.addr_free(v->base, (size_t)(v->tensors * v->tensor_bytes));
+        if (v->d_slot_tokens) cudaFree(v->d_slot_tokens);
+        return PA_ERR_CUDA;
+      }
     }
-    if (cudaMalloc(&v->d_slot_tokens, sizeof(int32_t) * num_slots) != cudaSuccess ||
-        cudaMemset(v->d_slot_tokens, 0, sizeof(int32_t) * num_slots) != cudaSuccess) {
-      cudaGetLastError();
-      d.addr_free(v->base, (size_t)(v->tensors * v->tensor_bytes));
-      if (v->d_slot_tokens) cudaFree(v->d_slot_tokens);
-      delete v;
-      return PA_ERR_CUDA;
-    }
-  }
-  *out = v;
-  return PA_OK;
+    *out = v.release();
+    return PA_OK;
+  });
 }
 
 void pa_vkv_destroy(pa_vkv* v) {
@@ -248,105 +246,108 @@ int pa_vkv_free_slot(pa_vkv* v, int slot) {
 }
 
 int pa_vkv_step(pa_vkv* v, const int32_t* lens, pa_stream stream) {
-  if (!v || !lens) return PA_ERR_INVALID;
-  std::vector<int64_t> need(v->B);
-  int64_t extra = 0;
-  for (int s = 0; s < v->B; ++s) {
-    const int32_t n = lens[s];
-    if (n < 0 || n > v->L || (n > 0 && !v->active[s])) return PA_ERR_INVALID;
-    need[s] = v->pages_for(n);
-    if (need[s] > v->mapped[s]) extra += (need[s] - v->mapped[s]) * v->tensors;
-  }
-  int64_t short_by = extra - (v->max_pages - v->in_use());
-  if (short_by > 0) {
-    int64_t reclaimable = 0;
-    for (int s = 0; s < v->B; ++s)
-      if (!v->active[s]) reclaimable += (int64_t)v->mapped[s] * v->tensors;
-    if (reclaimable < short_by) {
-      ++v->step_failures;
-      return PA_ERR_NO_FREE_BLOCKS;
+  return pa_guarded([&]() -> int {
+    if (!v || !lens) return PA_ERR_INVALID;
+    std::vector<int64_t> need(v->B);
+    int64_t extra = 0;
+    for (int s = 0; s < v->B; ++s) {
+      const int32_t n = lens[s];
+      if (n < 0 || n > v->L || (n > 0 && !v->active[s])) return PA_ERR_INVALID;
+      need[s] = v->pages_for(n);
+      if (need[s] > v->mapped[s]) extra += (need[s] - v->mapped[s]) * v->tensors;
     }
-    std::vector<int> donors;
-    for (int s = 0; s < v->B && short_by > 0; ++s) {
-      if (v->active[s] || v->mapped[s] == 0) continue;
-      short_by -= (int64_t)v->mapped[s] * v->tensors;
-      donors.push_back(s);
-    }
-    if (!v->dry) {
-      // every kernel launched so far has finished; the device copy of the
-      // bounds drops to zero for the donors (a blocking copy) before their
-      // pages go, so no later kernel can reach an unmapped row
-      if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
-      for (int s : donors) v->h_slot_tokens[s] = 0;
-      if (cudaMemcpy(v->d_slot_tokens, v->h_slot_tokens.data(), sizeof(int32_t) * v->B, cudaMemcpyHostToDevice) !=
-          cudaSuccess)
-        return PA_ERR_CUDA;
-    }
-    for (int s : donors) {
-      const int st = unmap_slot(v, s);
-      if (st != PA_OK) return st;
-    }
-  }
-  const auto t0 = std::chrono::steady_clock::now();
-  if (!v->dry && extra > 0) {
-    const Driver& d = driver();
-    // take every page first (pool, then new handles) so that a failed
-    // creation leaves the mappings as they were
-    std::vector<CUmemGenericAllocationHandle> got;
-    got.reserve((size_t)extra);
-    CUmemAllocationProp prop = page_prop(v->device);
-    while ((int64_t)got.size() < extra) {
-      if (!v->pool.empty()) {
-        got.push_back(v->pool.back());
-        v->pool.pop_back();
-        continue;
-      }
-      CUmemGenericAllocationHandle h = 0;
-      if (d.create(&h, (size_t)v->G, &prop, 0) != CUDA_SUCCESS) {
-        for (auto x : got) v->pool.push_back(x);
+    int64_t short_by = extra - (v->max_pages - v->in_use());
+    if (short_by > 0) {
+      int64_t reclaimable = 0;
+      for (int s = 0; s < v->B; ++s)
+        if (!v->active[s]) reclaimable += (int64_t)v->mapped[s] * v->tensors;
+      if (reclaimable < short_by) {
         ++v->step_failures;
         return PA_ERR_NO_FREE_BLOCKS;
       }
-      ++v->created;
-      got.push_back(h);
+      std::vector<int> donors;
+      for (int s = 0; s < v->B && short_by > 0; ++s) {
+        if (v->active[s] || v->mapped[s] == 0) continue;
+        short_by -= (int64_t)v->mapped[s] * v->tensors;
+        donors.push_back(s);
+      }
+      if (!v->dry) {
+        // every kernel launched so far has finished; the device copy of the
+        // bounds drops to zero for the donors (a blocking copy) before their
+        // pages go, so no later kernel can reach an unmapped row
+        if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+        for (int s : donors) v->h_slot_tokens[s] = 0;
+        if (cudaMemcpy(v->d_slot_tokens, v->h_slot_tokens.data(), sizeof(int32_t) * v->B, cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+          return PA_ERR_CUDA;
+      }
+      for (int s : donors) {
+        const int st = unmap_slot(v, s);
+        if (st != PA_OK) return st;
+      }
     }
-    CUmemAccessDesc acc;
-    std::memset(&acc, 0, sizeof(acc));
-    acc.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
-    acc.location.id = v->device;
-    acc.flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
-    size_t gi = 0;
-    for (int s = 0; s < v->B; ++s)
-      for (int64_t k = v->mapped[s]; k < need[s]; ++k)
-        for (int t = 0; t < v->tensors; ++t) {
-          const CUdeviceptr a = v->page_addr(t, s, k);
-          const CUmemGenericAllocationHandle h = got[gi++];
-          if (d.map(a, (size_t)v->G, 0, h, 0) != CUDA_SUCCESS ||
-              d.set_access(a, (size_t)v->G, &acc, 1) != CUDA_SUCCESS)
-            return PA_ERR_CUDA;
-          v->handles[((int64_t)t * v->B + s) * v->slot_pages + k] = h;
+    const auto t0 = std::chrono::steady_clock::now();
+    if (!v->dry && extra > 0) {
+      const Driver& d = driver();
+      // take every page first (pool, then new handles) so that a failed
+      // creation leaves the mappings as they were
+      std::vector<CUmemGenericAllocationHandle> got;
+      got.reserve((size_t)extra);
+      v->pool.reserve(v->pool.size() + (size_t)extra);  // the pages go back there if a creation fails
+      CUmemAllocationProp prop = page_prop(v->device);
+      while ((int64_t)got.size() < extra) {
+        if (!v->pool.empty()) {
+          got.push_back(v->pool.back());
+          v->pool.pop_back();
+          continue;
         }
-  }
-  for (int s = 0; s < v->B; ++s)
-    if (need[s] > v->mapped[s]) {
-      v->map_calls += (need[s] - v->mapped[s]) * v->tensors;
-      v->mapped[s] = (int)need[s];
+        CUmemGenericAllocationHandle h = 0;
+        if (d.create(&h, (size_t)v->G, &prop, 0) != CUDA_SUCCESS) {
+          for (auto x : got) v->pool.push_back(x);
+          ++v->step_failures;
+          return PA_ERR_NO_FREE_BLOCKS;
+        }
+        ++v->created;
+        got.push_back(h);
+      }
+      CUmemAccessDesc acc;
+      std::memset(&acc, 0, sizeof(acc));
+      acc.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+      acc.location.id = v->device;
+      acc.flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+      size_t gi = 0;
+      for (int s = 0; s < v->B; ++s)
+        for (int64_t k = v->mapped[s]; k < need[s]; ++k)
+          for (int t = 0; t < v->tensors; ++t) {
+            const CUdeviceptr a = v->page_addr(t, s, k);
+            const CUmemGenericAllocationHandle h = got[gi++];
+            if (d.map(a, (size_t)v->G, 0, h, 0) != CUDA_SUCCESS ||
+                d.set_access(a, (size_t)v->G, &acc, 1) != CUDA_SUCCESS)
+              return PA_ERR_CUDA;
+            v->handles[((int64_t)t * v->B + s) * v->slot_pages + k] = h;
+          }
     }
-  v->last_map_ns =
-      std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now() - t0).count();
-  for (int s = 0; s < v->B; ++s) v->held[s] = lens[s];  // nonzero only on active slots (checked above)
-  v->total_map_ns += v->last_map_ns;
-  bool changed = false;
-  for (int s = 0; s < v->B; ++s) {
-    const int32_t t = v->slot_tokens(s);
-    changed |= t != v->h_slot_tokens[s];
-    v->h_slot_tokens[s] = t;
-  }
-  if (!v->dry && changed &&
-      cudaMemcpyAsync(v->d_slot_tokens, v->h_slot_tokens.data(), sizeof(int32_t) * v->B, cudaMemcpyHostToDevice,
-                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PA_ERR_CUDA;
-  return PA_OK;
+    for (int s = 0; s < v->B; ++s)
+      if (need[s] > v->mapped[s]) {
+        v->map_calls += (need[s] - v->mapped[s]) * v->tensors;
+        v->mapped[s] = (int)need[s];
+      }
+    v->last_map_ns =
+        std::chrono::duration_cast<std::chrono::nanoseconds>(std::chrono::steady_clock::now() - t0).count();
+    for (int s = 0; s < v->B; ++s) v->held[s] = lens[s];  // nonzero only on active slots (checked above)
+    v->total_map_ns += v->last_map_ns;
+    bool changed = false;
+    for (int s = 0; s < v->B; ++s) {
+      const int32_t t = v->slot_tokens(s);
+      changed |= t != v->h_slot_tokens[s];
+      v->h_slot_tokens[s] = t;
+    }
+    if (!v->dry && changed &&
+        cudaMemcpyAsync(v->d_slot_tokens, v->h_slot_tokens.data(), sizeof(int32_t) * v->B, cudaMemcpyHostToDevice,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return PA_ERR_CUDA;
+    return PA_OK;
+  });
 }
 
 int pa_vkv_tensor(const pa_vkv* v, int layer, int is_v, void** out) {

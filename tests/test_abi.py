@@ -40,6 +40,9 @@ def test_binding_prototypes_cover_the_header():
 def test_host_only_calls(lib):
     assert lib.pa_version() >= 100
     assert lib.pa_status_string(-2) == b"PA_ERR_NO_FREE_BLOCKS"
+    assert lib.pa_status_string(-8) == b"PA_ERR_HOST_MEMORY"
+    with pytest.raises(MemoryError):                      # the binding raises it as a MemoryError
+        _lib.check(_lib.PA_ERR_HOST_MEMORY, "probe")
     assert lib.pa_decode_split_tokens(256, 16, 0) == 384          # auto, contexts up to 8K
     assert lib.pa_decode_split_tokens(1024, 16, 0) == 512         # auto, longer contexts
     assert lib.pa_decode_split_tokens(256, 16, 24) == _lib.PA_ERR_INVALID      # not a multiple of 16

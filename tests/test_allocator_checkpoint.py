@@ -137,6 +137,10 @@ def test_malformed_words_are_refused():
     x = w.copy(); x[12] = 12; bad.append(x)    # a block id past the pool
     nfree = int(w[11])
     x = w.copy(); x[12 + nfree] += 1; bad.append(x)  # a refcount that no table accounts for
+    # a swap pool larger than the words could describe: refused before the
+    # pool's bookkeeping is sized (a 2^31-block pool would be gigabytes)
+    x = w.copy(); x[5] = 2**31 - 1; bad.append(x)
+    x = w.copy(); x[5] = len(w) + 1; bad.append(x)
     for v in bad:
         with pytest.raises(_lib.PAError):
             BlockAllocator.from_words(v)
