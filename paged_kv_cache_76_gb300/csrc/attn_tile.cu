@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const CUtensorMap* map = isv ? &vmap : &kmap;
     const int full0 = isv ? B_VFULL : B_KFULL, empty0 = isv ? B_VEMPTY : B_KEMPTY;
     const uint32_t base = smem_u32(smem + (isv ? L::V_OFF : L::K_OFF));
-    const uint64_t pol = policy_evict_last();  // K/V tiles are re-read by the other row tiles
+    const uint64_t pol = policy_evict_first();  // a unit's K/V is read once: streamed
     const int nst = isv ? kVStages : kKStages;
     int gt = 0;  // K/V tiles issued by this CTA (ring position and phase)
     bool failed = false;
