@@ -29,10 +29,24 @@
 //               P = 2^(s*scale*log2e - m) for its 64 keys into TMEM, and sums
 //               them.  The running maximum m is raised only when a row
 //               maximum exceeds it by more than 2^8 (O is then rescaled in
-//               TMEM); the final O / sum uses the same m, so this is exact.
+//               TMEM, all D columns by the warp of the low key half, before
+//               either half of the tile's P.V, each of which adds to every
+//               column, can start); the final O / sum uses the same m, so
+//               this is exact.
 //               A warp whose 32 rows are all past the unit's rows skips the
 //               arithmetic and only keeps the barrier phases.  The next
 //               unit's Q rows are staged in shared memory by cp.async.
+//   (spread)    units of at most 32 rows (a verify of k+1 <= 32 / group
+//               queries): every lane quarter holds a copy of the same rows
+//               (Q is written four times; S costs the MMA the same), and
+//               quarter q takes keys [32q, +32) of every tile: each thread
+//               loads 32 scores instead of 128 and computes 16
+//               probabilities instead of 64.  P stays zero outside the
+//               quarter's window, so O of quarter q sums its keys only, with
+//               its own running maximum; the epilogue merges the four
+//               partial results (O = sum 2^(m_q - M) O_q / sum 2^(m_q - M)
+//               l_q) through shared memory.  The first half of P.V then
+//               takes the low 16 keys of every window.
 //   warp 8      issues S(j) = Q K_j^T into S(j % 2) (A from TMEM); owns TMEM
 //   warp 9      issues O += P(j) V_j (A from TMEM), in two 64-key halves
 //   warps 10,11 TMA producers of K (3-stage ring) and V (3 stages)
@@ -66,14 +80,16 @@ __device__ __forceinline__ uint8_t* align1024_tc(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int D, int BSUB>
+template <int D, int BSUB, bool SPREAD>
 struct TcSmem {
   using Tile = KvTile<D, BSUB, kKeys>;  // D/64 halves x 128 rows x 128 B
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + kKStages * Tile::BYTES;
-  static constexpr int Q_OFF = V_OFF + kVStages * Tile::BYTES;  // staged Q rows of the next unit
-  static constexpr int L_OFF = Q_OFF + kRows * D * 2;           // [2 key halves][128] row sums
-  static constexpr int BAR_OFF = L_OFF + 2 * kRows * 4;
+  // staged Q rows of the next unit; spread: two [32 rows][D] fp32 partial outputs
+  static constexpr int Q_OFF = V_OFF + kVStages * Tile::BYTES;
+  // row sums: [2 key halves][128 rows]; spread: maxima [4][32] and sums [4][2][32]
+  static constexpr int L_OFF = Q_OFF + kRows * D * 2;
+  static constexpr int BAR_OFF = L_OFF + (SPREAD ? 3 : 2) * kRows * 4;
   static constexpr int NBARS = 4 * 3 + 2 + 2 + 6;
   static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = SLOT_OFF + 16 + 1024;
@@ -89,8 +105,8 @@ constexpr int B_VFULL = B_KEMPTY + kKStages;  // [kVStages] V producer arrival (
 constexpr int B_VEMPTY = B_VFULL + kVStages;  // [kVStages] commit after P.V(j)
 constexpr int B_SFULL = B_VEMPTY + kVStages;  // [2] S buffer written (commit)
 constexpr int B_SFREE = B_SFULL + 2;          // [2] S buffer read out (8 softmax warps)
-constexpr int B_PLO = B_SFREE + 2;            // P keys 0..63 in TMEM (4 warps; V rows past the keys zeroed)
-constexpr int B_PHI = B_PLO + 1;              // P keys 64..127 (4 warps)
+constexpr int B_PLO = B_SFREE + 2;            // low key half of P in TMEM (4 warps; V rows past the keys zeroed, O rescaled)
+constexpr int B_PHI = B_PLO + 1;              // high key half of P (4 warps)
 constexpr int B_PVDONE = B_PHI + 1;           // P.V(j) complete (commit)
 constexpr int B_QFULL = B_PVDONE + 1;         // the unit's Q in TMEM (8 warps)
 constexpr int B_OFREE = B_QFULL + 1;          // the unit's O read out (8 warps)
@@ -133,11 +149,11 @@ __device__ __forceinline__ bool tc_unit(const PrefillParams& p, int u, int row_t
   return true;
 }
 
-template <int D, int BSUB, typename T>
+template <int D, int BSUB, typename T, bool SPREAD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const PrefillParams p) {
-  using L = TcSmem<D, BSUB>;
+  using L = TcSmem<D, BSUB, SPREAD>;
   using Tile = typename L::Tile;
   constexpr int NH = D / 64;
   constexpr int KSTEPS = D / 16;      // S = Q K^T: K dimension = head_dim
@@ -316,8 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-              // A = P[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
-              const int kk = hh * 4 + k4;
+              // A = P[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major.
+              // Half hh: keys 64hh.. (spread: the 16-key steps of key half hh of every window)
+              const int kk = SPREAD ? 2 * k4 + hh : hh * 4 + k4;
               const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
               tc_mma_f16_ts_warp(tmem + O_COL, tmem + P_COL + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
             }
@@ -332,38 +349,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kSoftmaxWarps) {
     // ---------------------------------------------------------------- softmax
-    const int quarter = warp & 3;           // TMEM lane quarter this warp may access
-    const int kh = warp >> 2;               // key half of P, dim half of O and Q
-    const int row = quarter * 32 + lane;    // row within the unit == TMEM lane
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int kh = warp >> 2;      // key half of P (of the quarter's window when spread), dim half of O and Q
+    // the unit row this thread owns: its TMEM lane, or (spread) the same 32
+    // rows in every lane quarter
+    const int row = SPREAD ? lane : quarter * 32 + lane;
+    const int vrow = quarter * 32 + lane;  // V row this thread zeroes past the keys
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     constexpr float kRescale = 8.f;
-    const uint32_t qst = smem_u32(smem + L::Q_OFF) + row * (D * 2);  // this row's staged Q
+    // S columns the warp reads: the whole tile, or (spread) its quarter's 32-key window
+    constexpr int KS = SPREAD ? 32 : kKeys;
+    const int s_key0 = SPREAD ? 32 * quarter : 0;
+    // keys of P the warp writes, two per TMEM column
+    constexpr int KP = SPREAD ? 16 : kKeys / 2;
+    const int p_key0 = SPREAD ? 32 * quarter + 16 * kh : 64 * kh;
+    const uint32_t qst = smem_u32(smem + L::Q_OFF) + row * (D * 2);  // this row's staged Q (not spread)
     float* lsum = reinterpret_cast<float*>(smem + L::L_OFF);
+    uint4 qreg[SPREAD ? DH / 8 : 1];  // spread: this thread's half of its Q row for the next unit
 
-    // this thread's half of its Q row for unit w -> shared memory (16-byte
-    // chunks, XOR-swizzled by row); rows past the unit are zero
+    // this thread's half of its Q row for unit w: into registers (spread), or
+    // into shared memory by cp.async (16-byte chunks, XOR-swizzled by row);
+    // rows past the unit are zero
     auto stage_q = [&](const TcUnit& w) {
       const int grow = w.row0 + row;
       const bool valid = grow < w.rows;
       const int qi = grow / G, g = grow % G;
       const char* src = reinterpret_cast<const char*>(p.q) +
                         (valid ? ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D * sizeof(T) : 0);
+      if constexpr (SPREAD) {
 #pragma unroll
-      for (int c = kh * (D / 16); c < (kh + 1) * (D / 16); ++c)
-        cp_async16(qst + ((c ^ (row & 7)) << 4), src + c * 16, valid ? 16u : 0u);
-      cp_async_commit();
+        for (int c = 0; c < DH / 8; ++c)
+          qreg[c] = valid ? __ldg(reinterpret_cast<const uint4*>(src) + kh * (DH / 8) + c) : make_uint4(0, 0, 0, 0);
+      } else {
+#pragma unroll
+        for (int c = kh * (D / 16); c < (kh + 1) * (D / 16); ++c)
+          cp_async16(qst + ((c ^ (row & 7)) << 4), src + c * 16, valid ? 16u : 0u);
+        cp_async_commit();
+      }
     };
     // the staged half row -> Q columns of TMEM (two elements per column)
     auto q_to_tmem = [&]() {
-      cp_async_wait_all();
+      if constexpr (!SPREAD) cp_async_wait_all();
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t v[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int c = kh * (D / 16) + cc * 4 + i;
-          const uint4 x = *reinterpret_cast<const uint4*>(smem + L::Q_OFF + row * (D * 2) + ((c ^ (row & 7)) << 4));
+          uint4 x;
+          if constexpr (SPREAD) {
+            x = qreg[cc * 4 + i];
+          } else {
+            const int c = kh * (D / 16) + cc * 4 + i;
+            x = *reinterpret_cast<const uint4*>(smem + L::Q_OFF + row * (D * 2) + ((c ^ (row & 7)) << 4));
+          }
           v[4 * i] = x.x, v[4 * i + 1] = x.y, v[4 * i + 2] = x.z, v[4 * i + 3] = x.w;
         }
         tmem_st16u(tl + Q_COL + kh * (D / 4) + cc * 16, v);
@@ -374,15 +413,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_QFULL));
     };
 
+    if constexpr (SPREAD) {
+      // P columns of the other quarters' windows stay zero in this lane
+      // quarter for the whole kernel.  Column c holds keys of window c / 16
+      // and key half (c / 8) % 2: exactly one warp ever writes it.
+      const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        if (qq != quarter) tmem_st8u(tl + P_COL + 16 * qq + 8 * kh, zero8);
+      tmem_wait_st();  // fenced before this warp's first arrival on a P barrier
+    }
+
     // units whose rows see no key at all (a verify request shorter than its
     // queries) are skipped by every role; their rows are written as zeros here
+    // (spread: by the first lane quarter)
     {
       TcUnit z;
       for (int uz = cta0; uz < nunits; uz += nctas) {
         if (!tc_unit(p, uz, row_tiles, z) || z.ntiles > 0 || z.row0 >= z.rows) continue;
         griddep_wait();
         const int grow = z.row0 + row;
-        if (grow < z.rows) {
+        if (grow < z.rows && (!SPREAD || quarter == 0)) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
                                                 ((size_t)(z.qs + grow / G) * p.q_heads + z.h * G + grow % G) * D + kh * DH);
 #pragma unroll
@@ -416,14 +467,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const int ts = w.k0 + j * kKeys;
-        const int nvis = lim - ts + 1;  // keys of this tile the row may see (<= 0: none)
+        const int nvis = lim - ts + 1 - s_key0;  // keys of this warp's S window the row may see (<= 0: none)
         // rows past the unit (whose output is never read) do not force the masking pass
-        const bool all_full = __all_sync(kAll, nvis >= kKeys || !valid);
+        const bool all_full = __all_sync(kAll, nvis >= KS || !valid);
 
-        // the whole S row in registers (one TMEM round trip); then the buffer
-        // may take S(gt + 2)
-        auto max64 = [](const float* x) {
+        // the warp's S window in registers (one TMEM round trip); then the
+        // buffer may take S(gt + 2)
+        auto max32 = [](const float* x) {
           float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;  // four chains of 3-input max
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            ma = fmax3(ma, x[e], x[e + 1]);
+            mb = fmax3(mb, x[e + 2], x[e + 3]);
+            mc = fmax3(mc, x[e + 4], x[e + 5]);
+            md = fmax3(md, x[e + 6], x[e + 7]);
+          }
+          return fmax3(ma, mb, fmaxf(mc, md));
+        };
+        auto max64 = [](const float* x) {
+          float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
 #pragma unroll
           for (int e = 0; e < 64; e += 8) {
             ma = fmax3(ma, x[e], x[e + 1]);
@@ -433,10 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return fmax3(ma, mb, fmaxf(mc, md));
         };
-        float sv[kKeys];
+        float sv[KS];
 #pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c)
-          tmem_ld32(tl + S_COL + b * kKeys + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
+        for (int c = 0; c < KS / 32; ++c)
+          tmem_ld32(tl + S_COL + b * kKeys + s_key0 + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -450,13 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = gt % kVStages;
             ok = __all_sync(kAll, mbar_wait(bar(B_VFULL + s), (gt / kVStages) & 1));
             if (!ok) break;
-            if (row >= nvalid) {
+            if (vrow >= nvalid) {
               uint8_t* vt = smem + L::V_OFF + s * Tile::BYTES;
 #pragma unroll
               for (int hf = 0; hf < NH; ++hf)
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                  *reinterpret_cast<uint4*>(vt + Tile::line(hf, row) + c * 16) = make_uint4(0, 0, 0, 0);
+                  *reinterpret_cast<uint4*>(vt + Tile::line(hf, vrow) + c * 16) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
           }
@@ -474,9 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (!all_full) {
 #pragma unroll
-          for (int e = 0; e < kKeys; ++e) sv[e] = e < nvis ? sv[e] : -INFINITY;
+          for (int e = 0; e < KS; ++e) sv[e] = e < nvis ? sv[e] : -INFINITY;
         }
-        const float mx = fmaxf(max64(sv), max64(sv + 64)) * sl2;
+        float mraw;
+        if constexpr (SPREAD) mraw = max32(sv);
+        else mraw = fmaxf(max64(sv), max64(sv + 64));
+        const float mx = mraw * sl2;
         const bool raise = mx > m + kRescale;  // also the first finite max (m = -inf)
         // O and l are rescaled by 2^(m_old - m_new) when the maximum is raised
         const float alpha = (raise && m != -INFINITY) ? ex2_approx(m - mx) : 1.f;
@@ -487,21 +552,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float neg_m = m == -INFINITY ? 0.f : -m;
 
-        // P = 2^(s*sl2 - m) for this warp's 64 keys (masked keys hold -inf:
+        // P = 2^(s*sl2 - m) for this warp's keys (masked keys hold -inf:
         // p = 0); the sum runs in four packed-pair chains
         float sx[4] = {0.f, 0.f, 0.f, 0.f}, sy[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk0[16], pk1[16];
+        uint32_t pk[KP / 2];
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
+        for (int e = 0; e < KP; e += 2) {
           float a0, a1;
           // selects with constant indices (a runtime index would put sv in local memory)
-          const float s0 = kh ? sv[64 + e] : sv[e], s1 = kh ? sv[65 + e] : sv[e + 1];
+          const float s0 = kh ? sv[KP + e] : sv[e], s1 = kh ? sv[KP + e + 1] : sv[e + 1];
           ffma2(a0, a1, s0, s1, sl2, sl2, neg_m, neg_m);
           const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
           const int k = (e >> 1) & 3;
           fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
-          if (e < 32) pk0[e >> 1] = Elem<T>::pack(p0v, p1v);
-          else pk1[(e - 32) >> 1] = Elem<T>::pack(p0v, p1v);
+          pk[e >> 1] = Elem<T>::pack(p0v, p1v);
         }
         // P(gt) overwrites P(gt - 1) and a rescale touches O: both once
         // P.V(gt - 1) has completed
@@ -510,15 +574,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
         }
-        if (rescale) {
+        if (kh == 0 && rescale) {
+          // all of the row's O, by the warp whose half of P the first half
+          // of P.V(gt) waits for: each half of P.V adds to every column of O
 #pragma unroll
-          for (int c = 0; c < DH / 16; ++c) {
+          for (int c = 0; c < D / 16; ++c) {
             float ov[16];
-            tmem_ld16(tl + O_COL + kh * DH + 16 * c, ov);
+            tmem_ld16(tl + O_COL + 16 * c, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) ov[e] *= alpha;
-            tmem_st16u(tl + O_COL + kh * DH + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(ov));
+            tmem_st16u(tl + O_COL + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(ov));
           }
         }
         if (kh == 0 && nvalid < kKeys) {
@@ -527,56 +593,145 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = gt % kVStages;
           ok = __all_sync(kAll, mbar_wait(bar(B_VFULL + s), (gt / kVStages) & 1));
           if (!ok) break;
-          if (row >= nvalid) {
+          if (vrow >= nvalid) {
             uint8_t* vt = smem + L::V_OFF + s * Tile::BYTES;
 #pragma unroll
             for (int hf = 0; hf < NH; ++hf)
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(vt + Tile::line(hf, row) + c * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(vt + Tile::line(hf, vrow) + c * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
-        tmem_st16u(tl + P_COL + kh * 32, pk0);
-        tmem_st16u(tl + P_COL + kh * 32 + 16, pk1);
+        if constexpr (SPREAD) {
+          tmem_st8u(tl + P_COL + p_key0 / 2, pk);
+        } else {
+          tmem_st16u(tl + P_COL + p_key0 / 2, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+          tmem_st16u(tl + P_COL + p_key0 / 2 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kh ? B_PHI : B_PLO));
         l += ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
       }
-      // epilogue: the unit's last P.V has completed.  The row's sum over both
-      // key halves is added in key-half order; the two warps of this lane
-      // quarter meet twice (written, then read).  The first meeting is an AND
-      // vote that every exit of the unit passes through, so that a warp that
-      // gave up on a wait never leaves its partner at a barrier.
+      // epilogue: the unit's last P.V has completed
       if (ok) ok = __all_sync(kAll, mbar_wait(bar(B_PVDONE), (gt - 1) & 1));
-      lsum[kh * kRows + row] = l;
-      if (!bar_red_and(1 + quarter, 64, ok)) {
-        ok = false;
-        break;
-      }
       tc_fence_after();
-      const float lt = lsum[row] + lsum[kRows + row];
-      asm volatile("bar.sync %0, %1;\n" ::"r"(1 + quarter), "r"(64) : "memory");
-      if (!wvalid) {
-        // nothing of this warp's rows is written
+      if constexpr (SPREAD) {
+        // The four lane quarters hold partial results of the same rows over
+        // disjoint keys, each relative to its own running maximum m_q:
+        //   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q,  M = max_q m_q.
+        // Quarters 1 and 3 put O_q into shared memory (the Q staging area,
+        // unused when spread), quarter 2 adds its scaled O_2 to quarter 3's,
+        // and quarter 0 adds the rest and writes the rows.  All 8 warps meet
+        // first in an AND vote that every exit of the unit passes through.
+        float* mq = lsum;           // [4 quarters][32 rows] running maxima
+        float* lq = lsum + 4 * 32;  // [4 quarters][2 key halves][32 rows] sums
+        if (kh == 0) mq[quarter * 32 + lane] = m;
+        lq[(quarter * 2 + kh) * 32 + lane] = l;
+        // 16-byte chunk c of this thread's half row in partial buffer pb, XOR-swizzled by row
+        auto part = [&](int pb, int c) {
+          return reinterpret_cast<float4*>(smem + L::Q_OFF + pb * (32 * D * 4) + lane * (D * 4)) +
+                 ((kh * (DH / 4) + c) ^ (lane & 7));
+        };
+        if (ok && (quarter & 1)) {
+#pragma unroll
+          for (int c = 0; c < DH / 32; ++c) {
+            float ov[32];
+            tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *part(quarter >> 1, 8 * c + i) = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+          }
+        }
+        if (!bar_red_and(5, 32 * kSoftmaxWarps, ok)) {
+          ok = false;
+          break;
+        }
+        float f[4], mmax = -INFINITY, lt = 0.f;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) mmax = fmaxf(mmax, mq[qq * 32 + lane]);
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const float mv = mq[qq * 32 + lane];
+          f[qq] = mv == -INFINITY ? 0.f : ex2_approx(mv - mmax);
+          lt += f[qq] * (lq[(qq * 2) * 32 + lane] + lq[(qq * 2 + 1) * 32 + lane]);
+        }
+        if (quarter == 2) {
+#pragma unroll
+          for (int c = 0; c < DH / 32; ++c) {
+            float ov[32];
+            tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4* a = part(1, 8 * c + i);
+              const float4 x = *a;
+              *a = make_float4(f[2] * ov[4 * i] + f[3] * x.x, f[2] * ov[4 * i + 1] + f[3] * x.y,
+                               f[2] * ov[4 * i + 2] + f[3] * x.z, f[2] * ov[4 * i + 3] + f[3] * x.w);
+            }
+          }
+        }
+        if ((quarter & 1) == 0) asm volatile("bar.sync %0, %1;\n" ::"r"(6), "r"(128) : "memory");
+        if (quarter == 0 && wvalid) {
+          const float inv = lt > 0.f ? 1.f / lt : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
+                                                ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D + kh * DH);
+#pragma unroll
+          for (int c = 0; c < DH / 32; ++c) {
+            float ov[32];
+            tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);  // warp-collective: every lane loads, valid rows store
+            tmem_wait_ld();
+            if (valid) {
+              float o[32];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 x1 = *part(0, 8 * c + i), x3 = *part(1, 8 * c + i);
+                o[4 * i] = (f[0] * ov[4 * i] + f[1] * x1.x + x3.x) * inv;
+                o[4 * i + 1] = (f[0] * ov[4 * i + 1] + f[1] * x1.y + x3.y) * inv;
+                o[4 * i + 2] = (f[0] * ov[4 * i + 2] + f[1] * x1.z + x3.z) * inv;
+                o[4 * i + 3] = (f[0] * ov[4 * i + 3] + f[1] * x1.w + x3.w) * inv;
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[4 * c + q] = make_uint4(Elem<T>::pack(o[8 * q], o[8 * q + 1]), Elem<T>::pack(o[8 * q + 2], o[8 * q + 3]),
+                                            Elem<T>::pack(o[8 * q + 4], o[8 * q + 5]),
+                                            Elem<T>::pack(o[8 * q + 6], o[8 * q + 7]));
+            }
+          }
+        }
       } else {
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
-                                              ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D + kh * DH);
+        // the row's sum over both key halves is added in key-half order; the
+        // two warps of this lane quarter meet twice (written, then read).  The
+        // first meeting is an AND vote that every exit of the unit passes
+        // through, so that a warp that gave up on a wait never leaves its
+        // partner at a barrier.
+        lsum[kh * kRows + row] = l;
+        if (!bar_red_and(1 + quarter, 64, ok)) {
+          ok = false;
+          break;
+        }
+        const float lt = lsum[row] + lsum[kRows + row];
+        asm volatile("bar.sync %0, %1;\n" ::"r"(1 + quarter), "r"(64) : "memory");
+        if (wvalid) {
+          const float inv = lt > 0.f ? 1.f / lt : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
+                                                ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D + kh * DH);
 #pragma unroll
-        for (int c = 0; c < DH / 32; ++c) {
-          float ov[32];
-          tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);  // warp-collective: every lane loads, valid rows store
-          tmem_wait_ld();
-          if (valid) {
+          for (int c = 0; c < DH / 32; ++c) {
+            float ov[32];
+            tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);  // warp-collective: every lane loads, valid rows store
+            tmem_wait_ld();
+            if (valid) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[4 * c + q] = make_uint4(Elem<T>::pack(ov[8 * q] * inv, ov[8 * q + 1] * inv),
-                                          Elem<T>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
-                                          Elem<T>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
-                                          Elem<T>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+              for (int q = 0; q < 4; ++q)
+                dst[4 * c + q] = make_uint4(Elem<T>::pack(ov[8 * q] * inv, ov[8 * q + 1] * inv),
+                                            Elem<T>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
+                                            Elem<T>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
+                                            Elem<T>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+            }
           }
         }
       }
@@ -591,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
-    cp_async_wait_all();  // no staging copy still in flight at exit
+    if constexpr (!SPREAD) cp_async_wait_all();  // no staging copy still in flight at exit
   }
 
   // ------------------------------------------------------------------ teardown
@@ -604,11 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BSUB, typename T>
+template <int D, int BSUB, typename T, bool SPREAD>
 cudaError_t launch_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p,
                          cudaStream_t stream) {
-  using L = TcSmem<D, BSUB>;
-  auto kern = attn_tile_kernel<D, BSUB, T>;
+  using L = TcSmem<D, BSUB, SPREAD>;
+  auto kern = attn_tile_kernel<D, BSUB, T, SPREAD>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -634,9 +789,14 @@ cudaError_t launch_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
 template <int D, typename T>
 cudaError_t launch_tc_bs(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int bsub,
                           cudaStream_t stream) {
+  // units of at most 32 rows: the rows are copied into every lane quarter
+  // and the softmax of a key tile is spread over all 8 softmax warps
+  const bool spread = p.fixed_q_len > 0 && p.fixed_q_len * p.group <= 32;
   switch (bsub) {
-    case 8: return launch_tc_t<D, 8, T>(kmap, vmap, p, stream);
-    case 16: return launch_tc_t<D, 16, T>(kmap, vmap, p, stream);
+    case 8: return spread ? launch_tc_t<D, 8, T, true>(kmap, vmap, p, stream)
+                          : launch_tc_t<D, 8, T, false>(kmap, vmap, p, stream);
+    case 16: return spread ? launch_tc_t<D, 16, T, true>(kmap, vmap, p, stream)
+                           : launch_tc_t<D, 16, T, false>(kmap, vmap, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
