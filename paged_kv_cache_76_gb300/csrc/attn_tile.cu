@@ -45,8 +45,9 @@
 //               quarter's window, so O of quarter q sums its keys only, with
 //               its own running maximum; the epilogue merges the four
 //               partial results (O = sum 2^(m_q - M) O_q / sum 2^(m_q - M)
-//               l_q) through shared memory.  The first half of P.V then
-//               takes the low 16 keys of every window.
+//               l_q) through shared memory (V stages 0 and 1, idle by then:
+//               the spread form runs one unit per CTA).  The first half of
+//               P.V takes the low 16 keys of every window.
 //   warp 8      issues S(j) = Q K_j^T into S(j % 2) (A from TMEM); owns TMEM
 //   warp 9      issues O += P(j) V_j (A from TMEM), in two 64-key halves
 //   warps 10,11 TMA producers of K (3-stage ring) and V (3 stages)
@@ -180,6 +181,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nunits = row_tiles * p.kv_heads * p.num_reqs;
   const int cta0 = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   const int nctas = gridDim.x * gridDim.y * gridDim.z;
+  // the spread form keeps its epilogue's partial outputs in V stages that
+  // the next unit's loads would overwrite: it takes one unit per CTA (the
+  // host launches it so)
+  if (SPREAD && nctas < nunits) {
+    if (threadIdx.x == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
+    return;
+  }
+
+  // the first unit >= u (in this CTA's stride) that has key tiles, or nunits
+  auto next_unit = [&](int u, TcUnit& w, bool report) -> int {
+    for (; u < nunits; u += nctas) {
+      if (!tc_unit(p, u, row_tiles, w)) {
+        if (report) {
+          griddep_wait();
+          if (lane == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
+        }
+        continue;
+      }
+      if (w.ntiles > 0) return u;
+    }
+    return nunits;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -213,21 +236,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   griddep_launch_dependents();
-
-  // the first unit >= u (in this CTA's stride) that has key tiles, or nunits
-  auto next_unit = [&](int u, TcUnit& w, bool report) -> int {
-    for (; u < nunits; u += nctas) {
-      if (!tc_unit(p, u, row_tiles, w)) {
-        if (report) {
-          griddep_wait();
-          if (lane == 0) record_error(p.err, PA_DEVERR_QUERY_RANGE);
-        }
-        continue;
-      }
-      if (w.ntiles > 0) return u;
-    }
-    return nunits;
-  };
 
   if (warp == kKWarp || warp == kVWarp) {
     // ---------------------------------------------------------------- producers
@@ -622,20 +630,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The four lane quarters hold partial results of the same rows over
         // disjoint keys, each relative to its own running maximum m_q:
         //   O = sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q,  M = max_q m_q.
-        // Quarters 1 and 3 put O_q into shared memory (the Q staging area,
-        // unused when spread), quarter 2 adds its scaled O_2 to quarter 3's,
-        // and quarter 0 adds the rest and writes the rows.  All 8 warps meet
-        // first in an AND vote that every exit of the unit passes through.
+        // Every warp puts its half of O_q (fp32) and its (m_q, l) into shared
+        // memory (the partial outputs in V stages 0 and 1, idle by now: a
+        // spread CTA has one unit and loads no further tile); after one AND
+        // vote of all 8 warps, which every exit of the unit passes through,
+        // the 256 threads merge and write 32 rows x D: thread t takes row
+        // t / 8 and the 16-byte chunks t % 8, t % 8 + 8, ... of it (8 threads
+        // per row: conflict-free shared-memory reads, 64-byte runs of output).
         float* mq = lsum;           // [4 quarters][32 rows] running maxima
         float* lq = lsum + 4 * 32;  // [4 quarters][2 key halves][32 rows] sums
         if (kh == 0) mq[quarter * 32 + lane] = m;
         lq[(quarter * 2 + kh) * 32 + lane] = l;
-        // 16-byte chunk c of this thread's half row in partial buffer pb, XOR-swizzled by row
-        auto part = [&](int pb, int c) {
-          return reinterpret_cast<float4*>(smem + L::Q_OFF + pb * (32 * D * 4) + lane * (D * 4)) +
-                 ((kh * (DH / 4) + c) ^ (lane & 7));
+        // 16-byte chunk ch of row r of quarter qq's partial, XOR-swizzled by row
+        auto part = [&](int qq, int r, int ch) {
+          return reinterpret_cast<float4*>(smem + L::V_OFF + qq * (32 * D * 4) + r * (D * 4)) + (ch ^ (r & 7));
         };
-        if (ok && (quarter & 1)) {
+        if (ok) {
 #pragma unroll
           for (int c = 0; c < DH / 32; ++c) {
             float ov[32];
@@ -643,63 +653,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              *part(quarter >> 1, 8 * c + i) = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+              *part(quarter, lane, kh * (DH / 4) + 8 * c + i) =
+                  make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
           }
         }
         if (!bar_red_and(5, 32 * kSoftmaxWarps, ok)) {
           ok = false;
           break;
         }
-        float f[4], mmax = -INFINITY, lt = 0.f;
+        const int t = threadIdx.x;  // 0..255: the softmax warps
+        const int r = t >> 3, c0 = t & 7;
+        if (w.row0 + r < w.rows) {
+          float f[4], mmax = -INFINITY, lt = 0.f;
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) mmax = fmaxf(mmax, mq[qq * 32 + lane]);
+          for (int qq = 0; qq < 4; ++qq) mmax = fmaxf(mmax, mq[qq * 32 + r]);
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const float mv = mq[qq * 32 + lane];
-          f[qq] = mv == -INFINITY ? 0.f : ex2_approx(mv - mmax);
-          lt += f[qq] * (lq[(qq * 2) * 32 + lane] + lq[(qq * 2 + 1) * 32 + lane]);
-        }
-        if (quarter == 2) {
-#pragma unroll
-          for (int c = 0; c < DH / 32; ++c) {
-            float ov[32];
-            tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4* a = part(1, 8 * c + i);
-              const float4 x = *a;
-              *a = make_float4(f[2] * ov[4 * i] + f[3] * x.x, f[2] * ov[4 * i + 1] + f[3] * x.y,
-                               f[2] * ov[4 * i + 2] + f[3] * x.z, f[2] * ov[4 * i + 3] + f[3] * x.w);
-            }
+          for (int qq = 0; qq < 4; ++qq) {
+            const float mv = mq[qq * 32 + r];
+            f[qq] = mv == -INFINITY ? 0.f : ex2_approx(mv - mmax);
+            lt += f[qq] * (lq[(qq * 2) * 32 + r] + lq[(qq * 2 + 1) * 32 + r]);
           }
-        }
-        if ((quarter & 1) == 0) asm volatile("bar.sync %0, %1;\n" ::"r"(6), "r"(128) : "memory");
-        if (quarter == 0 && wvalid) {
           const float inv = lt > 0.f ? 1.f / lt : 0.f;
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) +
-                                                ((size_t)(w.qs + qi) * p.q_heads + w.h * G + g) * D + kh * DH);
+          const int rr = w.row0 + r;
+          T* orow = reinterpret_cast<T*>(p.out) + ((size_t)(w.qs + rr / G) * p.q_heads + w.h * G + rr % G) * D;
 #pragma unroll
-          for (int c = 0; c < DH / 32; ++c) {
-            float ov[32];
-            tmem_ld32(tl + O_COL + kh * DH + 32 * c, ov);  // warp-collective: every lane loads, valid rows store
-            tmem_wait_ld();
-            if (valid) {
-              float o[32];
+          for (int i = 0; i < D / 32; ++i) {
+            const int ch = c0 + 8 * i;  // 16-byte chunk of the fp32 row = 4 output elements
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 x1 = *part(0, 8 * c + i), x3 = *part(1, 8 * c + i);
-                o[4 * i] = (f[0] * ov[4 * i] + f[1] * x1.x + x3.x) * inv;
-                o[4 * i + 1] = (f[0] * ov[4 * i + 1] + f[1] * x1.y + x3.y) * inv;
-                o[4 * i + 2] = (f[0] * ov[4 * i + 2] + f[1] * x1.z + x3.z) * inv;
-                o[4 * i + 3] = (f[0] * ov[4 * i + 3] + f[1] * x1.w + x3.w) * inv;
-              }
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[4 * c + q] = make_uint4(Elem<T>::pack(o[8 * q], o[8 * q + 1]), Elem<T>::pack(o[8 * q + 2], o[8 * q + 3]),
-                                            Elem<T>::pack(o[8 * q + 4], o[8 * q + 5]),
-                                            Elem<T>::pack(o[8 * q + 6], o[8 * q + 7]));
+            for (int qq = 0; qq < 4; ++qq) {
+              const float4 x = *part(qq, r, ch);
+              a.x += f[qq] * x.x, a.y += f[qq] * x.y, a.z += f[qq] * x.z, a.w += f[qq] * x.w;
             }
+            *reinterpret_cast<uint2*>(orow + 4 * ch) =
+                make_uint2(Elem<T>::pack(a.x * inv, a.y * inv), Elem<T>::pack(a.z * inv, a.w * inv));
           }
         }
       } else {
@@ -789,9 +776,11 @@ cudaError_t launch_tc_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
 template <int D, typename T>
 cudaError_t launch_tc_bs(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int bsub,
                           cudaStream_t stream) {
-  // units of at most 32 rows: the rows are copied into every lane quarter
-  // and the softmax of a key tile is spread over all 8 softmax warps
-  const bool spread = p.fixed_q_len > 0 && p.fixed_q_len * p.group <= 32;
+  // units of at most 32 rows, one per CTA: the rows are copied into every
+  // lane quarter and the softmax of a key tile is spread over all 8 softmax
+  // warps
+  const bool spread = p.fixed_q_len > 0 && p.fixed_q_len * p.group <= 32 &&
+                      (p.max_ctas <= 0 || (long long)p.max_ctas >= (long long)p.kv_heads * p.num_reqs);
   switch (bsub) {
     case 8: return spread ? launch_tc_t<D, 8, T, true>(kmap, vmap, p, stream)
                           : launch_tc_t<D, 8, T, false>(kmap, vmap, p, stream);
