@@ -92,15 +92,18 @@ VERIFY_TC = [
 ]
 
 
+@pytest.mark.parametrize("max_ctas", [0, 3], ids=["one_cta_per_unit", "capped_grid"])
 @pytest.mark.parametrize("case", VERIFY_TC, ids=[f"q{c[0]}_h{c[1]}x{c[2]}_d{c[3]}_{c[5]}" for c in VERIFY_TC])
-def test_verify_tensor_core(case):
+def test_verify_tensor_core(case, max_ctas):
+    # units of <= 32 rows: one CTA per unit runs the spread form, a capped
+    # grid the one-quarter form; both raise the maximum on nearly every tile
     q_len, hq, hkv, d, bs, dt, lens = case
     kc, vc, tables, g, dtype = _pool(22, lens, hkv, d, bs, dt)
     q = torch.randn(len(lens), q_len, hq, d, generator=g, device="cuda").to(dtype)
     scale = 1 / np.sqrt(d)
     out = torch.full_like(q, float("nan"))
     ops().verify_decode_tc(q, kc, vc, torch.from_numpy(tables).cuda(),
-                           torch.tensor(lens, dtype=torch.int32, device="cuda"), scale, out=out)
+                           torch.tensor(lens, dtype=torch.int32, device="cuda"), scale, out=out, max_ctas=max_ctas)
     _check(out, opa.verify_decode(to_f64(q), to_f64(kc), to_f64(vc), tables, lens, scale), f"verify tc {case}")
 
 

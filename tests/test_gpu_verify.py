@@ -182,13 +182,16 @@ TC_CASES = [c for c in VERIFY_CASES if c[4] >= 8 and (c[1] // c[2]) * c[0] <= 12
 ]
 
 
+@pytest.mark.parametrize("max_ctas", [0, 2], ids=["one_cta_per_unit", "capped_grid"])
 @pytest.mark.parametrize("case", TC_CASES, ids=[f"q{c[0]}_h{c[1]}x{c[2]}_d{c[3]}_bs{c[4]}_{c[5]}" for c in TC_CASES])
-def test_verify_tc_matches_the_oracle(case):
+def test_verify_tc_matches_the_oracle(case, max_ctas):
+    # <= 32 rows: the spread form (one CTA per unit) and the one-quarter form
+    # (a capped grid, several units per CTA)
     q_len, hq, hkv, d, bs, dt, lens, _ = case
     q, kc, vc, tables, lens_t = _case(7, q_len, hq, hkv, d, bs, dt, lens)
     scale = 1 / np.sqrt(d)
     out = torch.full_like(q, float("nan"))
-    ops().verify_decode_tc(q, kc, vc, tables, lens_t, scale, out=out)
+    ops().verify_decode_tc(q, kc, vc, tables, lens_t, scale, out=out, max_ctas=max_ctas)
     ref = opa.verify_decode(to_f64(q), to_f64(kc), to_f64(vc), tables.cpu().numpy(), lens, scale)
     assert_close(out, ref, f"verify tc {case}")
     for r, L in enumerate(lens):
