@@ -4,40 +4,50 @@
 //
 // A CTA owns two tiles of 128 rows (A and B) of one (request, KV head); a row
 // is one (query, head of the GQA group) pair, so the whole group shares every
-// K/V tile, and each 128-key K/V tile gathered from the paged cache serves
-// 256 rows.
+// K/V tile, and each 64-key K/V tile gathered from the paged cache serves 256
+// rows.
+//
+// Tensor memory (512 columns, one CTA per SM):
+//
+//   S_x buffer b  [(2x + b) * 64, +64)   S = Q_x K^T of key tiles j = b mod 2 (fp32);
+//                                        P_x(j) over its first 32 columns (two per column)
+//   O_A, O_B      [256, 384), [384, 512) fp32 accumulators, 128 rows x D
 //
 // Design points, each measured on GB300:
-//  * S = Q K^T uses N = 128 keys per instruction: at N = 64 an SS MMA is bound
-//    by its 6 KB of shared-memory operand reads and runs at 2/3 rate.
+//  * Two S buffers per Q tile break the chain S_x(j) -> softmax -> P.V_x(j)
+//    -> S_x(j+1): S_x(j) overwrites only P_x(j-2), so it is issued while the
+//    softmax still works on tile j-1.  Two of them fit beside both O
+//    accumulators only at 64 keys per tile, where an SS MMA is bound by its
+//    6 KB of shared-memory operand reads (2/3 rate); the kernel still gains,
+//    because the 128-key form spent most of each tile waiting on its chain.
 //  * P stays in tensor memory: the softmax writes P (bf16/fp16) over the
 //    first half of its S columns and O += P V reads A from TMEM, so P never
-//    crosses shared memory (about a quarter of the per-tile SMEM traffic).
-//  * Two producer warps (K and V) issue the TMA gather: one warp issuing
-//    16-row boxes moves about 27 B/clk per SM, more than the 256 rows of a
-//    K/V tile need at this kernel's period.
-//  * The softmax holds its whole S row in registers (one TMEM round trip per
-//    tile).
+//    crosses shared memory.
+//  * The softmax warps never issue MMAs and do not meet per tile: each warp
+//    waits for its S buffer on its own and signals its part of P on an
+//    mbarrier, so no warp waits for another's MMA issue.
+//  * The softmax holds its S row in registers (one TMEM round trip per tile).
 //
 // Warp roles (384 threads = 12 warps, so that each thread may hold 168
-// registers; one CTA per SM):
-//   warps 0,1   S issuers, one warp per Q tile x (one elected lane issues,
+// registers):
+//   warps 0,1   MMA issuers, one warp per Q tile x (one elected lane issues,
 //               with warp-uniform descriptors): per key tile j,
-//                 S_x(j) = Q_x K_j^T
-//               S_x(j) overwrites P_x(j-1), so it is issued once P.V_x(j-1)
-//               has completed.  The two issuers wait only on their own tile;
-//               the tensor pipe interleaves their MMAs.
-//   warp 2      TMA producer of K, warp 3 of V; separate K (3-stage) and V
-//               (2-stage) rings, so a K slot frees as soon as both S MMAs have
-//               read it.
+//                 S_x(j) = Q_x K_j^T into buffer j % 2, once P.V_x(j-2) has
+//                 completed (the tcgen05 ordering guarantee covers only MMAs
+//                 into the same accumulator), then
+//                 O_x += P_x(j-1) V_{j-1}, once the tile's four softmax warps
+//                 have written P_x(j-1).
+//               The two issuers wait only on their own tile; the tensor pipe
+//               interleaves their MMAs.
+//   warp 2      TMA producer of K, warp 3 of V; separate 4-stage rings, so a
+//               K slot frees as soon as both S MMAs have read it.
 //   warps 4..7  softmax of tile A, warps 8..11 of tile B: thread = TMEM lane
 //               = row.  It loads its S row, takes the row maximum, writes
-//               P = 2^(s*scale*log2e - m) into TMEM and sums it; after each
-//               half of P the group meets at a named barrier and its first
-//               warp issues O_x += P_x(j) V_j for that half.  The running
+//               P = 2^(s*scale*log2e - m) into TMEM and sums it.  The running
 //               maximum m is raised only when a row maximum exceeds it by
-//               more than 2^8 (O is then rescaled in TMEM); the final O / sum
-//               uses the same m, so this is exact.
+//               more than 2^8 (O is then rescaled in TMEM, once P.V_x(j-1)
+//               has completed); the final O / sum uses the same m, so this is
+//               exact.
 // Q and K are K-major and V is MN-major in the canonical 128-byte-swizzled
 // shared-memory layouts.  Every mbarrier wait is bounded.
 #include <float.h>
@@ -50,12 +60,11 @@ namespace pa {
 namespace {
 
 constexpr int kRows = 128;  // rows per Q tile (M of every MMA)
-constexpr int kKeys = 128;  // keys per K/V tile (N of S, K of P.V)
-// K ring 3 deep: K(j) is on the critical path (S_A(j) waits for it) and a
-// gathered tile lands a few microseconds after its slot frees; V is needed
-// later (P.V) and gets 2 stages.  Head_dim 128: 64 + 96 + 64 KB of smem.
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
+constexpr int kKeys = 64;   // keys per K/V tile (N of S, K of P.V)
+// 4 K and 4 V stages of 64-key tiles (head_dim 128: Q 64 KB + K 64 KB + V 64
+// KB of shared memory); 5 of either measured slower.
+constexpr int kKStages = 4;
+constexpr int kVStages = 4;
 constexpr int kMmaWarp = 0;  // warps 0, 1: MMA issuers of Q tiles A, B (warp 0 owns TMEM)
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kKWarp = 2;
@@ -78,7 +87,7 @@ struct TcSmem {
   static constexpr int K_OFF = Q_OFF + 2 * QTILE;
   static constexpr int V_OFF = K_OFF + kKStages * Tile::BYTES;
   static constexpr int BAR_OFF = V_OFF + kVStages * Tile::BYTES;
-  static constexpr int NBARS = 2 * kKStages + 2 * kVStages + 11;
+  static constexpr int NBARS = 2 * kKStages + 2 * kVStages + 15;
   static constexpr int SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int BYTES = SLOT_OFF + 16 + 1024;
   static_assert(BSUB * 128 >= 1024, "needs blocks of at least 8 tokens (one 8-row swizzle atom per box)");
@@ -91,13 +100,12 @@ constexpr int B_KFULL = 0;                     // [kKStages] the K producer warp
 constexpr int B_KEMPTY = B_KFULL + kKStages;   // [kKStages] one tcgen05.commit per issuer after S_x(j)
 constexpr int B_VFULL = B_KEMPTY + kKStages;   // [kVStages] the V producer warp arrives (+ TMA bytes)
 constexpr int B_VEMPTY = B_VFULL + kVStages;   // [kVStages] one tcgen05.commit per issuer after P.V_x(j)
-constexpr int B_SFULL = B_VEMPTY + kVStages;   // [2] per Q tile
-constexpr int B_PLO = B_SFULL + 2;             // [2] P_x keys 0..63 in TMEM (four softmax warps)
-constexpr int B_PHI = B_PLO + 2;               // [2] P_x keys 64..127
-constexpr int B_OFULL = B_PHI + 2;             // [2] P.V_x(j) complete
-constexpr int B_QFULL = B_OFULL + 2;            // [2] Q_x of the next work unit in smem (four softmax warps)
+constexpr int B_SFULL = B_VEMPTY + kVStages;   // [2 Q tiles][2 S buffers] S_x(j) written (commit)
+constexpr int B_PFULL = B_SFULL + 4;           // [2 Q tiles][2 S buffers] P_x(j) in TMEM (four softmax warps)
+constexpr int B_OFULL = B_PFULL + 4;           // [2 Q tiles][2 S buffers] P.V_x(j) complete (commit)
+constexpr int B_QFULL = B_OFULL + 4;            // [2] Q_x of the next work unit in smem (four softmax warps)
 constexpr int B_MMADONE = B_QFULL + 2;
-static_assert(B_MMADONE + 1 == 2 * kKStages + 2 * kVStages + 11, "barrier count");
+static_assert(B_MMADONE + 1 == 2 * kKStages + 2 * kVStages + 15, "barrier count");
 
 // One work unit: a tile of 2 x 128 rows of one (request, KV head) for the
 // causal prefill, or of one (prefix key range, KV head) for the shared-prefix
@@ -160,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int KSTEPS = D / 16;      // S = Q K^T: K dimension = head_dim
   constexpr int PSTEPS = kKeys / 16;  // O = P V:   K dimension = keys
   constexpr int SUBS = kKeys / BSUB;  // boxes per half per tile
-  constexpr uint32_t S_COL = 0;       // S_A, S_B: kKeys columns each; P_x in the first kKeys/2
-  constexpr uint32_t O_COL = 2 * kKeys;
+  constexpr uint32_t S_COL = 0;       // S_x buffer b at (2x + b) * kKeys; P_x(j) in the first kKeys/2 of its buffer
+  constexpr uint32_t O_COL = 4 * kKeys;
   constexpr uint32_t IDESC_S = idesc_f16<T>(kRows, kKeys, false);
   constexpr uint32_t IDESC_O = idesc_f16<T>(kRows, D, true);
 
@@ -188,15 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_VFULL + i), 1);
       mbar_init(bar(B_VEMPTY + i), 2);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(B_SFULL + x), 1);
-      mbar_init(bar(B_PLO + x), 4);
-      mbar_init(bar(B_PHI + x), 4);
-      mbar_init(bar(B_OFULL + x), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_PFULL + i), 4);
+      mbar_init(bar(B_OFULL + i), 1);
     }
     mbar_init(bar(B_QFULL), 4);
     mbar_init(bar(B_QFULL + 1), 4);
-    mbar_init(bar(B_MMADONE), 4);  // two S issuers + two softmax groups (P.V)
+    mbar_init(bar(B_MMADONE), 2);  // the two MMA issuers' last commits
     fence_mbar_init();
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
@@ -268,8 +275,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t kbase = smem_u32(smem + L::K_OFF);
       const uint32_t qa = smem_u32(smem + L::Q_OFF + x * L::QTILE);
-      const uint32_t sd = tmem + S_COL + x * kKeys;
+      const uint32_t sd = tmem + S_COL + 2 * x * kKeys;
+      const uint32_t vbase = smem_u32(smem + L::V_OFF);
+      const uint32_t od0 = tmem + O_COL + x * D;
       int gt = 0, nu = 0;  // key tiles and units processed by this CTA
+      // O_x += P_x(t) V_t once the four softmax warps have written P_x(t)
+      // (jt: the tile's index in its unit; its first P.V overwrites O_x)
+      auto issue_pv = [&](int t, int jt) -> bool {
+        const int pb = t & 1, vst = t % kVStages;
+        if (!__all_sync(kAll, mbar_wait(bar(B_PFULL + 2 * x + pb), (t >> 1) & 1) &&
+                                  mbar_wait(bar(B_VFULL + vst), (t / kVStages) & 1)))
+          return false;
+        tc_fence_after();
+        const uint32_t vb = vbase + vst * Tile::BYTES;
+#pragma unroll
+        for (int kk = 0; kk < PSTEPS; ++kk) {
+          // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
+          const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
+          tc_mma_f16_ts_warp(od0, sd + pb * kKeys + kk * 8, bd, IDESC_O, (jt > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit_warp(bar(B_OFULL + 2 * x + pb));
+        tc_commit_warp(bar(B_VEMPTY + vst));  // this issuer is done with V_t
+        return true;
+      };
       for (int u = cta0; ok && u < nunits; u += nctas) {
         TcUnit w;
         if (!tc_unit(p, u, row_tiles, w)) {
@@ -285,25 +313,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(kAll, mbar_wait(bar(B_QFULL + x), nu & 1))) { ok = false; break; }
         // Tile B starts half a key tile behind tile A (once P_A(0) is being
         // written), so that the two softmaxes alternate instead of overlapping.
-        if (x == 1 && nu == 0 && !__all_sync(kAll, mbar_wait(bar(B_PLO), 0))) { ok = false; break; }
+        if (x == 1 && nu == 0 && !__all_sync(kAll, mbar_wait(bar(B_PFULL), 0))) { ok = false; break; }
         ++nu;
         for (int j = 0; ok && j < w.ntiles; ++j, ++gt) {
-          const int sk = gt % kKStages;
-          // S_x(j) = Q_x K_j^T.  It overwrites P_x(j-1): wait for P.V_x(j-1).
+          const int sk = gt % kKStages, b = gt & 1;
+          // S_x(j) = Q_x K_j^T into buffer b.  It overwrites P_x(j-2): wait for P.V_x(j-2).
           if (!__all_sync(kAll, mbar_wait(bar(B_KFULL + sk), (gt / kKStages) & 1))) { ok = false; break; }
-          if (j > 0 && !__all_sync(kAll, mbar_wait(bar(B_OFULL + x), (gt - 1) & 1))) { ok = false; break; }
+          if (gt >= 2 && !__all_sync(kAll, mbar_wait(bar(B_OFULL + 2 * x + b), ((gt - 2) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t kb = kbase + sk * Tile::BYTES;
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             const uint64_t ad = smem_desc_sw128(qa + (ks >> 2) * L::QHALF + (ks & 3) * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * Tile::HALF + (ks & 3) * 32, 16, 1024);
-            tc_mma_f16_warp(sd, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
+            tc_mma_f16_warp(sd + b * kKeys, ad, bd, IDESC_S, ks > 0 ? 1u : 0u);
           }
-          tc_commit_warp(bar(B_SFULL + x));
+          tc_commit_warp(bar(B_SFULL + 2 * x + b));
           tc_commit_warp(bar(B_KEMPTY + sk));  // this issuer is done with K_j
-          // O_x += P_x(j) V_j is issued by tile x's softmax group itself
+          // P.V of the previous tile, behind S(j) so that S(j) does not wait for it
+          if (j > 0 && !issue_pv(gt - 1, j - 1)) {
+            ok = false;
+            break;
+          }
         }
+        if (ok && !issue_pv(gt - 1, w.ntiles - 1)) ok = false;  // the unit's last P.V
       }
       if (!ok && lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT);
       tc_commit_warp(bar(B_MMADONE));
@@ -316,17 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     constexpr float kRescale = 8.f;
-    const uint32_t scol = tmem + lane_addr + S_COL + x * kKeys;
+    const uint32_t scol0 = tmem + lane_addr + S_COL + 2 * x * kKeys;
     const uint32_t ocol = tmem + lane_addr + O_COL + x * D;
     uint8_t* qt = smem + L::Q_OFF + x * L::QTILE;
-    // The group's first warp issues the group's P.V MMAs (one elected lane,
-    // warp-uniform operands): the named barrier 1 + x (the group's 128
-    // threads, with an AND vote that keeps every exit uniform) replaces a
-    // hand-off to another warp.
-    const bool leader = quarter == 0;
-    const uint32_t sd0 = tmem + S_COL + x * kKeys, od0 = tmem + O_COL + x * D;
-    const uint32_t vbase = smem_u32(smem + L::V_OFF);
-    bool lok = true;  // leader warp: every V wait succeeded
     bool ok = true;
     int gt = 0;  // key tiles processed by this CTA
     for (int u = cta0; ok && u < nunits; u += nctas) {
@@ -354,8 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float m = -INFINITY, l = 0.f;  // running (possibly stale) max in log2 units, row sum
       for (int j = 0; j < w.ntiles; ++j, ++gt) {
-        const bool sfull = mbar_wait(bar(B_SFULL + x), gt & 1);
-        if (!bar_red_and(1 + x, 128, sfull)) { ok = false; break; }  // the group stops together
+        const int sb = gt & 1;  // S buffer of this tile
+        const uint32_t scol = scol0 + sb * kKeys;
+        // each warp waits on its own (S is double-buffered: no group meeting per tile)
+        if (!__all_sync(kAll, mbar_wait(bar(B_SFULL + 2 * x + sb), (gt >> 1) & 1))) { ok = false; break; }
         tc_fence_after();
         const int ts = w.k0 + j * kKeys;
         const int nvis = lim - ts + 1;  // keys of this tile the row may see (<= 0: none)
@@ -391,97 +421,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float neg_m = m == -INFINITY ? 0.f : -m;
 
         // P = 2^(s*sl2 - m) (masked keys hold -inf: p = 0), written over the
-        // first kKeys/2 S columns in two halves of 64 keys; each half is
-        // signalled on its own so that P.V can start on the first.  The sum
-        // runs in four packed-pair chains.
+        // first kKeys/2 columns of this tile's S buffer, 32 keys at a time;
+        // the sum runs in four packed-pair chains
         float sx[4] = {0.f, 0.f, 0.f, 0.f}, sy[4] = {0.f, 0.f, 0.f, 0.f};
         const int nvalid = min(kKeys, w.kend - ts);
         bool vok = true;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int c = 0; c < kKeys / 32; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int cc = 0; cc < kKeys / 64; ++cc) {
-            const int c = hh * (kKeys / 64) + cc;
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float a0, a1;
-              ffma2(a0, a1, sv[32 * c + e], sv[32 * c + e + 1], sl2, sl2, neg_m, neg_m);
-              const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
-              const int k = (e >> 1) & 3;
-              fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
-              pk[e >> 1] = Elem<T>::pack(p0v, p1v);
-            }
-            tmem_st16u(scol + 16 * c, pk);  // keys 32c..32c+31 -> columns 16c..16c+15
+          for (int e = 0; e < 32; e += 2) {
+            float a0, a1;
+            ffma2(a0, a1, sv[32 * c + e], sv[32 * c + e + 1], sl2, sl2, neg_m, neg_m);
+            const float p0v = ex2_approx(a0), p1v = ex2_approx(a1);
+            const int k = (e >> 1) & 3;
+            fadd2(sx[k], sy[k], sx[k], sy[k], p0v, p1v);
+            pk[e >> 1] = Elem<T>::pack(p0v, p1v);
           }
-          if (hh == 0) {
-            if (rescale) {
-              // rescale O_x in TMEM before P.V_x(j) starts (warp-collective).
-              // P.V_x(j-1) has completed: S_x(j) was issued after it.
+          tmem_st16u(scol + 16 * c, pk);  // keys 32c..32c+31 -> columns 16c..16c+15
+        }
+        if (rescale) {
+          // rescale O_x in TMEM before P.V_x(j) starts (warp-collective),
+          // once P.V_x(j-1) has completed (S_x(j) waited only for
+          // P.V_x(j-2)); a rescale needs a finite reference, so j >= 1
+          if (!mbar_wait(bar(B_OFULL + 2 * x + ((gt - 1) & 1)), ((gt - 1) >> 1) & 1)) vok = false;
+          tc_fence_after();
 #pragma unroll
-              for (int c = 0; c < D / 16; ++c) {
-                float ov[16];
-                tmem_ld16(ocol + 16 * c, ov);
-                tmem_wait_ld();
+          for (int c = 0; c < D / 16; ++c) {
+            float ov[16];
+            tmem_ld16(ocol + 16 * c, ov);
+            tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) ov[e] *= alpha;
-                tmem_st16u(ocol + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(ov));
-              }
-            }
-            if (nvalid < kKeys) {
-              // last key tile: keys past kend came from stale slots (or were
-              // not loaded); zero their V rows so that p = 0 never meets
-              // NaN/Inf.  Both Q tiles' softmax warps write the same zeros
-              // (either P.V may run first); each P.V starts only after its own
-              // group's.
-              const int s = gt % kVStages;
-              if (!mbar_wait(bar(B_VFULL + s), (gt / kVStages) & 1)) {
-                vok = false;
-              } else if (row >= nvalid) {
-                uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
-#pragma unroll
-                for (int hf = 0; hf < NH; ++hf)
-#pragma unroll
-                  for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(vrow + hf * Tile::HALF + c * 16) = make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_smem();
-            }
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar((hh ? B_PHI : B_PLO) + x));
-          // all 128 rows of P_x(j) half hh are in TMEM (and any V rows past the
-          // keys zeroed): the leader issues O_x += P_x(j)[half hh] V_j
-          if (!bar_red_and(1 + x, 128, vok)) {
-            ok = false;
-            break;
-          }
-          if (leader) {
-            tc_fence_after();
-            const int vst = gt % kVStages;
-            if (hh == 0 && lok) lok = __all_sync(kAll, mbar_wait(bar(B_VFULL + vst), (gt / kVStages) & 1));
-            if (lok) {  // else S_x(j+1) never comes and the group stops at its next vote
-              const uint32_t vb = vbase + vst * Tile::BYTES;
-#pragma unroll
-              for (int k4 = 0; k4 < PSTEPS / 2; ++k4) {
-                // A = P_x[128 rows x keys 16kk..16kk+15] in TMEM (8 columns); B = V rows 16kk.., MN-major
-                const int kk = hh * (PSTEPS / 2) + k4;
-                const uint64_t bd = smem_desc_sw128(vb + kk * 2048, Tile::HALF, 1024);
-                tc_mma_f16_ts_warp(od0, sd0 + kk * 8, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-              }
-              if (hh == 1) {
-                tc_commit_warp(bar(B_OFULL + x));
-                tc_commit_warp(bar(B_VEMPTY + vst));  // this group is done with V_j
-              }
-            }
+            for (int e = 0; e < 16; ++e) ov[e] *= alpha;
+            tmem_st16u(ocol + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(ov));
           }
         }
+        if (nvalid < kKeys) {
+          // last key tile: keys past kend came from stale slots (or were
+          // not loaded); zero their V rows so that p = 0 never meets
+          // NaN/Inf.  Both Q tiles' softmax warps write the same zeros
+          // (either P.V may run first); each P.V starts only after its own
+          // group's.
+          const int s = gt % kVStages;
+          if (!mbar_wait(bar(B_VFULL + s), (gt / kVStages) & 1)) {
+            vok = false;
+          } else if (row >= nvalid && row < kKeys) {
+            uint8_t* vrow = smem + L::V_OFF + s * Tile::BYTES + row * 128;
+#pragma unroll
+            for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(vrow + hf * Tile::HALF + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        // P_x(j), any rescale of O_x and any V rows past the keys are this
+        // warp's share of what the Q tile's MMA warp waits for before
+        // P.V_x(j); one barrier per (Q tile, S buffer), so that arrivals for
+        // tile j+1 never land in tile j's phase
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL + 2 * x + sb));
+        if (!vok) ok = false;
         l += ((sx[0] + sy[0]) + (sx[1] + sy[1])) + ((sx[2] + sy[2]) + (sx[3] + sy[3]));
         if (!ok) break;
       }
-      const bool ofull = ok && mbar_wait(bar(B_OFULL + x), (gt - 1) & 1);  // the unit's last P.V_x
+      const bool ofull = ok && mbar_wait(bar(B_OFULL + 2 * x + ((gt - 1) & 1)), ((gt - 1) >> 1) & 1);  // the unit's last P.V_x
       ok = bar_red_and(1 + x, 128, ofull);
       if (!ok) break;
       tc_fence_after();
@@ -525,8 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();  // O_x read out before the next unit's P.V overwrites it
     }
-    if (lane == 0 && (!ok || (leader && !lok))) record_error(p.err, PA_DEVERR_TIMEOUT);
-    if (leader) tc_commit_warp(bar(B_MMADONE));  // this group's P.V MMAs have completed
+    if (lane == 0 && !ok) record_error(p.err, PA_DEVERR_TIMEOUT);
   }
 
   // ------------------------------------------------------------------ teardown
