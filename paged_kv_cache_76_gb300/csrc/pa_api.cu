@@ -207,14 +207,16 @@ int sm_count() {
 
 // Key range of a prefix pass that runs beside the suffix pass: 512 x 2^k
 // tokens, the smallest whose units (pairs of 128-row tiles x KV heads x
-// ranges) fit in half of the SMs.  Measured on GB300 (256 requests, 2048-token
-// prefix, 32/8 heads): 512-token ranges (128 CTAs) 78.1 us per step, 1024
-// (64 CTAs) 69.4 us, 2048 (32 CTAs) 76.5 us; all on one stream: 79.0 us.
+// ranges) fit in a quarter of the SMs: the suffix pass is bound by the bytes
+// each SM keeps in flight, so the SMs it keeps matter more than how soon the
+// prefix pass ends.  Measured on GB300 (256 requests, 2048-token prefix, 32/8
+// heads), shared-prefix call: 512-token ranges (128 CTAs) 73.1 us, 1024 (64
+// CTAs) 65.5 us, 2048 (32 CTAs) 62.0 us.
 int concurrent_key_split(int num_seqs, int group, int kv_heads, int prefix_len) {
   const int64_t row_pairs = ((int64_t)num_seqs * group + 255) / 256;
-  const int64_t half = sm_count() / 2;
+  const int64_t quarter = sm_count() / 4;
   int ks = kPrefixKeySplit;
-  while (ks < prefix_len && row_pairs * kv_heads * ((prefix_len + ks - 1) / ks) > half) ks *= 2;
+  while (ks < prefix_len && row_pairs * kv_heads * ((prefix_len + ks - 1) / ks) > quarter) ks *= 2;
   return ks;
 }
 
