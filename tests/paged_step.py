@@ -17,12 +17,13 @@ import workloads as W
 from oracle import paged_attention as opa
 from oracle.block_pool import SequenceManager
 
-TOL_MAX = 1e-2    # max-abs error vs the float64 oracle, besides the output's own rounding
+TOL_MAX = 1e-2    # max-abs error vs the float64 oracle
 TOL_MEAN = 1e-3   # mean-abs error vs the float64 oracle
 # The output is stored once in the input type (round to nearest even): half
 # an ulp, at most 2^-8 |x| in bf16 (8 significant bits) and 2^-11 |x| in fp16.
-# It matters where a row's softmax is nearly one-hot and the output is a V
-# row of magnitude ~4; averages over many keys stay far smaller.
+# It matters only where a row's softmax is nearly one-hot and the output is a
+# V row of magnitude ~4 (inputs built for that: assert_close(..., rounding=True));
+# averages over many keys stay far below 1e-2 with it or without it.
 OUT_ROUNDING = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11, torch.float32: 0.0}
 
 
@@ -162,12 +163,14 @@ class DeviceStep:
                    out=self.out_decode, split_tokens=self.split_tokens, workspace=self.workspace, stream=stream)
 
 
-def assert_close(got: torch.Tensor, ref: np.ndarray, what=""):
+def assert_close(got: torch.Tensor, ref: np.ndarray, what="", rounding=False):
+    """max-abs <= TOL_MAX and mean-abs <= TOL_MEAN against the oracle; with
+    ``rounding``, the max-abs bound also admits the output's own rounding."""
     g = to_f64(got)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - ref)
-    excess = err - OUT_ROUNDING[got.dtype] * np.abs(ref)
-    assert excess.max() <= TOL_MAX, f"{what}: max-abs {err.max():.3g} (beyond the output rounding " \
+    excess = err - (OUT_ROUNDING[got.dtype] * np.abs(ref) if rounding else 0.0)
+    assert excess.max() <= TOL_MAX, f"{what}: max-abs {err.max():.3g} (beyond the allowed rounding " \
                                     f"{excess.max():.3g}) > {TOL_MAX}"
     assert err.mean() <= TOL_MEAN, f"{what}: mean-abs {err.mean():.3g} > {TOL_MEAN}"
     return float(err.max()), float(err.mean())

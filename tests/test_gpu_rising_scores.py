@@ -65,8 +65,11 @@ def _pool(seed, lens, hkv, d, bs, dt, shared_blocks=0):
 
 
 def _check(out, ref, what):
+    # a nearly one-hot softmax makes the output a V row of magnitude up to
+    # ~4.5, whose own rounding to bf16 is up to 2^-8 of it (0.018): the
+    # bound admits that rounding on top of 1e-2
     torch.cuda.synchronize()
-    assert_close(out, ref, what)
+    assert_close(out, ref, what, rounding=True)
     assert ops().get_device_error() == 0
 
 

@@ -216,9 +216,12 @@ def test_verify_tc_persistent_grid_matches_one_cta_per_unit_and_the_mma_form(q_l
     if q_len * hq // hkv > 32:
         assert torch.equal(a, b)
     else:
+        # contexts of 1 to 17 tokens leave some queries a softmax over a few
+        # keys, whose output is close to a V row of magnitude up to ~4: the
+        # bound admits the output's own rounding to bf16 on top of 1e-2
         ref = opa.verify_decode(to_f64(q), to_f64(kc), to_f64(vc), tables.cpu().numpy(), lens, scale)
-        assert_close(a, ref, "one CTA per unit")
-        assert_close(b, ref, "capped grid")
+        assert_close(a, ref, "one CTA per unit", rounding=True)
+        assert_close(b, ref, "capped grid", rounding=True)
     if q_len * hq // hkv <= 32:  # the warp-MMA form takes up to 32 columns
         m = ops().verify_decode(q, kc, vc, tables, lens_t, scale)
         err = (to_f64(a) - to_f64(m))
