@@ -256,6 +256,9 @@ int pa_verify_decode(const void* q, const void* k_cache, const void* v_cache, co
  *   block_size    8, 16 or 32 (the gather's boxes hold 8-row swizzle atoms)
  *   max_ctas      0: one CTA per unit; > 0: that many CTAs, each taking units
  *                 b, b + max_ctas, ... (one CTA per SM fits)
+ * With one CTA per unit, units of at most 32 rows are spread over all four
+ * tensor-memory lane quarters (each takes a quarter of every key tile; the
+ * four partial results are merged exactly); a capped grid keeps them in one.
  * Results equal pa_verify_decode's within the attention tolerance (the sums
  * are taken in another order); a query that sees no token gives a zero row.
  * Errors as pa_chunked_prefill.
