@@ -395,7 +395,7 @@ int pa_vkv_reshape_and_cache(const pa_vkv* v, int layer, const void* k, const vo
  *                  write of q, prefix_blocks and the prefix's K/V, and after
  *                  every earlier use of the workspace.  In this mode the
  *                  prefix key ranges grow (512 x 2^k tokens) until the prefix
- *                  pass needs at most half of the SMs.
+ *                  pass needs at most a quarter of the SMs.
  * Other arguments as pa_decode.  With 4-token blocks this is pa_decode (on
  * `stream`).
  * ------------------------------------------------------------------------- */
