@@ -109,8 +109,9 @@ static_assert(B_MMADONE + 1 == 2 * kKStages + 2 * kVStages + 15, "barrier count"
 
 // One work unit: a tile of 2 x 128 rows of one (request, KV head) for the
 // causal prefill, or of one (prefix key range, KV head) for the shared-prefix
-// pass.  Units are numbered z-major, then head, then row tile in reverse (the
-// last row tiles of a causal chunk see the most keys, so they come first).
+// pass.  Units are numbered z-major, then row tile in reverse, then head: the
+// last row tiles of a causal chunk see the most keys, so dispatch in index
+// order starts the longest units of every head first.
 struct TcUnit {
   int z, h, row0, r, qs, chunk, p0, k0, kend, rows, ntiles;
 };
@@ -121,8 +122,9 @@ __device__ __forceinline__ bool tc_unit(const PrefillParams& p, int u, int row_t
   const int per_z = row_tiles * p.kv_heads;
   w.z = u / per_z;
   const int rem = u - w.z * per_z;
-  w.h = rem / row_tiles;
-  w.row0 = (row_tiles - 1 - (rem - w.h * row_tiles)) * 2 * kRows;
+  const int rt = rem / p.kv_heads;
+  w.h = rem - rt * p.kv_heads;
+  w.row0 = (row_tiles - 1 - rt) * 2 * kRows;
   w.ntiles = 0;
   const int G = p.group;
   if (p.causal) {
